@@ -1,0 +1,102 @@
+"""Seeded synthetic workloads shared by the tests, the smoke check and the bench.
+
+This module holds no attention arithmetic: it only names the workloads and
+draws their inputs.  Q, K and V are drawn in that order from a seeded CPU
+``torch.Generator`` as float32 N(0, 1) samples and then rounded to the
+workload's dtype, so the CUDA path and the CPU oracle see identical values.
+"""
+from dataclasses import dataclass, replace
+import math
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Sq: int
+    Skv: int
+    D: int
+    dtype: str          # "f16" or "bf16"
+    causal: bool
+    input_pos: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def torch_dtype(self):
+        return torch.float16 if self.dtype == "f16" else torch.bfloat16
+
+    def flops(self) -> float:
+        """4*B*Hq*Sq*Skv*D, halved for causal (the reported convention)."""
+        f = 4.0 * self.B * self.Hq * self.Sq * self.Skv * self.D
+        return f / 2 if self.causal else f
+
+    def visible_pairs(self) -> int:
+        """Exact number of (query, key) pairs the mask keeps."""
+        if not self.causal:
+            return self.B * self.Hq * self.Sq * self.Skv
+        total = 0
+        for i in range(self.Sq):
+            total += min(self.Skv, self.input_pos + i + 1)
+        return self.B * self.Hq * total
+
+    def exact_flops(self) -> float:
+        """4*D flops per visible score (QK^T and PV, 2*D each)."""
+        return 4.0 * self.D * self.visible_pairs()
+
+    def io_bytes(self) -> int:
+        """Q, K, V read once; O written once; LSE written once (fp32)."""
+        e = 2
+        q = self.B * self.Hq * self.Sq * self.D * e
+        kv = 2 * self.B * self.Hkv * self.Skv * self.D * e
+        return 2 * q + kv + 4 * self.B * self.Hq * self.Sq
+
+    def with_(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+
+# The pages' workload shapes (see the design doc for the list and its sources).
+SMALL = Workload("small_B1_H2_S128_D64_f16", 1, 2, 2, 128, 128, 64, "f16", False)
+MHA_4K = Workload("mha_B1_H32_S4096_D128_f16_causal", 1, 32, 32, 4096, 4096,
+                  128, "f16", True)
+GQA_8K = Workload("gqa_B1_Hq32_Hkv4_S8192_D128_bf16_causal", 1, 32, 4, 8192,
+                  8192, 128, "bf16", True)
+PREFILL_CHUNK = Workload("prefill_B8_Hq32_Hkv8_Sq512_pos3584_Skv4096_D128_bf16",
+                         8, 32, 8, 512, 4096, 128, "bf16", True, 3584)
+
+
+def sweep():
+    """B=4, H=16 non-causal sweep over S, D and dtype."""
+    out = []
+    for S in (1024, 2048, 4096, 8192):
+        for D in (64, 128):
+            for dt in ("f16", "bf16"):
+                out.append(Workload("sweep_B4_H16_S%d_D%d_%s" % (S, D, dt),
+                                    4, 16, 16, S, S, D, dt, False))
+    return out
+
+
+ALL = [SMALL, MHA_4K, GQA_8K, PREFILL_CHUNK] + sweep()
+
+
+def make_qkv(w: Workload, seed: int = 0, device="cpu"):
+    """Draw Q, K, V for workload ``w`` (in that order) and round to its dtype.
+
+    Layouts: Q [B, Hq, Sq, D]; K, V [B, Hkv, Skv, D]; contiguous.
+    """
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    q = torch.randn((w.B, w.Hq, w.Sq, w.D), generator=g, dtype=torch.float32)
+    k = torch.randn((w.B, w.Hkv, w.Skv, w.D), generator=g, dtype=torch.float32)
+    v = torch.randn((w.B, w.Hkv, w.Skv, w.D), generator=g, dtype=torch.float32)
+    dt = w.torch_dtype
+    q, k, v = q.to(dt), k.to(dt), v.to(dt)
+    if device != "cpu":
+        q, k, v = q.to(device), k.to(device), v.to(device)
+    return q, k, v

@@ -1,0 +1,132 @@
+"""fp64 CPU oracle for attention forward — TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product (the CUDA library and its
+Python binding) never imports it, and it imports nothing from the product.
+
+The arithmetic lives in ``attn_oracle.c`` (plain loops in double); this file
+only widens inputs to float64 and marshals arrays through ctypes.
+"""
+import ctypes
+
+import numpy as np
+
+from .build import LIB, build_oracle
+
+
+def _f64(x):
+    """Exact widening of a torch tensor / numpy array to contiguous float64."""
+    if hasattr(x, "detach"):  # torch tensor, any dtype/device
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _shapes(q, k, v):
+    if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
+        raise ValueError("expected 4-D [B, H, S, D] arrays")
+    B, Hq, Sq, D = q.shape
+    Bk, Hkv, Skv, Dk = k.shape
+    if (Bk, Dk) != (B, D) or v.shape != k.shape:
+        raise ValueError("inconsistent q/k/v shapes")
+    return B, Hq, Hkv, Sq, Skv, D
+
+
+class Oracle:
+    """ctypes view of one build of ``attn_oracle.c``."""
+
+    def __init__(self, lib_path):
+        lib = ctypes.CDLL(lib_path)
+        dp = ctypes.POINTER(ctypes.c_double)
+        L = ctypes.c_long
+        lib.attn_oracle_fwd.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, L, L,
+                                        ctypes.c_double, ctypes.c_int, L]
+        lib.attn_oracle_fwd.restype = ctypes.c_int
+        lib.attn_oracle_rows.argtypes = [dp, dp, dp, L, L, L, L, L, L,
+                                         ctypes.c_double, ctypes.c_int, L,
+                                         ctypes.POINTER(ctypes.c_int64), L,
+                                         dp, dp]
+        lib.attn_oracle_rows.restype = ctypes.c_int
+        lib.attn_oracle_prob_row.argtypes = [dp, dp, dp, L, L, L, L, L, L,
+                                             ctypes.c_double, ctypes.c_int, L,
+                                             L, L, L, dp]
+        lib.attn_oracle_prob_row.restype = ctypes.c_int
+        lib.attn_oracle_threads.argtypes = []
+        lib.attn_oracle_threads.restype = ctypes.c_int
+        self._lib = lib
+
+    def attention(self, q, k, v, scale, causal=False, input_pos=0):
+        """Full forward: (O [B,Hq,Sq,D], LSE [B,Hq,Sq]) in float64."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, Hq, Hkv, Sq, Skv, D = _shapes(q, k, v)
+        o = np.zeros((B, Hq, Sq, D), np.float64)
+        lse = np.zeros((B, Hq, Sq), np.float64)
+        rc = self._lib.attn_oracle_fwd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq,
+            Skv, D, float(scale), int(bool(causal)), int(input_pos))
+        if rc != 0:
+            raise ValueError("oracle rejected the arguments (code %d)" % rc)
+        return o, lse
+
+    def attention_rows(self, q, k, v, scale, causal, input_pos, rows):
+        """Rows (b, h, i) given as an (n, 3) int array: (O [n,D], LSE [n])."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, Hq, Hkv, Sq, Skv, D = _shapes(q, k, v)
+        rows = np.ascontiguousarray(
+            np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+        n = rows.shape[0]
+        o = np.zeros((n, D), np.float64)
+        lse = np.zeros((n,), np.float64)
+        rc = self._lib.attn_oracle_rows(
+            _ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Sq, Skv, D, float(scale),
+            int(bool(causal)), int(input_pos),
+            rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n, _ptr(o),
+            _ptr(lse))
+        if rc != 0:
+            raise ValueError("oracle rejected the arguments (code %d)" % rc)
+        return o, lse
+
+    def prob_row(self, q, k, v, scale, causal, input_pos, b, h, i):
+        """Softmax weights of query (b, h, i) over all keys, float64 [Skv]."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, Hq, Hkv, Sq, Skv, D = _shapes(q, k, v)
+        p = np.zeros((Skv,), np.float64)
+        rc = self._lib.attn_oracle_prob_row(
+            _ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Sq, Skv, D, float(scale),
+            int(bool(causal)), int(input_pos), b, h, i, _ptr(p))
+        if rc != 0:
+            raise ValueError("oracle rejected the arguments (code %d)" % rc)
+        return p
+
+    def threads(self) -> int:
+        """Number of OpenMP threads the oracle's loops use."""
+        return int(self._lib.attn_oracle_threads())
+
+
+_default = None
+
+
+def default() -> Oracle:
+    global _default
+    if _default is None:
+        _default = Oracle(build_oracle())
+    return _default
+
+
+def attention(q, k, v, scale, causal=False, input_pos=0):
+    return default().attention(q, k, v, scale, causal, input_pos)
+
+
+def attention_rows(q, k, v, scale, causal, input_pos, rows):
+    return default().attention_rows(q, k, v, scale, causal, input_pos, rows)
+
+
+def prob_row(q, k, v, scale, causal, input_pos, b, h, i):
+    return default().prob_row(q, k, v, scale, causal, input_pos, b, h, i)
+
+
+def threads() -> int:
+    return default().threads()

@@ -1,0 +1,213 @@
+/*
+ * Plain fp64 CPU oracle for scaled-dot-product attention forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file: only the tests, the smoke check and the bench's CPU
+ * baseline leg use it.  It shares no code, header, table or constant with
+ * the CUDA library.
+ *
+ * What it computes (one query row at a time, every step in double):
+ *
+ *   "Flash Attention in CUDA Tile (cuTile)" (NVIDIA blog), section "The
+ *   memory bandwidth problem": standard attention materialises the score
+ *   row, applies softmax to it, then multiplies by V.  The flash method in
+ *   the same page's section "Understanding online softmax" reaches exactly
+ *   this result, so the oracle is the plain definition written out:
+ *
+ *     g     = Hq / Hkv,  kvh = h / g             (section "Grouped-query
+ *                                                 attention": query heads
+ *                                                 0-7 use K/V head 0, ...)
+ *     s_j   = scale * sum_d Q[b,h,i,d] * K[b,kvh,j,d]        j in [0, Skv)
+ *     key j is visible iff causal == 0 or j <= input_pos + i
+ *                                                (section "Causal attention";
+ *                                                 the kernel listing adds
+ *                                                 input_pos to the query
+ *                                                 offsets and keeps keys with
+ *                                                 query offset >= key offset)
+ *     M     = max over visible j of s_j
+ *     p_j   = exp(s_j - M) if visible else 0      (safe softmax)
+ *     L     = sum_j p_j
+ *     O[b,h,i,:] = sum_j (p_j / L) * V[b,kvh,j,:]
+ *     LSE[b,h,i] = M + ln(L)                      (natural log; the pages
+ *                                                 define no LSE output, this
+ *                                                 is the reading taken)
+ *
+ * Layouts: Q, O are [B, Hq, Sq, D]; K, V are [B, Hkv, Skv, D]; LSE is
+ * [B, Hq, Sq]; all contiguous, row-major, in double.  Inputs in half or
+ * bfloat16 are widened to double exactly by the caller before the call.
+ *
+ * Parity is pinned by tests that do not use this file's arithmetic: hand
+ * derived small cases, the single-key closed form, uniform-score invariants,
+ * probability row sums, GQA equivalence with repeated heads, key permutation
+ * invariance and a library softmax-attention routine in float64.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Return codes. */
+#define ORACLE_OK 0
+#define ORACLE_BAD_ARG 1
+#define ORACLE_NO_MEMORY 2
+
+static int check_shape(long B, long Hq, long Hkv, long Sq, long Skv, long D,
+                       long input_pos) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Skv <= 0 || D <= 0) return 0;
+  if (Hq % Hkv != 0) return 0;
+  if (input_pos < 0) return 0;
+  return 1;
+}
+
+/*
+ * One query row (b, h, i).  Fills prob[0..Skv) with the softmax weights
+ * p_j / L, out[0..D) with the output row, and *lse with M + ln L.
+ * `score` is caller-provided scratch of Skv doubles.
+ */
+static void oracle_row(const double* Q, const double* K, const double* V,
+                       long Hq, long Hkv, long Sq, long Skv, long D,
+                       double scale, int causal, long input_pos,
+                       long b, long h, long i,
+                       double* score, double* prob, double* out, double* lse) {
+  const long group = Hq / Hkv;
+  const long kvh = h / group;
+  const double* q = Q + ((b * Hq + h) * Sq + i) * D;
+  const double* k = K + (b * Hkv + kvh) * Skv * D;
+  const double* v = V + (b * Hkv + kvh) * Skv * D;
+
+  /* Scores for every key: S = Q K^T * scale, one row of it. */
+  for (long j = 0; j < Skv; ++j) {
+    double dot = 0.0;
+    for (long d = 0; d < D; ++d) dot += q[d] * k[j * D + d];
+    score[j] = scale * dot;
+  }
+
+  /* Visibility and the row maximum over visible keys. */
+  double M = -INFINITY;
+  for (long j = 0; j < Skv; ++j) {
+    const int visible = !causal || j <= input_pos + i;
+    if (visible && score[j] > M) M = score[j];
+  }
+
+  /* Safe softmax: exponentials shifted by the maximum, then normalised. */
+  double L = 0.0;
+  for (long j = 0; j < Skv; ++j) {
+    const int visible = !causal || j <= input_pos + i;
+    prob[j] = visible ? exp(score[j] - M) : 0.0;
+    L += prob[j];
+  }
+  for (long j = 0; j < Skv; ++j) prob[j] /= L;
+
+  /* Weighted sum of value rows. */
+  for (long d = 0; d < D; ++d) out[d] = 0.0;
+  for (long j = 0; j < Skv; ++j) {
+    if (prob[j] == 0.0) continue;
+    for (long d = 0; d < D; ++d) out[d] += prob[j] * v[j * D + d];
+  }
+  *lse = M + log(L);
+}
+
+/* Full forward pass: every (b, h, i) row.  LSE may be NULL. */
+int attn_oracle_fwd(const double* Q, const double* K, const double* V,
+                    double* O, double* LSE, long B, long Hq, long Hkv, long Sq,
+                    long Skv, long D, double scale, int causal, long input_pos) {
+  if (!check_shape(B, Hq, Hkv, Sq, Skv, D, input_pos)) return ORACLE_BAD_ARG;
+  const long rows = B * Hq * Sq;
+  int failed = 0;
+#pragma omp parallel
+  {
+    double* score = (double*)malloc(sizeof(double) * (size_t)Skv);
+    double* prob = (double*)malloc(sizeof(double) * (size_t)Skv);
+    if (!score || !prob) {
+#pragma omp atomic write
+      failed = 1;
+    } else {
+#pragma omp for schedule(dynamic, 16)
+      for (long r = 0; r < rows; ++r) {
+        const long b = r / (Hq * Sq);
+        const long h = (r / Sq) % Hq;
+        const long i = r % Sq;
+        double lse;
+        oracle_row(Q, K, V, Hq, Hkv, Sq, Skv, D, scale, causal, input_pos, b,
+                   h, i, score, prob, O + r * D, &lse);
+        if (LSE) LSE[r] = lse;
+      }
+    }
+    free(score);
+    free(prob);
+  }
+  return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
+}
+
+/*
+ * Selected rows only.  rows_bhi holds n triplets (b, h, i); row r of the
+ * result goes to O_rows[r*D .. r*D+D) and LSE_rows[r].  Used for parity at
+ * sizes where computing every row would take too long.
+ */
+int attn_oracle_rows(const double* Q, const double* K, const double* V,
+                     long B, long Hq, long Hkv, long Sq, long Skv, long D,
+                     double scale, int causal, long input_pos,
+                     const int64_t* rows_bhi, long n, double* O_rows,
+                     double* LSE_rows) {
+  if (!check_shape(B, Hq, Hkv, Sq, Skv, D, input_pos)) return ORACLE_BAD_ARG;
+  for (long r = 0; r < n; ++r) {
+    const int64_t b = rows_bhi[3 * r], h = rows_bhi[3 * r + 1],
+                  i = rows_bhi[3 * r + 2];
+    if (b < 0 || b >= B || h < 0 || h >= Hq || i < 0 || i >= Sq)
+      return ORACLE_BAD_ARG;
+  }
+  int failed = 0;
+#pragma omp parallel
+  {
+    double* score = (double*)malloc(sizeof(double) * (size_t)Skv);
+    double* prob = (double*)malloc(sizeof(double) * (size_t)Skv);
+    if (!score || !prob) {
+#pragma omp atomic write
+      failed = 1;
+    } else {
+#pragma omp for schedule(dynamic, 4)
+      for (long r = 0; r < n; ++r) {
+        oracle_row(Q, K, V, Hq, Hkv, Sq, Skv, D, scale, causal, input_pos,
+                   rows_bhi[3 * r], rows_bhi[3 * r + 1], rows_bhi[3 * r + 2],
+                   score, prob, O_rows + r * D, &LSE_rows[r]);
+      }
+    }
+    free(score);
+    free(prob);
+  }
+  return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
+}
+
+/* The softmax weight row p_j / L of one query (b, h, i): prob[0..Skv). */
+int attn_oracle_prob_row(const double* Q, const double* K, const double* V,
+                         long B, long Hq, long Hkv, long Sq, long Skv, long D,
+                         double scale, int causal, long input_pos, long b,
+                         long h, long i, double* prob) {
+  if (!check_shape(B, Hq, Hkv, Sq, Skv, D, input_pos)) return ORACLE_BAD_ARG;
+  if (b < 0 || b >= B || h < 0 || h >= Hq || i < 0 || i >= Sq)
+    return ORACLE_BAD_ARG;
+  double* score = (double*)malloc(sizeof(double) * (size_t)Skv);
+  double* out = (double*)malloc(sizeof(double) * (size_t)D);
+  if (!score || !out) {
+    free(score);
+    free(out);
+    return ORACLE_NO_MEMORY;
+  }
+  double lse;
+  oracle_row(Q, K, V, Hq, Hkv, Sq, Skv, D, scale, causal, input_pos, b, h, i,
+             score, prob, out, &lse);
+  free(score);
+  free(out);
+  return ORACLE_OK;
+}
+
+/* Threads the parallel loops will use. */
+int attn_oracle_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

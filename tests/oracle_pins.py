@@ -1,0 +1,247 @@
+"""Checks that pin the CPU oracle to facts that do not come from its own code.
+
+Each check takes an ``oracle.Oracle`` instance so the same checks can run
+against the real oracle and against deliberately broken copies of it (see
+test_oracle_mutants.py).  Every check raises AssertionError on failure.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                      "hand_cases.json")
+
+_MATH = {"log": math.log, "exp": math.exp, "e": math.e}
+
+
+def _val(x):
+    if isinstance(x, str):
+        return float(eval(x, {"__builtins__": {}}, _MATH))
+    return float(x)
+
+
+def _arr(nested):
+    def conv(n):
+        return [conv(t) for t in n] if isinstance(n, list) else _val(n)
+    return np.array(conv(nested), dtype=np.float64)
+
+
+def _rand(shape, rng):
+    return rng.standard_normal(shape)
+
+
+def pin_hand_cases(orc):
+    """Hand-derived small cases stored under tests/golden/."""
+    with open(GOLDEN) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        q, k, v = _arr(c["q"]), _arr(c["k"]), _arr(c["v"])
+        o, lse = orc.attention(q, k, v, _val(c["scale"]), c["causal"],
+                               c["input_pos"])
+        np.testing.assert_allclose(o, _arr(c["o"]), rtol=0, atol=1e-12,
+                                   err_msg=c["name"])
+        np.testing.assert_allclose(lse, _arr(c["lse"]), rtol=0, atol=1e-12,
+                                   err_msg=c["name"])
+
+
+def pin_single_key(orc):
+    """Skv = 1: the only weight is 1, so O = V_0 and LSE = scale * q.k_0."""
+    rng = np.random.default_rng(1)
+    B, Hq, Hkv, Sq, D = 2, 4, 2, 5, 8
+    q = _rand((B, Hq, Sq, D), rng)
+    k = _rand((B, Hkv, 1, D), rng)
+    v = _rand((B, Hkv, 1, D), rng)
+    for causal, pos in ((False, 0), (True, 0), (True, 3)):
+        o, lse = orc.attention(q, k, v, 0.3, causal, pos)
+        for h in range(Hq):
+            kvh = h // (Hq // Hkv)
+            np.testing.assert_allclose(
+                o[:, h], np.broadcast_to(v[:, kvh, 0][:, None, :], (B, Sq, D)),
+                rtol=0, atol=1e-13)
+            dots = np.einsum("bsd,bd->bs", q[:, h], k[:, kvh, 0])
+            np.testing.assert_allclose(lse[:, h], 0.3 * dots, rtol=0,
+                                       atol=1e-12)
+
+
+def _visible_counts(Sq, Skv, causal, pos):
+    if not causal:
+        return np.full(Sq, Skv)
+    return np.array([min(Skv, pos + i + 1) for i in range(Sq)])
+
+
+def pin_uniform_scores(orc):
+    """scale = 0 (or Q = 0): O_i = mean of the visible V rows, LSE = ln(#visible)."""
+    rng = np.random.default_rng(2)
+    B, Hq, Hkv, Sq, Skv, D = 1, 4, 2, 7, 11, 6
+    q = _rand((B, Hq, Sq, D), rng)
+    k = _rand((B, Hkv, Skv, D), rng)
+    v = _rand((B, Hkv, Skv, D), rng)
+    for causal, pos in ((False, 0), (True, 0), (True, 2), (True, 9)):
+        cnt = _visible_counts(Sq, Skv, causal, pos)
+        for qq, sc in ((q, 0.0), (np.zeros_like(q), 1.7)):
+            o, lse = orc.attention(qq, k, v, sc, causal, pos)
+            for h in range(Hq):
+                kvh = h // (Hq // Hkv)
+                for i in range(Sq):
+                    mean = v[0, kvh, :cnt[i]].mean(axis=0)
+                    np.testing.assert_allclose(o[0, h, i], mean, rtol=0,
+                                               atol=1e-12)
+                    assert abs(lse[0, h, i] - math.log(cnt[i])) < 1e-12
+
+
+def pin_prob_rows(orc):
+    """Softmax weights are >= 0, zero where masked, and sum to 1."""
+    rng = np.random.default_rng(3)
+    B, Hq, Hkv, Sq, Skv, D = 1, 2, 1, 6, 9, 4
+    q = _rand((B, Hq, Sq, D), rng) * 3
+    k = _rand((B, Hkv, Skv, D), rng)
+    v = _rand((B, Hkv, Skv, D), rng)
+    for causal, pos in ((False, 0), (True, 0), (True, 2)):
+        for h in range(Hq):
+            for i in range(Sq):
+                p = orc.prob_row(q, k, v, 0.5, causal, pos, 0, h, i)
+                assert np.all(p >= 0)
+                assert abs(p.sum() - 1.0) < 1e-12
+                if causal:
+                    assert np.all(p[pos + i + 1:] == 0)
+                    assert np.all(p[:min(Skv, pos + i + 1)] > 0)
+
+
+def pin_gqa_equivalence(orc):
+    """GQA equals MHA on K/V whose heads are repeated group-size times."""
+    rng = np.random.default_rng(4)
+    B, Hq, Hkv, Sq, Skv, D = 2, 8, 2, 5, 7, 4
+    q = _rand((B, Hq, Sq, D), rng)
+    k = _rand((B, Hkv, Skv, D), rng)
+    v = _rand((B, Hkv, Skv, D), rng)
+    g = Hq // Hkv
+    k_rep, v_rep = np.repeat(k, g, axis=1), np.repeat(v, g, axis=1)
+    for causal, pos in ((False, 0), (True, 1)):
+        o1, l1 = orc.attention(q, k, v, 0.4, causal, pos)
+        o2, l2 = orc.attention(q, k_rep, v_rep, 0.4, causal, pos)
+        np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
+
+
+def pin_causal_first_row(orc):
+    """Causal with input_pos = 0: query 0 sees only key 0, so O = V_0."""
+    rng = np.random.default_rng(5)
+    B, Hq, Hkv, Sq, Skv, D = 2, 4, 4, 3, 6, 5
+    q = _rand((B, Hq, Sq, D), rng)
+    k = _rand((B, Hkv, Skv, D), rng)
+    v = _rand((B, Hkv, Skv, D), rng)
+    o, _ = orc.attention(q, k, v, 0.7, True, 0)
+    np.testing.assert_allclose(o[:, :, 0], v[:, :, 0], rtol=0, atol=1e-13)
+
+
+def pin_permutation_invariance(orc):
+    """Non-causal: permuting K and V rows together changes nothing."""
+    rng = np.random.default_rng(6)
+    B, Hq, Hkv, Sq, Skv, D = 1, 2, 2, 4, 9, 3
+    q = _rand((B, Hq, Sq, D), rng)
+    k = _rand((B, Hkv, Skv, D), rng)
+    v = _rand((B, Hkv, Skv, D), rng)
+    perm = rng.permutation(Skv)
+    o1, l1 = orc.attention(q, k, v, 0.9, False, 0)
+    o2, l2 = orc.attention(q, k[:, :, perm], v[:, :, perm], 0.9, False, 0)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
+
+
+def pin_causal_prefix(orc):
+    """Causal row i equals non-causal attention over the keys [0, pos+i]."""
+    rng = np.random.default_rng(7)
+    B, Hq, Hkv, Sq, Skv, D = 1, 2, 1, 4, 10, 3
+    q = _rand((B, Hq, Sq, D), rng)
+    k = _rand((B, Hkv, Skv, D), rng)
+    v = _rand((B, Hkv, Skv, D), rng)
+    # Future keys with huge scores must not leak in: with a maximum taken over
+    # masked keys too, every visible weight would underflow to zero.
+    k = k.copy()
+    k[:, :, 7:] = 1000.0 * np.sign(q[0, 0, 0])[None, None, None, :]
+    for pos in (0, 3, 6, 20):
+        o, lse = orc.attention(q, k, v, 0.8, True, pos)
+        for i in range(Sq):
+            n = min(Skv, pos + i + 1)
+            o2, l2 = orc.attention(q[:, :, i:i + 1], k[:, :, :n], v[:, :, :n],
+                                   0.8, False, 0)
+            np.testing.assert_allclose(o[:, :, i], o2[:, :, 0], rtol=0,
+                                       atol=1e-13)
+            np.testing.assert_allclose(lse[:, :, i], l2[:, :, 0], rtol=0,
+                                       atol=1e-13)
+
+
+def pin_shift_invariance(orc):
+    """Adding c to every key shifts row i's scores by scale*q_i.c: O is
+    unchanged and LSE moves by exactly that amount, even when the shift is
+    far beyond exp's range (a softmax without the max subtraction fails)."""
+    rng = np.random.default_rng(12)
+    B, Hq, Hkv, Sq, Skv, D = 1, 2, 1, 4, 6, 3
+    q = np.abs(_rand((B, Hq, Sq, D), rng)) + 1.0
+    k = _rand((B, Hkv, Skv, D), rng)
+    v = _rand((B, Hkv, Skv, D), rng)
+    c = np.full(D, 400.0)
+    for causal in (False, True):
+        o1, l1 = orc.attention(q, k, v, 1.0, causal, 0)
+        o2, l2 = orc.attention(q, k + c, v, 1.0, causal, 0)
+        shift = np.einsum("bhsd,d->bhs", q, c)
+        assert np.all(np.isfinite(o2)) and np.all(np.isfinite(l2))
+        np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-9)
+        np.testing.assert_allclose(l2 - shift, l1, rtol=0, atol=1e-9)
+
+
+def pin_negated_scale(orc):
+    """scale -> -scale with K -> -K is the same computation."""
+    rng = np.random.default_rng(8)
+    B, Hq, Hkv, Sq, Skv, D = 1, 2, 1, 3, 5, 4
+    q = _rand((B, Hq, Sq, D), rng)
+    k = _rand((B, Hkv, Skv, D), rng)
+    v = _rand((B, Hkv, Skv, D), rng)
+    o1, l1 = orc.attention(q, k, v, -0.6, True, 1)
+    o2, l2 = orc.attention(q, -k, v, 0.6, True, 1)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
+
+
+def pin_torch_sdpa(orc):
+    """Library pin: torch's softmax-attention and logsumexp in float64 on CPU."""
+    F = torch.nn.functional
+    rng = np.random.default_rng(9)
+    for (B, Hq, Hkv, Sq, Skv, D, causal, pos) in (
+            (2, 4, 4, 9, 13, 16, False, 0),
+            (1, 4, 4, 12, 12, 8, True, 0),
+            (1, 2, 2, 5, 11, 8, True, 4)):
+        q = _rand((B, Hq, Sq, D), rng)
+        k = _rand((B, Hkv, Skv, D), rng)
+        v = _rand((B, Hkv, Skv, D), rng)
+        scale = 0.35
+        o, lse = orc.attention(q, k, v, scale, causal, pos)
+        tq, tk, tv = (torch.from_numpy(x) for x in (q, k, v))
+        if causal and pos == 0 and Sq == Skv:
+            ref = F.scaled_dot_product_attention(tq, tk, tv, is_causal=True,
+                                                 scale=scale)
+            mask = torch.ones(Sq, Skv, dtype=torch.bool).tril()
+        elif causal:
+            rows = torch.arange(Sq)[:, None] + pos
+            mask = torch.arange(Skv)[None, :] <= rows
+            ref = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask,
+                                                 scale=scale)
+        else:
+            mask = torch.ones(Sq, Skv, dtype=torch.bool)
+            ref = F.scaled_dot_product_attention(tq, tk, tv, scale=scale)
+        np.testing.assert_allclose(o, ref.numpy(), rtol=0, atol=1e-12)
+        s = torch.matmul(tq, tk.transpose(-1, -2)) * scale
+        s = s.masked_fill(~mask, float("-inf"))
+        np.testing.assert_allclose(lse, torch.logsumexp(s, dim=-1).numpy(),
+                                   rtol=0, atol=1e-12)
+
+
+ALL_PINS = [
+    pin_hand_cases, pin_single_key, pin_uniform_scores, pin_prob_rows,
+    pin_gqa_equivalence, pin_causal_first_row, pin_permutation_invariance,
+    pin_causal_prefix, pin_shift_invariance, pin_negated_scale,
+    pin_torch_sdpa,
+]
