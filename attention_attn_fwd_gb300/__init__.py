@@ -1,0 +1,168 @@
+"""GB300 (sm_103a) FlashAttention-style attention forward.
+
+Python binding of the C ABI declared in ``include/attn.h``: argument
+marshalling only.  Every step of the computation runs in the CUDA library
+``_build/libattn_fwd_gb300.so`` (built by ``attention_attn_fwd_gb300.build``);
+there is no fallback, and every entry point raises ``AttnError`` when the
+library is missing.
+
+Layouts follow the host launcher of "Flash Attention in CUDA Tile (cuTile)":
+Q, O are [B, Hq, Sq, D] and K, V are [B, Hkv, Skv, D], contiguous.
+"""
+import ctypes
+import math
+import os
+import threading
+
+__all__ = [
+    "ATTN_F16", "ATTN_BF16", "AttnError", "attn_fwd", "attn_status_string",
+    "attn_device_status", "attn_tile_config", "attn_version", "fwd",
+    "library_path", "load_library",
+]
+
+ATTN_F16 = 0
+ATTN_BF16 = 1
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_ALIGNMENT = 3
+ATTN_ERR_CUDA = 4
+ATTN_ERR_TIMEOUT = 5
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libattn_fwd_gb300.so")
+_lib = None
+_lock = threading.Lock()
+
+
+class AttnError(RuntimeError):
+    """A non-OK status from the C ABI, or the library is not available."""
+
+    def __init__(self, msg, status=None):
+        super().__init__(msg)
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load the CUDA library (once).  Raises AttnError if it is not built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise AttnError(
+                "CUDA library not built (%s); run "
+                "`python -m attention_attn_fwd_gb300.build`" % _LIB_PATH)
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, i = ctypes.c_void_p, ctypes.c_int
+        ip = ctypes.POINTER(ctypes.c_int)
+        lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i,
+                                 ctypes.c_float, i, i, i, vp]
+        lib.attn_fwd.restype = i
+        lib.attn_status_string.argtypes = [i]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        lib.attn_device_status.restype = i
+        lib.attn_tile_config.argtypes = [i, i, i, i, i, i, i, i, i,
+                                         ip, ip, ip, ip, ip]
+        lib.attn_tile_config.restype = i
+        lib.attn_version.argtypes = []
+        lib.attn_version.restype = i
+        _lib = lib
+        return lib
+
+
+def attn_fwd(Q, K, V, O, LSE, B, Hq, Hkv, Sq, Skv, D, scale, causal,
+             input_pos, dtype, stream) -> int:
+    """Raw C-ABI call; pointers and the stream are integers (0 = NULL)."""
+    return int(load_library().attn_fwd(
+        Q or None, K or None, V or None, O or None, LSE or None, B, Hq, Hkv,
+        Sq, Skv, D, float(scale), int(causal), int(input_pos), int(dtype),
+        stream or None))
+
+
+def attn_status_string(status: int) -> str:
+    return load_library().attn_status_string(int(status)).decode()
+
+
+def attn_device_status():
+    """(status, code): synchronises the device and clears the status word."""
+    code = ctypes.c_uint(0)
+    st = int(load_library().attn_device_status(ctypes.byref(code)))
+    return st, int(code.value)
+
+
+def attn_tile_config(B, Hq, Hkv, Sq, Skv, D, causal, input_pos, dtype):
+    """Tile configuration attn_fwd would launch, as a dict (host only)."""
+    out = [ctypes.c_int(0) for _ in range(5)]
+    st = int(load_library().attn_tile_config(
+        B, Hq, Hkv, Sq, Skv, D, int(causal), int(input_pos), int(dtype),
+        *[ctypes.byref(o) for o in out]))
+    if st != ATTN_OK:
+        raise AttnError("attn_tile_config: " + attn_status_string(st), st)
+    keys = ("block_m", "block_n", "stages", "grid", "smem_bytes")
+    return {k: o.value for k, o in zip(keys, out)}
+
+
+def attn_version() -> int:
+    return int(load_library().attn_version())
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.float16:
+        return ATTN_F16
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    raise AttnError("dtype must be float16 or bfloat16, got %s" % t.dtype,
+                    ATTN_ERR_INVALID_ARG)
+
+
+def fwd(q, k, v, scale=None, causal=True, input_pos=0, out=None, lse=None,
+        need_lse=True, stream=None):
+    """Attention forward on CUDA tensors.
+
+    q [B, Hq, Sq, D], k and v [B, Hkv, Skv, D] (contiguous, same dtype,
+    float16 or bfloat16).  ``scale`` defaults to 1/sqrt(D).  Returns
+    (O, LSE) with LSE float32 [B, Hq, Sq] (None if ``need_lse`` is False).
+    The kernel is enqueued on ``stream`` (default: torch's current stream).
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dim() != 4:
+            raise AttnError("%s must be 4-D [B, H, S, D]" % name,
+                            ATTN_ERR_INVALID_ARG)
+        if not t.is_cuda:
+            raise AttnError("%s must be a CUDA tensor" % name,
+                            ATTN_ERR_INVALID_ARG)
+        if not t.is_contiguous():
+            raise AttnError("%s must be contiguous" % name,
+                            ATTN_ERR_INVALID_ARG)
+    if not (q.dtype == k.dtype == v.dtype):
+        raise AttnError("q, k, v must share a dtype", ATTN_ERR_INVALID_ARG)
+    dt = _dtype_code(q)
+    B, Hq, Sq, D = q.shape
+    Bk, Hkv, Skv, Dk = k.shape
+    if (Bk, Dk) != (B, D) or tuple(v.shape) != tuple(k.shape):
+        raise AttnError("inconsistent q/k/v shapes", ATTN_ERR_INVALID_ARG)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if need_lse and lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        st = attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                      out.data_ptr(), lse.data_ptr() if need_lse else 0,
+                      B, Hq, Hkv, Sq, Skv, D, scale, causal, input_pos, dt,
+                      stream.cuda_stream)
+    if st != ATTN_OK:
+        raise AttnError("attn_fwd: " + attn_status_string(st), st)
+    return out, (lse if need_lse else None)

@@ -1,0 +1,268 @@
+// C ABI of the attention-forward library: argument checks, tile dispatch,
+// tensor-map construction and the kernel launch.  No device memory is
+// allocated here; the caller owns every buffer.
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "../../include/attn.h"
+#include "attn_launch.h"
+
+// Device status word: bit 0 = a pipeline wait ran out, bits 8-15 = role.
+__device__ unsigned int g_attn_status;
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s
+constexpr int kMaxDevices = 64;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+std::mutex g_status_mu;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    g_encode_err = cudaGetDriverEntryPointByVersion(
+        "cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+// Address of the status word on the current device (looked up once).
+unsigned int* status_ptr(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_attn_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+unsigned long long timeout_ns() {
+  static const unsigned long long t = [] {
+    const char* e = std::getenv("ATTN_WAIT_TIMEOUT_NS");
+    if (e != nullptr) {
+      const unsigned long long v = std::strtoull(e, nullptr, 10);
+      if (v > 0) return v;
+    }
+    return kDefaultTimeoutNs;
+  }();
+  return t;
+}
+
+struct Shape {
+  int B, Hq, Hkv, Sq, Skv, D, causal, input_pos;
+};
+
+attn_status_t check_scalars(const Shape& s, float scale, attn_dtype_t dtype) {
+  if (s.B < 0 || s.Hq <= 0 || s.Hkv <= 0 || s.Sq < 0 || s.Skv <= 0 ||
+      s.D <= 0 || s.input_pos < 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (s.Hq % s.Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(s.input_pos) + s.Sq > 0x7fffffffLL)
+    return ATTN_ERR_INVALID_ARG;
+  // Planes (B*H) index a 32-bit tensor-map dimension and kernel ints.
+  if (static_cast<long long>(s.B) * s.Hq > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  if (s.D != 64 && s.D != 128) return ATTN_ERR_UNSUPPORTED;
+  const long long m_blocks = (static_cast<long long>(s.Sq) + attn::cfg::kBlockM - 1) /
+                             attn::cfg::kBlockM;
+  if (m_blocks * s.B * s.Hq > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+// Dispatch table keyed on (D, causal, S, dtype).  One tile shape serves every
+// entry for now: 2 x 128 query rows per CTA, 128-key K/V tiles; the ring
+// depth depends on D (shared-memory budget).
+struct TileChoice {
+  int block_m, block_n, stages, smem_bytes;
+};
+
+TileChoice choose_tiles(const Shape& s) {
+  return TileChoice{attn::cfg::kBlockM, attn::cfg::kTN, attn::fwd_stages(s.D),
+                    attn::fwd_smem_bytes(s.D)};
+}
+
+long long grid_size(const Shape& s) {
+  const long long m_blocks = (static_cast<long long>(s.Sq) + attn::cfg::kBlockM - 1) /
+                             attn::cfg::kBlockM;
+  return m_blocks * s.B * s.Hq;
+}
+
+bool is_device_ptr(const void* p, int dev) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error state
+    return false;
+  }
+  if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
+    return false;
+  return a.device == dev;
+}
+
+bool make_map(CUtensorMap* m, const void* base, attn_dtype_t dtype, int D,
+              int S, long long planes) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D),
+                              static_cast<cuuint64_t>(S),
+                              static_cast<cuuint64_t>(planes)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(S) * D * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  const CUresult r = enc(
+      m, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+      3, const_cast<void*>(base), dims, strides, box, estride,
+      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a);
+  const uintptr_t y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+}  // namespace
+
+namespace attn {
+int fwd_smem_bytes(int D) {
+  return D == 64 ? Layout<64>::kSmemBytes : Layout<128>::kSmemBytes;
+}
+int fwd_stages(int D) {
+  // Each slot holds one K or one V tile; a stage is a K and a V tile.
+  return (D == 64 ? Layout<64>::kSlots : Layout<128>::kSlots) / 2;
+}
+}  // namespace attn
+
+extern "C" {
+
+attn_status_t attn_fwd(const void* Q, const void* K, const void* V, void* O,
+                       float* LSE, int B, int Hq, int Hkv, int Sq, int Skv,
+                       int D, float scale, int causal, int input_pos,
+                       attn_dtype_t dtype, attn_stream_t stream) {
+  const Shape s{B, Hq, Hkv, Sq, Skv, D, causal != 0, input_pos};
+  attn_status_t st = check_scalars(s, scale, dtype);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || Sq == 0) return ATTN_OK;
+  if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  auto misaligned = [](const void* p, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(p) % a) != 0;
+  };
+  if (misaligned(Q, 16) || misaligned(K, 16) || misaligned(V, 16) ||
+      misaligned(O, 16) || (LSE != nullptr && misaligned(LSE, 4)))
+    return ATTN_ERR_ALIGNMENT;
+  const size_t q_bytes = static_cast<size_t>(B) * Hq * Sq * D * 2;
+  const size_t kv_bytes = static_cast<size_t>(B) * Hkv * Skv * D * 2;
+  if (overlaps(O, q_bytes, Q, q_bytes) || overlaps(O, q_bytes, K, kv_bytes) ||
+      overlaps(O, q_bytes, V, kv_bytes))
+    return ATTN_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (!is_device_ptr(Q, dev) || !is_device_ptr(K, dev) ||
+      !is_device_ptr(V, dev) || !is_device_ptr(O, dev) ||
+      (LSE != nullptr && !is_device_ptr(LSE, dev)))
+    return ATTN_ERR_INVALID_ARG;
+  unsigned int* status = status_ptr(dev);
+  if (status == nullptr) return ATTN_ERR_CUDA;
+
+  CUtensorMap tq, tk, tv, to;
+  const long long q_planes = static_cast<long long>(B) * Hq;
+  const long long kv_planes = static_cast<long long>(B) * Hkv;
+  if (!make_map(&tq, Q, dtype, D, Sq, q_planes) ||
+      !make_map(&tk, K, dtype, D, Skv, kv_planes) ||
+      !make_map(&tv, V, dtype, D, Skv, kv_planes) ||
+      !make_map(&to, O, dtype, D, Sq, q_planes))
+    return ATTN_ERR_CUDA;
+
+  attn::FwdParams p{};
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Sq = Sq;
+  p.Skv = Skv;
+  p.causal = causal != 0;
+  p.input_pos = causal != 0 ? input_pos : 0;
+  p.num_m_blocks = (Sq + attn::cfg::kBlockM - 1) / attn::cfg::kBlockM;
+  p.scale_log2 = std::fabs(scale) * 1.4426950408889634f;
+  p.negate_scores = scale < 0.f;
+  p.lse = LSE;
+  p.status = status;
+  p.timeout_ns = timeout_ns();
+
+  const int grid = static_cast<int>(grid_size(s));
+  const bool bf16 = dtype == ATTN_BF16;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t err =
+      D == 64 ? attn::launch_fwd_d64(bf16, tq, tk, tv, to, p, grid, cs)
+              : attn::launch_fwd_d128(bf16, tq, tk, tv, to, p, grid, cs);
+  return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+const char* attn_status_string(attn_status_t status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_ALIGNMENT: return "misaligned pointer";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "device pipeline wait timed out";
+  }
+  return "unknown status";
+}
+
+attn_status_t attn_device_status(unsigned int* code) {
+  if (code != nullptr) *code = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_attn_status, sizeof(v)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (v != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_attn_status, &zero, sizeof(zero)) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+  }
+  if (code != nullptr) *code = v;
+  return v != 0 ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+attn_status_t attn_tile_config(int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                               int causal, int input_pos, attn_dtype_t dtype,
+                               int* block_m, int* block_n, int* stages,
+                               int* grid, int* smem_bytes) {
+  const Shape s{B, Hq, Hkv, Sq, Skv, D, causal != 0, input_pos};
+  const attn_status_t st = check_scalars(s, 1.0f, dtype);
+  if (st != ATTN_OK) return st;
+  const TileChoice t = choose_tiles(s);
+  if (block_m) *block_m = t.block_m;
+  if (block_n) *block_n = t.block_n;
+  if (stages) *stages = t.stages;
+  if (grid) *grid = static_cast<int>(grid_size(s));
+  if (smem_bytes) *smem_bytes = t.smem_bytes;
+  return ATTN_OK;
+}
+
+int attn_version(void) { return kVersion; }
+
+}  // extern "C"

@@ -1,0 +1,476 @@
+// Warp-specialised FlashAttention-style forward kernel for sm_103a.
+//
+// Method (from "Flash Attention in CUDA Tile (cuTile)", sections "How Flash
+// Attention solves the memory bandwidth problem" and "Understanding online
+// softmax"): tile Q, stream K/V tiles through on-chip memory, keep the
+// running row maximum m, running sum l and accumulator O, rescale O and l by
+// alpha = 2^(m_old - m_new) when the maximum moves, and divide O by l at the
+// end.  Scores are taken in the log2 domain with scale*log2(e) folded into
+// one multiply (the listing's INV_LOG_2 step).  Causal tiles that are fully
+// masked are never visited and the mask is applied only to tiles that reach
+// the diagonal or the key tail (same page, "K-loop split").  Query heads map
+// to K/V heads by integer division (section "Grouped-query attention"), and
+// query rows sit at absolute positions input_pos + i (the KV-cache offset).
+//
+// One CTA owns 256 query rows of one (batch, head) as two 128-row Q tiles.
+// Roles (320 threads):
+//   warps 0-3  softmax + correction + epilogue for Q tile 0 (TMEM lanes 0-127)
+//   warps 4-7  the same for Q tile 1
+//   warp  8    TMA producer: Q tiles once, then K_j, V_j into a slot ring
+//   warp  9    TMEM allocator and single-thread tcgen05.mma issuer
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 and O1 (D columns each)
+// from 256.  P_t (16-bit) overwrites the first 64 columns of S_t and is the
+// A operand of O_t += P_t V straight from TMEM.
+//
+// Every mbarrier wait is bounded: on timeout the waiter raises a CTA-wide
+// abort flag and a device status word, every role stops issuing work, waits
+// (again bounded) for its own copies / MMAs in flight, and the CTA frees its
+// TMEM and exits.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "sm103_ptx.cuh"
+
+namespace attn {
+
+struct FwdParams {
+  int B, Hq, Hkv, Sq, Skv;
+  int causal;
+  int input_pos;
+  int num_m_blocks;        // ceil(Sq / 256)
+  float scale_log2;        // |scale| * log2(e)
+  int negate_scores;       // scale < 0: S is computed as -(Q K^T)
+  float* lse;              // [B, Hq, Sq] or nullptr
+  unsigned int* status;    // device status word (timeouts)
+  unsigned long long timeout_ns;
+};
+
+namespace cfg {
+constexpr int kTM = 128;          // rows per Q tile (TMEM lanes)
+constexpr int kTN = 128;          // keys per K/V tile
+constexpr int kBlockM = 256;      // query rows per CTA (two Q tiles)
+constexpr int kThreads = 320;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kTmemCols = 512;
+constexpr float kRescaleTau = 8.0f;  // lazy rescale threshold (log2 units)
+constexpr float kLn2 = 0.6931471805599453f;
+}  // namespace cfg
+
+template <int D>
+struct Layout {
+  static constexpr int kChunks = D / 64;                 // 128-byte boxes/row
+  static constexpr int kBoxBytes = 128 * 128;            // 128 rows x 128 B
+  static constexpr int kTileBytes = kChunks * kBoxBytes; // one Q/K/V tile
+  static constexpr int kSlots = (D == 128) ? 4 : 8;      // K/V ring slots
+  static constexpr int kQOff = 0;
+  static constexpr int kRingOff = kQOff + 2 * kTileBytes;
+  static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
+  // barriers: q_full[2], full[S], empty[S], s_full[2], p_full[2], o_full[2],
+  // drain[1]
+  static constexpr int kNumBars = 2 + 2 * kSlots + 2 + 2 + 2 + 1;
+  static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
+  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kSmemBytes = kBytes + 1024;  // slack for 1 KB alignment
+};
+
+// Keys [0, n*128) are visited; tiles j >= ms need the mask.
+__device__ __forceinline__ void tile_extent(const FwdParams& p, int m0, int& n,
+                                            int& ms) {
+  if (m0 >= p.Sq) {
+    n = 0;
+    ms = 0;
+    return;
+  }
+  const int rows_end = min(m0 + cfg::kTM, p.Sq);
+  const int kend = p.causal ? min(p.input_pos + rows_end, p.Skv) : p.Skv;
+  n = (kend + cfg::kTN - 1) / cfg::kTN;
+  const int full_tiles = p.Skv / cfg::kTN;
+  ms = p.causal ? min((p.input_pos + m0 + 1) / cfg::kTN, full_tiles)
+                : full_tiles;
+}
+
+// Bounded wait.  Returns false if the CTA is aborting or the wait ran out.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+                                             volatile int* abort_flag,
+                                             const FwdParams& p, int role) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+      *abort_flag = 1;
+      atomicOr(p.status, 1u | (static_cast<unsigned>(role) << 8));
+      return false;
+    }
+  }
+}
+
+// Wait used while tearing down after an abort: ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity,
+                                           const FwdParams& p) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer_ns() - t0 > p.timeout_ns) return;
+  }
+}
+
+template <int D, bool kBF16>
+__global__ void __launch_bounds__(cfg::kThreads, 1)
+    attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q,
+                          const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v,
+                          const __grid_constant__ CUtensorMap tm_o,
+                          const FwdParams p) {
+  using L = Layout<D>;
+  using namespace cfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s_base = ptx::smem_u32(smem);
+  const uint32_t s_q = s_base + L::kQOff;
+  const uint32_t s_ring = s_base + L::kRingOff;
+  const uint32_t bar0 = s_base + L::kBarOff;
+  const uint32_t bar_q = bar0;                         // [2]
+  const uint32_t bar_full = bar0 + 8 * 2;              // [kSlots]
+  const uint32_t bar_empty = bar_full + 8 * L::kSlots; // [kSlots]
+  const uint32_t bar_s = bar_empty + 8 * L::kSlots;    // [2]
+  const uint32_t bar_p = bar_s + 8 * 2;                // [2]
+  const uint32_t bar_o = bar_p + 8 * 2;                // [2]
+  const uint32_t bar_drain = bar_o + 8 * 2;            // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<int*>(smem + L::kMiscOff + 4);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  // Work unit: heaviest causal m-blocks first (the page's reversed block
+  // order); consecutive units are consecutive heads, so GQA heads sharing a
+  // K/V head run together and find K/V in L2.
+  const int bh_count = p.B * p.Hq;
+  const int mb = p.num_m_blocks - 1 - static_cast<int>(blockIdx.x) / bh_count;
+  const int bh = static_cast<int>(blockIdx.x) % bh_count;
+  const int b = bh / p.Hq;
+  const int h = bh % p.Hq;
+  const int kvh = h / (p.Hq / p.Hkv);
+  const int q_plane = b * p.Hq + h;     // index into the [B*Hq] plane dim
+  const int kv_plane = b * p.Hkv + kvh;
+  int n_t[2], ms_t[2];
+  tile_extent(p, mb * kBlockM, n_t[0], ms_t[0]);
+  tile_extent(p, mb * kBlockM + kTM, n_t[1], ms_t[1]);
+  const int n_kv = max(n_t[0], n_t[1]);
+
+  if (threadIdx.x == 0) {
+    // P-ready barriers collect one arrival per softmax thread; the others
+    // one arrival (an expect-tx, a tcgen05.commit).
+    for (int i = 0; i < L::kNumBars; ++i) {
+      const uint32_t bar = bar0 + 8 * i;
+      ptx::mbar_init(bar, (bar == bar_p || bar == bar_p + 8) ? kTM : 1);
+    }
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      ptx::prefetch_tensormap(&tm_q);
+      ptx::prefetch_tensormap(&tm_k);
+      ptx::prefetch_tensormap(&tm_v);
+      for (int t = 0; t < 2; ++t) {
+        if (n_t[t] == 0) continue;
+        const uint32_t dst = s_q + t * L::kTileBytes;
+        ptx::mbar_arrive_expect_tx(bar_q + 8 * t, L::kTileBytes);
+        for (int c = 0; c < L::kChunks; ++c)
+          ptx::tma_load_3d(dst + c * L::kBoxBytes, &tm_q, bar_q + 8 * t, c * 64,
+                           mb * kBlockM + t * kTM, q_plane);
+      }
+      bool ok = true;
+      int issued = 0;  // ring items (K_0, V_0, K_1, ...) issued so far
+      for (int j = 0; j < n_kv && ok; ++j) {
+        for (int kv = 0; kv < 2; ++kv) {
+          const int it = 2 * j + kv;
+          const int slot = it % L::kSlots;
+          if (it >= L::kSlots) {
+            ok = wait_bounded(bar_empty + 8 * slot,
+                              ((it / L::kSlots) - 1) & 1, abort_flag, p, 1);
+            if (!ok) break;
+          }
+          const uint32_t dst = s_ring + slot * L::kTileBytes;
+          ptx::mbar_arrive_expect_tx(bar_full + 8 * slot, L::kTileBytes);
+          for (int c = 0; c < L::kChunks; ++c)
+            ptx::tma_load_3d(dst + c * L::kBoxBytes, kv ? &tm_v : &tm_k,
+                             bar_full + 8 * slot, c * 64, j * kTN, kv_plane);
+          issued = it + 1;
+        }
+      }
+      if (!ok) {
+        // Let every copy still in flight land before the CTA goes away.
+        for (int t = 0; t < 2; ++t)
+          if (n_t[t] > 0) drain_wait(bar_q + 8 * t, 0, p);
+        const int first = max(0, issued - L::kSlots);
+        for (int it = first; it < issued; ++it)
+          drain_wait(bar_full + 8 * (it % L::kSlots), (it / L::kSlots) & 1, p);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_qk =
+          ptx::idesc_f16(kBF16, kTM, kTN, false, p.negate_scores != 0);
+      const uint32_t idesc_pv = ptx::idesc_f16(kBF16, kTM, D, true, false);
+      bool ok = true;
+      bool issued_any = false;
+
+      // S_t = Q_t K_j^T : A = Q tile (K-major), B = K tile (K-major).
+      auto issue_qk = [&](int t, int slot) {
+        const uint32_t qa = s_q + t * L::kTileBytes;
+        const uint32_t kb = s_ring + slot * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * L::kBoxBytes + (kk % 4) * 32;
+          ptx::mma_ss(tmem + t * kTN, ptx::sdesc_sw128(qa + off, 16, 1024),
+                      ptx::sdesc_sw128(kb + off, 16, 1024), idesc_qk,
+                      kk > 0 ? 1u : 0u);
+        }
+      };
+      // O_t (+)= P_t V_j : A = P_t in TMEM, B = V tile (MN-major).
+      auto issue_pv = [&](int t, int slot, bool acc) {
+        const uint32_t vb = s_ring + slot * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTN / 16; ++kk) {
+          ptx::mma_ts(tmem + 2 * kTN + t * D, tmem + t * kTN + kk * 8,
+                      ptx::sdesc_sw128(vb + kk * 16 * 128, L::kBoxBytes, 1024),
+                      idesc_pv, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+
+      ok = wait_bounded(bar_full, 0, abort_flag, p, 2);  // K_0 in slot 0
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (!ok) break;
+        if (n_t[t] == 0) continue;
+        ok = wait_bounded(bar_q + 8 * t, 0, abort_flag, p, 2);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_qk(t, 0);
+        ptx::tc_commit(bar_s + 8 * t);
+        issued_any = true;
+      }
+      if (ok) ptx::tc_commit(bar_empty + 0);
+
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int it_v = 2 * j + 1;
+        const int slot_v = it_v % L::kSlots;
+        const int it_k = 2 * j + 2;
+        const int slot_k = it_k % L::kSlots;
+        ok = wait_bounded(bar_full + 8 * slot_v, (it_v / L::kSlots) & 1,
+                          abort_flag, p, 2);
+        if (!ok) break;
+        bool k_ready = false;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok) break;
+          if (j >= n_t[t]) continue;
+          ok = wait_bounded(bar_p + 8 * t, j & 1, abort_flag, p, 2);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_pv(t, slot_v, j > 0);
+          if (j == n_t[t] - 1) {
+            ptx::tc_commit(bar_o + 8 * t);
+          } else {
+            if (!k_ready) {
+              ok = wait_bounded(bar_full + 8 * slot_k, (it_k / L::kSlots) & 1,
+                                abort_flag, p, 2);
+              if (!ok) break;
+              k_ready = true;
+            }
+            issue_qk(t, slot_k);
+            ptx::tc_commit(bar_s + 8 * t);
+          }
+        }
+        if (!ok) break;
+        ptx::tc_commit(bar_empty + 8 * slot_v);
+        if (j + 1 < n_kv) ptx::tc_commit(bar_empty + 8 * slot_k);
+      }
+      if (!ok && issued_any) {
+        // Wait for the MMAs already issued before TMEM is released.
+        ptx::tc_commit(bar_drain);
+        drain_wait(bar_drain, 0, p);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------- softmax / correction / epilogue
+    const int t = warp / 4;                 // Q tile of this warpgroup
+    const int r = threadIdx.x % 128;        // row within the tile
+    const int n = t == 0 ? n_t[0] : n_t[1];
+    const int ms = t == 0 ? ms_t[0] : ms_t[1];
+    if (n > 0) {
+      const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
+      const uint32_t t_s = tmem + lane_off + t * kTN;
+      const uint32_t t_o = tmem + lane_off + 2 * kTN + t * D;
+      const int m0 = mb * kBlockM + t * kTM;
+      const int row_pos = p.input_pos + m0 + r;  // absolute query position
+      const float c = p.scale_log2;
+      float m_run = -INFINITY;  // running max of scaled scores (log2 units)
+      float l_run = 0.f;        // running sum of 2^(s*c - m_run)
+      bool ok = true;
+
+      for (int j = 0; j < n; ++j) {
+        ok = wait_bounded(bar_s + 8 * t, j & 1, abort_flag, p, 3);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        ptx::tc_fence_after();
+
+        uint32_t sr[kTN];
+#pragma unroll
+        for (int q = 0; q < kTN / 32; ++q) ptx::tmem_ld32(t_s + 32 * q, sr + 32 * q);
+        ptx::tmem_wait_ld();
+
+        const bool masked = j >= ms;
+        float mx;
+        if (masked) {
+          // Visible keys of this row in the tile are the columns < lim:
+          // key < Skv, and key <= row_pos when causal.
+          const int kbase = j * kTN;
+          int lim = p.Skv - kbase;
+          if (p.causal) lim = min(lim, row_pos - kbase + 1);
+          mx = -INFINITY;
+#pragma unroll
+          for (int q = 0; q < kTN; ++q) {
+            const float v = (q < lim) ? __uint_as_float(sr[q]) * c : -INFINITY;
+            sr[q] = __float_as_uint(v);
+            mx = fmaxf(mx, v);
+          }
+        } else {
+          float m0a = __uint_as_float(sr[0]), m1a = __uint_as_float(sr[1]);
+#pragma unroll
+          for (int q = 2; q < kTN; q += 2) {
+            m0a = fmaxf(m0a, __uint_as_float(sr[q]));
+            m1a = fmaxf(m1a, __uint_as_float(sr[q + 1]));
+          }
+          mx = fmaxf(m0a, m1a) * c;
+        }
+
+        // Lazy rescale: keep the stale maximum unless some row of the warp
+        // grew by more than kRescaleTau (P stays <= 2^tau; exact either way,
+        // since O and l share the same reference maximum).
+        float m_new = m_run;
+        if (__any_sync(0xffffffffu, mx > m_run + kRescaleTau))
+          m_new = fmaxf(m_run, mx);
+        const float alpha = (m_new == -INFINITY) ? 1.f : ptx::ex2(m_run - m_new);
+
+        // P = 2^(s*c - m_new), row sum, packed to 16-bit into TMEM over S_t:
+        // 32 scores -> 16 columns, key 2e+1 | key 2e in column e.
+        const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
+        float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+        for (int q = 0; q < kTN / 32; ++q) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float x0 = __uint_as_float(sr[32 * q + 2 * e]);
+            const float x1 = __uint_as_float(sr[32 * q + 2 * e + 1]);
+            const float p0 = masked ? ptx::ex2(x0 + neg_m)
+                                    : ptx::ex2(fmaf(x0, c, neg_m));
+            const float p1 = masked ? ptx::ex2(x1 + neg_m)
+                                    : ptx::ex2(fmaf(x1, c, neg_m));
+            sum0 += p0;
+            sum1 += p1;
+            pk[e] = ptx::pack2<kBF16>(p0, p1);
+          }
+          ptx::tmem_st16(t_s + 16 * q, pk);
+        }
+
+        if (j > 0 && __any_sync(0xffffffffu, m_new != m_run)) {
+          // Correction: O_t *= alpha.  The previous PV into O_t is complete:
+          // it was issued before this tile's S_t, whose commit we waited on.
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t o[32];
+            ptx::tmem_ld32(t_o + 32 * q, o);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            ptx::tmem_st32(t_o + 32 * q, o);
+          }
+        }
+        l_run *= alpha;
+        ptx::tmem_wait_st();
+        l_run += sum0 + sum1;
+        m_run = m_new;
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_p + 8 * t);
+      }
+
+      // ---------------------------------------------------------- epilogue
+      if (ok) {
+        ok = wait_bounded(bar_o + 8 * t, 0, abort_flag, p, 4);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      const uint32_t stage = s_q + t * L::kTileBytes;  // Q_t is no longer read
+      if (ok) {
+        ptx::tc_fence_after();
+        const float inv_l = ptx::rcp(l_run);
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t o[32];
+          ptx::tmem_ld32(t_o + 32 * q, o);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = ptx::pack2<kBF16>(
+                  __uint_as_float(o[8 * v + 2 * e]) * inv_l,
+                  __uint_as_float(o[8 * v + 2 * e + 1]) * inv_l);
+            const int col = 32 * q + 8 * v;          // first element
+            const int box = col / 64;
+            const int unit = (col % 64) / 8;         // 16-byte unit in row
+            const uint32_t addr = stage + box * L::kBoxBytes + r * 128 +
+                                  ((unit ^ (r & 7)) * 16);
+            ptx::st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+          }
+        }
+        if (p.lse != nullptr && m0 + r < p.Sq) {
+          const long long row =
+              (static_cast<long long>(q_plane) * p.Sq) + m0 + r;
+          p.lse[row] = (m_run + ptx::lg2(l_run)) * kLn2;
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::named_barrier_sync(1 + t, 128);
+      if (r == 0 && !*abort_flag) {
+        for (int cidx = 0; cidx < L::kChunks; ++cidx)
+          ptx::tma_store_3d(&tm_o, stage + cidx * L::kBoxBytes, cidx * 64, m0,
+                            q_plane);
+        ptx::bulk_commit_group();
+        ptx::bulk_wait_group_all();
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace attn

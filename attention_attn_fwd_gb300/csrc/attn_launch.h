@@ -1,0 +1,26 @@
+// Internal launch interface between the C ABI and the kernel translation
+// units (one per head dimension, compiled in parallel).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "attn_fwd_kernel.cuh"
+
+namespace attn {
+
+// Dynamic shared memory one CTA of the D-variant needs.
+int fwd_smem_bytes(int D);
+// Ring slots (K/V tiles in flight) of the D-variant.
+int fwd_stages(int D);
+
+cudaError_t launch_fwd_d64(bool bf16, const CUtensorMap& q,
+                           const CUtensorMap& k, const CUtensorMap& v,
+                           const CUtensorMap& o, const FwdParams& p, int grid,
+                           cudaStream_t stream);
+cudaError_t launch_fwd_d128(bool bf16, const CUtensorMap& q,
+                            const CUtensorMap& k, const CUtensorMap& v,
+                            const CUtensorMap& o, const FwdParams& p, int grid,
+                            cudaStream_t stream);
+
+}  // namespace attn

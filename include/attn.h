@@ -1,0 +1,113 @@
+/*
+ * attn.h — C ABI of the GB300 (sm_103a) attention-forward library.
+ *
+ * One call computes, for every batch b, query head h and query row i,
+ *
+ *   O[b,h,i,:] = softmax_j( scale * Q[b,h,i,:] . K[b,kvh,j,:] ) V[b,kvh,j,:]
+ *
+ * over the keys j that are visible to row i, plus the row's log-sum-exp.
+ * Sources (web pages this library restates):
+ *   - "Flash Attention in CUDA Tile (cuTile)" (NVIDIA blog), sections
+ *     "What is attention?" and "Understanding online softmax": the operation
+ *     and the tiled online-softmax method that computes it exactly;
+ *   - same page, section "Causal attention" and the kernel listing's
+ *     "Applying the causal mask" step: key j is visible to query row i iff
+ *     j <= input_pos + i (queries sit at absolute positions input_pos + i,
+ *     the KV-cache offset of the listing's "Initializing accumulators" step);
+ *   - same page, section "Grouped-query attention": kvh = h / (Hq / Hkv);
+ *   - same page, host-launcher section: [B, H, S, D] contiguous tensors,
+ *     the scale defaulting to 1/sqrt(D) on the Python side.
+ *
+ * No function here allocates device memory; the caller owns every buffer.
+ */
+#ifndef ATTN_FWD_GB300_ATTN_H
+#define ATTN_FWD_GB300_ATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream; NULL is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st* attn_stream_t;
+
+/* Element type of Q, K, V and O. */
+typedef enum {
+  ATTN_F16 = 0,  /* IEEE binary16 */
+  ATTN_BF16 = 1  /* bfloat16 */
+} attn_dtype_t;
+
+/* Return codes.  Everything but ATTN_OK leaves O and LSE untouched. */
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,  /* bad size, NULL or host pointer, bad dtype   */
+  ATTN_ERR_UNSUPPORTED = 2,  /* valid but not implemented (D not 64 or 128) */
+  ATTN_ERR_ALIGNMENT = 3,    /* Q/K/V/O not 16-byte or LSE not 4-byte aligned */
+  ATTN_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed            */
+  ATTN_ERR_TIMEOUT = 5       /* a kernel pipeline wait ran out (device status) */
+} attn_status_t;
+
+/*
+ * attn_fwd — scaled-dot-product attention forward on the GPU.
+ *
+ * Q    device, [B, Hq,  Sq,  D] contiguous, dtype      (read)
+ * K    device, [B, Hkv, Skv, D] contiguous, dtype      (read)
+ * V    device, [B, Hkv, Skv, D] contiguous, dtype      (read)
+ * O    device, [B, Hq,  Sq,  D] contiguous, dtype      (written)
+ * LSE  device, [B, Hq,  Sq] float32, or NULL to skip   (written)
+ *      LSE[b,h,i] = ln( sum over visible j of exp(scale * q_i . k_j) ),
+ *      natural log, scale included.
+ * B >= 0, Hq > 0, Hkv > 0 with Hq % Hkv == 0, Sq >= 0, Skv >= 1,
+ * D in {64, 128}.  B == 0 or Sq == 0 is a successful no-op.
+ * scale     finite; any sign (0 gives uniform weights over visible keys).
+ * causal    0: every key is visible and input_pos is ignored;
+ *           non-zero: key j is visible to query row i iff j <= input_pos + i.
+ *           Queries with input_pos + i >= Skv - 1 see every key.
+ * input_pos >= 0, and input_pos + Sq must fit in a signed 32-bit int.
+ * dtype     ATTN_F16 or ATTN_BF16 (Q, K, V and O share it).
+ * stream    the CUDA stream the kernel is enqueued on.
+ *
+ * Q/K/V/O must be 16-byte aligned (tensor-memory-accelerator copies), LSE
+ * 4-byte aligned; O must not overlap Q, K or V.  The call is asynchronous:
+ * the return code covers argument checks and the launch only.  A device
+ * side pipeline timeout is reported later by attn_device_status().
+ * Results are deterministic for a given shape and dtype.
+ */
+attn_status_t attn_fwd(const void* Q, const void* K, const void* V, void* O,
+                       float* LSE, int B, int Hq, int Hkv, int Sq, int Skv,
+                       int D, float scale, int causal, int input_pos,
+                       attn_dtype_t dtype, attn_stream_t stream);
+
+/* Short English description of a status code (static storage). */
+const char* attn_status_string(attn_status_t status);
+
+/*
+ * attn_device_status — synchronises the current device, then reads and
+ * clears the library's device status word.  *code receives 0 when no kernel
+ * wait has run out since the last call; otherwise a non-zero code
+ * (bits 0-7: 1 = wait timed out; bits 8-15: the pipeline role that gave
+ * up) and the function returns ATTN_ERR_TIMEOUT.  code may be NULL.
+ */
+attn_status_t attn_device_status(unsigned int* code);
+
+/*
+ * attn_tile_config — the tile configuration attn_fwd would launch for these
+ * arguments (host only, no GPU needed).  Fills, when non-NULL:
+ *   block_m   query rows per CTA, block_n keys per K/V tile,
+ *   stages    K/V tiles the shared-memory ring holds,
+ *   grid      CTAs launched, smem_bytes dynamic shared memory per CTA.
+ * Returns the same validation code attn_fwd would (pointers not checked).
+ */
+attn_status_t attn_tile_config(int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                               int causal, int input_pos, attn_dtype_t dtype,
+                               int* block_m, int* block_n, int* stages,
+                               int* grid, int* smem_bytes);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_FWD_GB300_ATTN_H */

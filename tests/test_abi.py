@@ -1,0 +1,134 @@
+"""C ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, and rejects bad arguments with the documented codes before
+touching the device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import attention_attn_fwd_gb300 as attn
+from attention_attn_fwd_gb300 import build as cuda_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    return attn.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for n in ("attn_fwd", "attn_status_string", "attn_device_status",
+              "attn_tile_config", "attn_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", attn.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if line)
+    for name in declared_functions():
+        assert name in exported, name
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        s = attn.attn_status_string(code)
+        assert s and s != "unknown status"
+    assert attn.attn_status_string(99) == "unknown status"
+
+
+def test_version(lib):
+    assert attn.attn_version() >= 100
+
+
+BAD = 0x1000  # an aligned address that is never dereferenced on these paths
+
+
+def call(**kw):
+    a = dict(Q=BAD, K=BAD + 0x100000, V=BAD + 0x200000, O=BAD + 0x300000,
+             LSE=0, B=1, Hq=2, Hkv=2, Sq=128, Skv=128, D=64, scale=0.125,
+             causal=0, input_pos=0, dtype=attn.ATTN_F16, stream=0)
+    a.update(kw)
+    return attn.attn_fwd(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Hq=3, Hkv=2), attn.ATTN_ERR_INVALID_ARG),       # Hq % Hkv
+    (dict(Hq=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Hkv=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(B=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Sq=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Skv=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(D=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(input_pos=-1, causal=1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(input_pos=2**31 - 100, Sq=128), attn.ATTN_ERR_INVALID_ARG),
+    (dict(dtype=7), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(D=96), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(D=256), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(Q=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(O=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Q=BAD + 8), attn.ATTN_ERR_ALIGNMENT),
+    (dict(V=BAD + 0x200002), attn.ATTN_ERR_ALIGNMENT),
+    (dict(LSE=BAD + 0x400002), attn.ATTN_ERR_ALIGNMENT),
+    (dict(O=BAD + 0x40), attn.ATTN_ERR_INVALID_ARG),       # O overlaps Q
+])
+def test_argument_checks(lib, kw, code):
+    assert call(**kw) == code
+
+
+def test_empty_problem_is_a_noop(lib):
+    assert call(B=0) == attn.ATTN_OK
+    assert call(Sq=0) == attn.ATTN_OK
+    # Even with NULL pointers: nothing is read or written.
+    assert call(Sq=0, Q=0, K=0, V=0, O=0) == attn.ATTN_OK
+
+
+def test_tile_config(lib):
+    c = attn.attn_tile_config(1, 32, 4, 8192, 8192, 128, 1, 0, attn.ATTN_BF16)
+    assert c["block_m"] == 256 and c["block_n"] == 128
+    assert c["grid"] == 32 * 8192 // 256
+    assert 0 < c["smem_bytes"] <= 227 * 1024
+    assert c["stages"] >= 2
+    c64 = attn.attn_tile_config(4, 16, 16, 1000, 1000, 64, 0, 0, attn.ATTN_F16)
+    assert c64["grid"] == 4 * 16 * 4
+    with pytest.raises(attn.AttnError):
+        attn.attn_tile_config(1, 3, 2, 8, 8, 64, 0, 0, attn.ATTN_F16)
+
+
+def test_no_device_is_an_error_not_a_crash(lib):
+    """Without a GPU a well-formed call fails cleanly with ATTN_ERR_CUDA or
+    ATTN_ERR_INVALID_ARG (pointers are not device memory)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert call() in (attn.ATTN_ERR_CUDA, attn.ATTN_ERR_INVALID_ARG)
+
+
+def test_fwd_rejects_cpu_tensors():
+    import torch
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.float16)
+    with pytest.raises(attn.AttnError):
+        attn.fwd(q, q, q)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(attn, "_LIB_PATH", str(tmp_path / "nope.so"))
+    monkeypatch.setattr(attn, "_lib", None)
+    with pytest.raises(attn.AttnError, match="not built"):
+        attn.load_library()
