@@ -1,0 +1,410 @@
+"""Attention-forward throughput on GB300.
+
+One step = one attention forward (the whole hot path: one kernel launch) over
+the GQA long-context workload B=1, Hq=32, Hkv=4, Sq=Skv=8192, D=128, bf16,
+causal, Q/K/V ~ N(0,1), scale = 1/sqrt(128).  Throughput is reported in
+TFLOPS with 4*B*Hq*Sq*Skv*D FLOPs per step, halved for causal.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica of the same
+workload (the path has no exchange step); the value is the FLOPs of all
+ranks over the slowest rank's time.  ``--impl reference`` times the fp64 CPU
+oracle on the host cores instead (rank 0 only), a bounded sample per step.
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("attention fwd TFLOPS on 1 GB300 (causal-halved FLOPs) and % of "
+          "dense bf16 peak")
+UNIT = "TFLOPS"
+FLUSH_BYTES = 256 << 20  # > 129 MB L2
+KERNEL_SOURCES = ["attention_attn_fwd_gb300/csrc/attn_fwd_kernel.cuh",
+                  "attention_attn_fwd_gb300/csrc/sm103_ptx.cuh"]
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles",
+                               "attn_fwd_sm103_gqa8k_traffic.md")
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic():
+    """DRAM bytes per launch from the committed ncu summary, or None when
+    the summary is missing or the kernel source changed since the capture."""
+    try:
+        text = open(TRAFFIC_PROFILE).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return int(m_bytes.group(1))
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples every 100 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev),
+                 "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"),
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None,
+                    "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.path)
+        # Median over the busier half of the samples (the kernel runs).
+        busy = sorted(sm)[len(sm) // 2:] if sm else []
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def workload():
+    from attention_attn_fwd_gb300.inputs import GQA_8K
+    return GQA_8K
+
+
+def config_dict(w, extra=None):
+    d = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq,
+         "Skv": w.Skv, "D": w.D, "causal": w.causal,
+         "input_pos": w.input_pos, "scale": "1/sqrt(D)",
+         "flops_per_step": w.flops(),
+         "flops_convention": "4*B*Hq*Sq*Skv*D, halved for causal",
+         "exact_visible_flops_per_step": w.exact_flops()}
+    if extra:
+        d.update(extra)
+    return d
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import attention_attn_fwd_gb300 as attn
+    from attention_attn_fwd_gb300.inputs import make_qkv
+
+    ws, rank, local = dist_info()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = workload()
+    q, k, v = make_qkv(w, seed=0)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    dt = attn.ATTN_BF16 if w.dtype == "bf16" else attn.ATTN_F16
+
+    def step(qp, kp, vp, op, lp):
+        st = attn.attn_fwd(qp, kp, vp, op, lp, w.B, w.Hq, w.Hkv, w.Sq, w.Skv,
+                           w.D, w.scale, int(w.causal), w.input_pos, dt,
+                           stream.cuda_stream)
+        if st != attn.ATTN_OK:
+            raise RuntimeError("attn_fwd: " + attn.attn_status_string(st))
+
+    ptrs = (qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(),
+            lse.data_ptr())
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step(*ptrs)
+    torch.cuda.synchronize()
+
+    # ---- device-timed region: K launches, L2 flushed between them.
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            starts[i].record(stream)
+            step(*ptrs)
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if ws > 1:
+        dist.barrier()
+    clk = clocks.summary()
+    st, code = attn.attn_device_status()
+    if st != attn.ATTN_OK:
+        raise RuntimeError("device status %d code %#x" % (st, code))
+    times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kernel_ms = sum(times_ms) / len(times_ms)
+
+    # ---- end-to-end through the C ABI with host buffers: every step copies
+    # its Q/K/V from pinned host memory and reads O and LSE back, inside the
+    # timed region.  Copies and kernels run on three streams with double
+    # buffers, so step i+1's upload and step i-1's download overlap step i.
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = (o.numel() * o.element_size() + lse.numel() * lse.element_size())
+    dev_bufs = [(qd, kd, vd, o, lse),
+                (torch.empty_like(qd), torch.empty_like(kd),
+                 torch.empty_like(vd), torch.empty_like(o),
+                 torch.empty_like(lse))]
+    host_out = [(torch.empty(o.shape, dtype=o.dtype).pin_memory(),
+                 torch.empty(lse.shape, dtype=lse.dtype).pin_memory())
+                for _ in range(2)]
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_up = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_down = [torch.cuda.Event() for _ in range(2)]
+
+    def e2e_steps(n):
+        for i in range(n):
+            s = i % 2
+            qb, kb, vb, ob, lb = dev_bufs[s]
+            if i >= 2:
+                up.wait_event(ev_comp[s])       # inputs of step i-2 consumed
+            with torch.cuda.stream(up):
+                qb.copy_(qh, non_blocking=True)
+                kb.copy_(kh, non_blocking=True)
+                vb.copy_(vh, non_blocking=True)
+                ev_up[s].record(up)
+            stream.wait_event(ev_up[s])
+            if i >= 2:
+                stream.wait_event(ev_down[s])   # outputs of step i-2 read back
+            step(qb.data_ptr(), kb.data_ptr(), vb.data_ptr(), ob.data_ptr(),
+                 lb.data_ptr())
+            ev_comp[s].record(stream)
+            down.wait_event(ev_comp[s])
+            with torch.cuda.stream(down):
+                host_out[s][0].copy_(ob, non_blocking=True)
+                host_out[s][1].copy_(lb, non_blocking=True)
+                ev_down[s].record(down)
+
+    e2e_steps(max(2, args.warmup))
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(up)
+    e2e_steps(args.steps)
+    down.wait_event(ev_comp[(args.steps - 1) % 2])
+    e1.record(down)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    e2e_launches = args.steps
+
+    # Max over ranks.
+    if ws > 1:
+        t = torch.tensor([kernel_ms, e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        kernel_ms, e2e_ms = float(t[0]), float(t[1])
+
+    flops = w.flops()
+    value = ws * flops / (kernel_ms * 1e-3) / 1e12
+    e2e_value = ws * flops / (e2e_ms * 1e-3) / 1e12
+    peak_tf, _, peak_src = peaks()
+    achieved = flops / (kernel_ms * 1e-3) / 1e12  # one launch, one GPU
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(kernel_ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic: Q/K/V ~ N(0,1) from a seeded CPU generator",
+        "config": config_dict(w, {
+            "l2": "flushed between timed steps (256 MiB write, untimed)",
+            "parallelism": "replicas" if ws > 1 else "single GPU",
+            "pct_of_dense_bf16_peak": round(100 * achieved / peak_tf, 2),
+            "exact_visible_tflops": round(
+                w.exact_flops() / (kernel_ms * 1e-3) / 1e12, 2),
+            "ms_per_step_p50": round(statistics.median(times_ms), 4),
+            "ms_per_step_max": round(max(times_ms), 4),
+            "wall_s_timed_region": round(wall, 4)}),
+        "roofline": {
+            "bound": "tensor", "achieved": round(achieved, 2),
+            "peak": peak_tf, "unit": "TFLOP/s",
+            "frac": round(achieved / peak_tf, 4),
+            "peak_source": "%s bf16 dense burst (cuBLAS)" % peak_src,
+            "traffic": measured_traffic(),
+            "algorithmic_bytes": w.io_bytes()},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4),
+                "pipelining": "3 streams (upload, compute, download), "
+                              "double-buffered"},
+        "gpu_launches": args.steps + e2e_launches,
+        "clocks": clk,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, q, k, v, budget_s=args.cpu_s)
+    if ws > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------- CPU oracle
+def oracle_sample(w, q, k, v, heads):
+    """Time the oracle on every row of the given query heads."""
+    import numpy as np
+
+    import oracle
+    rows = np.array([(b, h, i) for b in range(w.B) for h in heads
+                     for i in range(w.Sq)], dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k, v, w.scale, w.causal, w.input_pos, rows)
+    dt = time.perf_counter() - t0
+    flops = w.flops() * len(heads) / w.Hq
+    return flops, dt
+
+
+def cpu_baseline(w, q, k, v, budget_s=15.0):
+    import oracle
+    heads, flops, secs = [], 0.0, 0.0
+    h = 0
+    while h < w.Hq and (secs < budget_s or not heads):
+        f, dt = oracle_sample(w, q, k, v, [h])
+        heads.append(h)
+        flops += f
+        secs += dt
+        h += 1
+    return {"value": round(flops / secs / 1e12, 6), "unit": UNIT,
+            "cores": oracle.threads(), "kind": "oracle",
+            "sample": "all %d rows of query heads %s (of %d), same inputs; "
+                      "%.1f s" % (w.Sq, heads, w.Hq, secs)}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return
+    import oracle
+    from attention_attn_fwd_gb300.inputs import make_qkv
+    w = workload()
+    q, k, v = make_qkv(w, seed=0)
+    oracle.threads()  # build/load before timing
+    for i in range(args.warmup):
+        oracle_sample(w, q, k, v, [i % w.Hq])
+    flops, secs = 0.0, 0.0
+    for i in range(args.steps):
+        f, dt = oracle_sample(w, q, k, v, [i % w.Hq])
+        flops += f
+        secs += dt
+    value = flops / secs / 1e12
+    out = {
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+        "impl": "reference", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * secs / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic: Q/K/V ~ N(0,1) from a seeded "
+                                "CPU generator",
+        "config": config_dict(w, {"sample_per_step": "all rows of one query "
+                                                     "head"}),
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT,
+                         "cores": oracle.threads(), "kind": "oracle",
+                         "sample": "each step: all %d rows of one query head"
+                                   % w.Sq},
+        "e2e": {"value": round(value, 6), "unit": UNIT,
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-s", type=float, default=15.0,
+                    help="CPU-oracle baseline budget in seconds")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
