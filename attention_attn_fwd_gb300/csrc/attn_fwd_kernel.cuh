@@ -13,11 +13,12 @@
 // query rows sit at absolute positions input_pos + i (the KV-cache offset).
 //
 // One CTA owns 256 query rows of one (batch, head) as two 128-row Q tiles.
-// Roles (320 threads):
-//   warps 0-3  softmax + correction + epilogue for Q tile 0 (TMEM lanes 0-127)
-//   warps 4-7  the same for Q tile 1
-//   warp  8    TMA producer: Q tiles once, then K_j, V_j into a slot ring
-//   warp  9    TMEM allocator and single-thread tcgen05.mma issuer
+// Roles (384 threads):
+//   warp  0    TMEM allocator and single-thread tcgen05.mma issuer
+//   warp  1    TMA producer: Q tiles once, then K_j, V_j into a slot ring
+//   warps 2-3  idle
+//   warps 4-7  softmax + correction + epilogue for Q tile 0 (TMEM lanes 0-127)
+//   warps 8-11 the same for Q tile 1
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 and O1 (D columns each)
 // from 256.  P_t (16-bit) overwrites the first 64 columns of S_t and is the
 // A operand of O_t += P_t V straight from TMEM.
@@ -51,9 +52,13 @@ namespace cfg {
 constexpr int kTM = 128;          // rows per Q tile (TMEM lanes)
 constexpr int kTN = 128;          // keys per K/V tile
 constexpr int kBlockM = 256;      // query rows per CTA (two Q tiles)
-constexpr int kThreads = 320;
-constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
+// The MMA issuer and the TMA producer take the lowest warp indices: warp
+// schedulers favour older (lower-index) warps, and the single-thread MMA
+// issue must not starve behind the instruction-dense softmax warps.
+constexpr int kThreads = 384;
+constexpr int kMmaWarp = 0;
+constexpr int kLoadWarp = 1;
+constexpr int kSoftmaxWarp0 = 4;  // warps 4-7: Q tile 0, warps 8-11: Q tile 1
 constexpr int kTmemCols = 512;
 constexpr float kRescaleTau = 8.0f;  // lazy rescale threshold (log2 units)
 constexpr float kLn2 = 0.6931471805599453f;
@@ -93,13 +98,17 @@ __device__ __forceinline__ void tile_extent(const FwdParams& p, int m0, int& n,
 }
 
 // Bounded wait.  Returns false if the CTA is aborting or the wait ran out.
+// try_wait suspends the thread for a while by itself; the abort flag and the
+// clock are checked once every 32 tries.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
                                              volatile int* abort_flag,
                                              const FwdParams& p, int role) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (ptx::mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
       *abort_flag = 1;
@@ -184,137 +193,156 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
 
   if (warp == kLoadWarp) {
     // ------------------------------------------------------ TMA producer
+    // The whole warp runs this loop (warp-uniform); one elected lane issues.
     if (lane == 0) {
       ptx::prefetch_tensormap(&tm_q);
       ptx::prefetch_tensormap(&tm_k);
       ptx::prefetch_tensormap(&tm_v);
-      for (int t = 0; t < 2; ++t) {
-        if (n_t[t] == 0) continue;
-        const uint32_t dst = s_q + t * L::kTileBytes;
-        ptx::mbar_arrive_expect_tx(bar_q + 8 * t, L::kTileBytes);
-        for (int c = 0; c < L::kChunks; ++c)
-          ptx::tma_load_3d(dst + c * L::kBoxBytes, &tm_q, bar_q + 8 * t, c * 64,
-                           mb * kBlockM + t * kTM, q_plane);
-      }
-      bool ok = true;
-      int issued = 0;  // ring items (K_0, V_0, K_1, ...) issued so far
-      for (int j = 0; j < n_kv && ok; ++j) {
-        for (int kv = 0; kv < 2; ++kv) {
-          const int it = 2 * j + kv;
-          const int slot = it % L::kSlots;
-          if (it >= L::kSlots) {
-            ok = wait_bounded(bar_empty + 8 * slot,
-                              ((it / L::kSlots) - 1) & 1, abort_flag, p, 1);
-            if (!ok) break;
-          }
-          const uint32_t dst = s_ring + slot * L::kTileBytes;
-          ptx::mbar_arrive_expect_tx(bar_full + 8 * slot, L::kTileBytes);
-          for (int c = 0; c < L::kChunks; ++c)
-            ptx::tma_load_3d(dst + c * L::kBoxBytes, kv ? &tm_v : &tm_k,
-                             bar_full + 8 * slot, c * 64, j * kTN, kv_plane);
-          issued = it + 1;
+    }
+    for (int t = 0; t < 2; ++t) {
+      if (n_t[t] == 0) continue;
+      const uint32_t dst = s_q + t * L::kTileBytes;
+      ptx::mbar_arrive_expect_tx_elect(bar_q + 8 * t, L::kTileBytes);
+      for (int c = 0; c < L::kChunks; ++c)
+        ptx::tma_load_3d_elect(dst + c * L::kBoxBytes, &tm_q, bar_q + 8 * t,
+                               c * 64, mb * kBlockM + t * kTM, q_plane);
+    }
+    bool ok = true;
+    int issued = 0;  // ring items (K_0, V_0, K_1, ...) issued so far
+    for (int j = 0; j < n_kv && ok; ++j) {
+      for (int kv = 0; kv < 2; ++kv) {
+        const int it = 2 * j + kv;
+        const int slot = it % L::kSlots;
+        if (it >= L::kSlots) {
+          ok = wait_bounded(bar_empty + 8 * slot, ((it / L::kSlots) - 1) & 1,
+                            abort_flag, p, 1);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
         }
+        const uint32_t dst = s_ring + slot * L::kTileBytes;
+        ptx::mbar_arrive_expect_tx_elect(bar_full + 8 * slot, L::kTileBytes);
+        for (int c = 0; c < L::kChunks; ++c)
+          ptx::tma_load_3d_elect(dst + c * L::kBoxBytes, kv ? &tm_v : &tm_k,
+                                 bar_full + 8 * slot, c * 64, j * kTN,
+                                 kv_plane);
+        issued = it + 1;
       }
-      if (!ok) {
-        // Let every copy still in flight land before the CTA goes away.
-        for (int t = 0; t < 2; ++t)
-          if (n_t[t] > 0) drain_wait(bar_q + 8 * t, 0, p);
-        const int first = max(0, issued - L::kSlots);
-        for (int it = first; it < issued; ++it)
-          drain_wait(bar_full + 8 * (it % L::kSlots), (it / L::kSlots) & 1, p);
-      }
+    }
+    if (!ok) {
+      // Let every copy still in flight land before the CTA goes away.
+      for (int t = 0; t < 2; ++t)
+        if (n_t[t] > 0) drain_wait(bar_q + 8 * t, 0, p);
+      const int first = max(0, issued - L::kSlots);
+      for (int it = first; it < issued; ++it)
+        drain_wait(bar_full + 8 * (it % L::kSlots), (it / L::kSlots) & 1, p);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop (warp-uniform); one elected lane issues.
+    {
       const uint32_t idesc_qk =
           ptx::idesc_f16(kBF16, kTM, kTN, false, p.negate_scores != 0);
       const uint32_t idesc_pv = ptx::idesc_f16(kBF16, kTM, D, true, false);
       bool ok = true;
       bool issued_any = false;
 
+      // Descriptor low words, computed once; per MMA one add of a
+      // compile-time offset.  K-major tiles: LBO unused (16), SBO = 1024
+      // (8 rows of 128 B).  V (MN-major): LBO = 16 KB between the 64-column
+      // halves of D, SBO = 1024 between groups of 8 keys.
+      constexpr uint32_t kHi = ptx::sdesc_hi_sw128(1024);
+      const uint32_t q_lo = ptx::sdesc_lo(s_q, 16);
+      const uint32_t k_lo = ptx::sdesc_lo(s_ring, 16);
+      const uint32_t v_lo = ptx::sdesc_lo(s_ring, L::kBoxBytes);
+      constexpr uint32_t kTile16 = L::kTileBytes >> 4;
+
       // S_t = Q_t K_j^T : A = Q tile (K-major), B = K tile (K-major).
       auto issue_qk = [&](int t, int slot) {
-        const uint32_t qa = s_q + t * L::kTileBytes;
-        const uint32_t kb = s_ring + slot * L::kTileBytes;
+        const uint32_t a0 = q_lo + t * kTile16;
+        const uint32_t b0 = k_lo + slot * kTile16;
+        const uint32_t d = tmem + t * kTN;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * L::kBoxBytes + (kk % 4) * 32;
-          ptx::mma_ss(tmem + t * kTN, ptx::sdesc_sw128(qa + off, 16, 1024),
-                      ptx::sdesc_sw128(kb + off, 16, 1024), idesc_qk,
-                      kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk / 4) * L::kBoxBytes + (kk % 4) * 32) >> 4;
+          ptx::mma_ss_elect(d, a0 + off, b0 + off, kHi, idesc_qk,
+                            kk > 0 ? 1u : 0u);
         }
       };
       // O_t (+)= P_t V_j : A = P_t in TMEM, B = V tile (MN-major).
       auto issue_pv = [&](int t, int slot, bool acc) {
-        const uint32_t vb = s_ring + slot * L::kTileBytes;
+        const uint32_t b0 = v_lo + slot * kTile16;
+        const uint32_t d = tmem + 2 * kTN + t * D;
+        const uint32_t a = tmem + t * kTN;
 #pragma unroll
         for (int kk = 0; kk < kTN / 16; ++kk) {
-          ptx::mma_ts(tmem + 2 * kTN + t * D, tmem + t * kTN + kk * 8,
-                      ptx::sdesc_sw128(vb + kk * 16 * 128, L::kBoxBytes, 1024),
-                      idesc_pv, (acc || kk > 0) ? 1u : 0u);
+          ptx::mma_ts_elect(d, a + kk * 8, b0 + ((kk * 16 * 128) >> 4), kHi,
+                            idesc_pv, (acc || kk > 0) ? 1u : 0u);
         }
       };
 
-      ok = wait_bounded(bar_full, 0, abort_flag, p, 2);  // K_0 in slot 0
+      ok = __all_sync(0xffffffffu, wait_bounded(bar_full, 0, abort_flag, p, 2));  // K_0
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (!ok) break;
         if (n_t[t] == 0) continue;
-        ok = wait_bounded(bar_q + 8 * t, 0, abort_flag, p, 2);
+        ok = __all_sync(0xffffffffu, wait_bounded(bar_q + 8 * t, 0, abort_flag, p, 2));
         if (!ok) break;
         ptx::tc_fence_after();
         issue_qk(t, 0);
-        ptx::tc_commit(bar_s + 8 * t);
+        ptx::tc_commit_elect(bar_s + 8 * t);
         issued_any = true;
       }
-      if (ok) ptx::tc_commit(bar_empty + 0);
+      if (ok) ptx::tc_commit_elect(bar_empty + 0);
 
       for (int j = 0; j < n_kv && ok; ++j) {
         const int it_v = 2 * j + 1;
         const int slot_v = it_v % L::kSlots;
         const int it_k = 2 * j + 2;
         const int slot_k = it_k % L::kSlots;
-        ok = wait_bounded(bar_full + 8 * slot_v, (it_v / L::kSlots) & 1,
-                          abort_flag, p, 2);
+        ok = __all_sync(0xffffffffu,
+                        wait_bounded(bar_full + 8 * slot_v,
+                                     (it_v / L::kSlots) & 1, abort_flag, p, 2));
         if (!ok) break;
         bool k_ready = false;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok) break;
           if (j >= n_t[t]) continue;
-          ok = wait_bounded(bar_p + 8 * t, j & 1, abort_flag, p, 2);
+          ok = __all_sync(0xffffffffu,
+                          wait_bounded(bar_p + 8 * t, j & 1, abort_flag, p, 2));
           if (!ok) break;
           ptx::tc_fence_after();
           issue_pv(t, slot_v, j > 0);
           if (j == n_t[t] - 1) {
-            ptx::tc_commit(bar_o + 8 * t);
+            ptx::tc_commit_elect(bar_o + 8 * t);
           } else {
             if (!k_ready) {
-              ok = wait_bounded(bar_full + 8 * slot_k, (it_k / L::kSlots) & 1,
-                                abort_flag, p, 2);
+              ok = __all_sync(0xffffffffu,
+                              wait_bounded(bar_full + 8 * slot_k,
+                                           (it_k / L::kSlots) & 1, abort_flag,
+                                           p, 2));
               if (!ok) break;
               k_ready = true;
             }
             issue_qk(t, slot_k);
-            ptx::tc_commit(bar_s + 8 * t);
+            ptx::tc_commit_elect(bar_s + 8 * t);
           }
         }
         if (!ok) break;
-        ptx::tc_commit(bar_empty + 8 * slot_v);
-        if (j + 1 < n_kv) ptx::tc_commit(bar_empty + 8 * slot_k);
+        ptx::tc_commit_elect(bar_empty + 8 * slot_v);
+        if (j + 1 < n_kv) ptx::tc_commit_elect(bar_empty + 8 * slot_k);
       }
       if (!ok && issued_any) {
         // Wait for the MMAs already issued before TMEM is released.
-        ptx::tc_commit(bar_drain);
+        ptx::tc_commit_elect(bar_drain);
         drain_wait(bar_drain, 0, p);
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp >= kSoftmaxWarp0) {
     // ------------------------------------- softmax / correction / epilogue
-    const int t = warp / 4;                 // Q tile of this warpgroup
+    const int t = warp / 4 - 1;             // Q tile of this warpgroup
     const int r = threadIdx.x % 128;        // row within the tile
     const int n = t == 0 ? n_t[0] : n_t[1];
     const int ms = t == 0 ? ms_t[0] : ms_t[1];
@@ -335,34 +363,51 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
         if (!ok) break;
         ptx::tc_fence_after();
 
-        uint32_t sr[kTN];
-#pragma unroll
-        for (int q = 0; q < kTN / 32; ++q) ptx::tmem_ld32(t_s + 32 * q, sr + 32 * q);
-        ptx::tmem_wait_ld();
-
+        // Pass 1: row maximum of the scaled scores over the visible keys.
+        // Visible keys of this row in the tile are the columns < lim: key <
+        // Skv, and key <= row_pos when causal (only tiles j >= ms can cut).
         const bool masked = j >= ms;
-        float mx;
+        int lim = kTN;
         if (masked) {
-          // Visible keys of this row in the tile are the columns < lim:
-          // key < Skv, and key <= row_pos when causal.
           const int kbase = j * kTN;
-          int lim = p.Skv - kbase;
+          lim = min(kTN, p.Skv - kbase);
           if (p.causal) lim = min(lim, row_pos - kbase + 1);
-          mx = -INFINITY;
+        }
+        float mx;
+        {
+          uint32_t sr[kTN];
 #pragma unroll
-          for (int q = 0; q < kTN; ++q) {
-            const float v = (q < lim) ? __uint_as_float(sr[q]) * c : -INFINITY;
-            sr[q] = __float_as_uint(v);
-            mx = fmaxf(mx, v);
-          }
-        } else {
-          float m0a = __uint_as_float(sr[0]), m1a = __uint_as_float(sr[1]);
+          for (int q = 0; q < kTN / 32; ++q)
+            ptx::tmem_ld32(t_s + 32 * q, sr + 32 * q);
+          ptx::tmem_wait_ld();
+          if (masked) {
 #pragma unroll
-          for (int q = 2; q < kTN; q += 2) {
-            m0a = fmaxf(m0a, __uint_as_float(sr[q]));
-            m1a = fmaxf(m1a, __uint_as_float(sr[q + 1]));
+            for (int q = 0; q < kTN; ++q)
+              if (q >= lim) sr[q] = __float_as_uint(-INFINITY);
           }
-          mx = fmaxf(m0a, m1a) * c;
+          // Four independent chains of 3-input max.
+          float mc[4];
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+            mc[a] = ptx::fmax3(__uint_as_float(sr[2 * a]),
+                               __uint_as_float(sr[2 * a + 1]),
+                               __uint_as_float(sr[8 + 2 * a]));
+#pragma unroll
+          for (int q = 16; q < kTN; q += 8) {
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+              mc[a] = ptx::fmax3(mc[a], __uint_as_float(sr[q + 2 * a]),
+                                 __uint_as_float(sr[q + 2 * a + 1]));
+          }
+          // Columns 9, 11, 13, 15 are not yet in any chain.
+          const float h0 = ptx::fmax3(mc[0], mc[1],
+                                      fmaxf(__uint_as_float(sr[9]),
+                                            __uint_as_float(sr[11])));
+          const float h1 = ptx::fmax3(mc[2], mc[3],
+                                      fmaxf(__uint_as_float(sr[13]),
+                                            __uint_as_float(sr[15])));
+          const float raw = fmaxf(h0, h1);
+          mx = (raw == -INFINITY) ? -INFINITY : raw * c;
         }
 
         // Lazy rescale: keep the stale maximum unless some row of the warp
@@ -373,26 +418,42 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
           m_new = fmaxf(m_run, mx);
         const float alpha = (m_new == -INFINITY) ? 1.f : ptx::ex2(m_run - m_new);
 
-        // P = 2^(s*c - m_new), row sum, packed to 16-bit into TMEM over S_t:
-        // 32 scores -> 16 columns, key 2e+1 | key 2e in column e.
+        // Pass 2: P = 2^(s*c - m_new) and its row sum, packed to 16 bits into
+        // TMEM over S_t (32 scores -> 16 columns, key 2e+1 | key 2e in column
+        // e).  S is re-read from TMEM in 32-column chunks, the next chunk's
+        // load in flight while this one is computed; P chunk q only
+        // overwrites S columns already consumed.
         const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
-        float sum0 = 0.f, sum1 = 0.f;
+        float sm[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+          uint32_t buf[2][32];
+          ptx::tmem_ld32(t_s, buf[0]);
+          ptx::tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < kTN / 32; ++q) {
-          uint32_t pk[16];
+          for (int q = 0; q < kTN / 32; ++q) {
+            uint32_t* cur = buf[q & 1];
+            if (q + 1 < kTN / 32) ptx::tmem_ld32(t_s + 32 * (q + 1), buf[(q + 1) & 1]);
+            uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float x0 = __uint_as_float(sr[32 * q + 2 * e]);
-            const float x1 = __uint_as_float(sr[32 * q + 2 * e + 1]);
-            const float p0 = masked ? ptx::ex2(x0 + neg_m)
-                                    : ptx::ex2(fmaf(x0, c, neg_m));
-            const float p1 = masked ? ptx::ex2(x1 + neg_m)
-                                    : ptx::ex2(fmaf(x1, c, neg_m));
-            sum0 += p0;
-            sum1 += p1;
-            pk[e] = ptx::pack2<kBF16>(p0, p1);
+            for (int e = 0; e < 16; ++e) {
+              float x0, x1;
+              ptx::ffma2(x0, x1, __uint_as_float(cur[2 * e]),
+                         __uint_as_float(cur[2 * e + 1]), c, neg_m);
+              if (masked) {
+                if (32 * q + 2 * e >= lim) x0 = -INFINITY;
+                if (32 * q + 2 * e + 1 >= lim) x1 = -INFINITY;
+              }
+              const float p0 = ptx::ex2(x0);
+              const float p1 = ptx::ex2(x1);
+              if (e & 1)
+                ptx::fadd2(sm[2], sm[3], p0, p1);
+              else
+                ptx::fadd2(sm[0], sm[1], p0, p1);
+              pk[e] = ptx::pack2<kBF16>(p0, p1);
+            }
+            ptx::tmem_st16(t_s + 16 * q, pk);
+            if (q + 1 < kTN / 32) ptx::tmem_wait_ld();
           }
-          ptx::tmem_st16(t_s + 16 * q, pk);
         }
 
         if (j > 0 && __any_sync(0xffffffffu, m_new != m_run)) {
@@ -411,7 +472,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
         }
         l_run *= alpha;
         ptx::tmem_wait_st();
-        l_run += sum0 + sum1;
+        l_run += (sm[0] + sm[1]) + (sm[2] + sm[3]);
         m_run = m_new;
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar_p + 8 * t);

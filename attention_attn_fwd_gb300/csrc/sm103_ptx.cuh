@@ -147,42 +147,110 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
       : "memory");
 }
 
-// D(tmem) (+)= A(smem desc) * B(smem desc)
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc,
-                                       uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
+// Shared-memory matrix descriptors for 128-byte-swizzled operand tiles.
+// Low word: start address (bits 0-13, 16-byte units) and leading byte offset
+// (bits 16-29, 16-byte units).  High word: stride byte offset (bits 32-45),
+// descriptor version 1 (bits 46-47) and swizzle mode 2 = 128B (bits 61-63).
+// Operand tiles lie below 256 KB of shared memory, so a byte offset `off`
+// moves a descriptor by adding off >> 4 to its low word.
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sdesc_hi_sw128(uint32_t sbo) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+
+// The *_elect variants below are executed by a whole warp with warp-uniform
+// operands; `elect.sync` picks one lane (always the same, the lowest active
+// one) to issue the single-thread instruction.  Keeping the issuing loop
+// warp-uniform lets the operands live in uniform registers.
+
+// D(tmem) (+)= A(smem) * B(smem); descriptors given as (lo, hi) words.
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint32_t a_lo,
+                                       uint32_t b_lo, uint32_t hi,
+                                       uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %3};\n\tmov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n\t}" ::"r"(
           d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-// D(tmem) (+)= A(tmem) * B(smem desc)
+__device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint32_t a_lo,
+                                             uint32_t b_lo, uint32_t hi,
+                                             uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %3};\n\tmov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n\t}" ::"r"(
+          d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem,
+                                             uint32_t b_lo, uint32_t hi,
+                                             uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
+      "[%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint32_t bar,
+                                                            uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(
+          bar),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_elect(uint32_t dst,
+                                                  const CUtensorMap* m,
+                                                  uint32_t bar, int c0, int c1,
+                                                  int c2) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::"
+      "complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];\n\t}" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// D(tmem) (+)= A(tmem) * B(smem)
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem,
-                                       uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
+                                       uint32_t b_lo, uint32_t hi,
+                                       uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(
           d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
       : "memory");
-}
-
-// Shared-memory matrix descriptor for a 128-byte-swizzled operand tile:
-// start address, leading/stride byte offsets (16-byte units), descriptor
-// version 1 (bits 46-47) and swizzle mode 2 = 128B (bits 61-63).
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo,
-                                                uint32_t sbo) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-  d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
-  return d;
 }
 
 // Instruction descriptor, kind::f16, fp32 accumulator.
@@ -256,6 +324,36 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// (x0, x1) * m + (a, a) as one packed f32x2 FMA.
+__device__ __forceinline__ void ffma2(float& y0, float& y1, float x0, float x1,
+                                      float m, float a) {
+  asm("{\n\t.reg .b64 x, mm, aa, y;\n\t"
+      "mov.b64 x, {%2, %3};\n\tmov.b64 mm, {%4, %4};\n\t"
+      "mov.b64 aa, {%5, %5};\n\t"
+      "fma.rn.ftz.f32x2 y, x, mm, aa;\n\t"
+      "mov.b64 {%0, %1}, y;\n\t}"
+      : "=f"(y0), "=f"(y1)
+      : "f"(x0), "f"(x1), "f"(m), "f"(a));
+}
+
+// (s0, s1) += (x0, x1) as one packed f32x2 add.
+__device__ __forceinline__ void fadd2(float& s0, float& s1, float x0,
+                                      float x1) {
+  asm("{\n\t.reg .b64 s, x;\n\t"
+      "mov.b64 s, {%0, %1};\n\tmov.b64 x, {%2, %3};\n\t"
+      "add.rn.ftz.f32x2 s, s, x;\n\t"
+      "mov.b64 {%0, %1}, s;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(x0), "f"(x1));
+}
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __device__ __forceinline__ float lg2(float x) {
