@@ -98,17 +98,17 @@ __device__ __forceinline__ void tile_extent(const FwdParams& p, int m0, int& n,
 }
 
 // Bounded wait.  Returns false if the CTA is aborting or the wait ran out.
-// try_wait suspends the thread for a while by itself; the abort flag and the
-// clock are checked once every 32 tries.
+// After one immediate test the thread sleeps in try_wait (woken when the
+// phase completes, or after at most 20 us), so waiting warps do not take
+// issue slots from the working ones; abort flag and clock are checked
+// between sleeps.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
                                              volatile int* abort_flag,
                                              const FwdParams& p, int role) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (ptx::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*abort_flag) return false;
     if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
       *abort_flag = 1;
