@@ -69,6 +69,22 @@ struct Shape {
   int B, Hq, Hkv, Sq, Skv, D, causal, input_pos;
 };
 
+// A CTA owns two 128-row Q tiles: two query heads of one K/V group at the
+// same rows when the group size is even, else 256 consecutive rows of one
+// head.
+bool pair_heads(const Shape& s) { return (s.Hq / s.Hkv) % 2 == 0; }
+
+long long m_blocks(const Shape& s) {
+  const int rows = pair_heads(s) ? attn::cfg::kTM : attn::cfg::kBlockM;
+  return (static_cast<long long>(s.Sq) + rows - 1) / rows;
+}
+
+long long grid_size(const Shape& s) {
+  const long long units = pair_heads(s) ? static_cast<long long>(s.B) * (s.Hq / 2)
+                                        : static_cast<long long>(s.B) * s.Hq;
+  return m_blocks(s) * units;
+}
+
 attn_status_t check_scalars(const Shape& s, float scale, attn_dtype_t dtype) {
   if (s.B < 0 || s.Hq <= 0 || s.Hkv <= 0 || s.Sq < 0 || s.Skv <= 0 ||
       s.D <= 0 || s.input_pos < 0)
@@ -76,14 +92,14 @@ attn_status_t check_scalars(const Shape& s, float scale, attn_dtype_t dtype) {
   if (s.Hq % s.Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-  if (static_cast<long long>(s.input_pos) + s.Sq > 0x7fffffffLL)
+  // Row positions of the last (partial) tile must stay within int32.
+  if (static_cast<long long>(s.input_pos) + s.Sq + 2 * attn::cfg::kBlockM >
+      0x7fffffffLL)
     return ATTN_ERR_INVALID_ARG;
   // Planes (B*H) index a 32-bit tensor-map dimension and kernel ints.
   if (static_cast<long long>(s.B) * s.Hq > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
   if (s.D != 64 && s.D != 128) return ATTN_ERR_UNSUPPORTED;
-  const long long m_blocks = (static_cast<long long>(s.Sq) + attn::cfg::kBlockM - 1) /
-                             attn::cfg::kBlockM;
-  if (m_blocks * s.B * s.Hq > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  if (grid_size(s) > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }
 
@@ -97,12 +113,6 @@ struct TileChoice {
 TileChoice choose_tiles(const Shape& s) {
   return TileChoice{attn::cfg::kBlockM, attn::cfg::kTN, attn::fwd_stages(s.D),
                     attn::fwd_smem_bytes(s.D)};
-}
-
-long long grid_size(const Shape& s) {
-  const long long m_blocks = (static_cast<long long>(s.Sq) + attn::cfg::kBlockM - 1) /
-                             attn::cfg::kBlockM;
-  return m_blocks * s.B * s.Hq;
 }
 
 bool is_device_ptr(const void* p, int dev) {
@@ -204,7 +214,8 @@ attn_status_t attn_fwd(const void* Q, const void* K, const void* V, void* O,
   p.Skv = Skv;
   p.causal = causal != 0;
   p.input_pos = causal != 0 ? input_pos : 0;
-  p.num_m_blocks = (Sq + attn::cfg::kBlockM - 1) / attn::cfg::kBlockM;
+  p.num_m_blocks = static_cast<int>(m_blocks(s));
+  p.pair_heads = pair_heads(s);
   p.scale_log2 = std::fabs(scale) * 1.4426950408889634f;
   p.negate_scores = scale < 0.f;
   p.lse = LSE;

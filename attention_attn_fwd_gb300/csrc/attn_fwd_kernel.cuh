@@ -40,7 +40,8 @@ struct FwdParams {
   int B, Hq, Hkv, Sq, Skv;
   int causal;
   int input_pos;
-  int num_m_blocks;        // ceil(Sq / 256)
+  int num_m_blocks;        // m-blocks per head (of 128 or 256 rows)
+  int pair_heads;          // a unit = 2 heads x 128 rows (else 1 head x 256)
   float scale_log2;        // |scale| * log2(e)
   int negate_scores;       // scale < 0: S is computed as -(Q K^T)
   float* lse;              // [B, Hq, Sq] or nullptr
@@ -156,20 +157,28 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
-  // Work unit: heaviest causal m-blocks first (the page's reversed block
-  // order); consecutive units are consecutive heads, so GQA heads sharing a
-  // K/V head run together and find K/V in L2.
-  const int bh_count = p.B * p.Hq;
-  const int mb = p.num_m_blocks - 1 - static_cast<int>(blockIdx.x) / bh_count;
-  const int bh = static_cast<int>(blockIdx.x) % bh_count;
-  const int b = bh / p.Hq;
-  const int h = bh % p.Hq;
-  const int kvh = h / (p.Hq / p.Hkv);
-  const int q_plane = b * p.Hq + h;     // index into the [B*Hq] plane dim
+  // Work unit: two 128-row Q tiles.  With an even GQA group the tiles are
+  // two query heads of one K/V group at the same rows (identical causal
+  // extents and masks, shared K/V tiles); otherwise two consecutive row
+  // blocks of one head.  Heaviest causal m-blocks first (the page's reversed
+  // block order); consecutive units are consecutive heads, so the heads of
+  // a K/V group run together and find K/V in L2.
+  const int units_per_m = p.pair_heads ? p.B * (p.Hq / 2) : p.B * p.Hq;
+  const int mb = p.num_m_blocks - 1 - static_cast<int>(blockIdx.x) / units_per_m;
+  const int ub = static_cast<int>(blockIdx.x) % units_per_m;
+  const int b = p.pair_heads ? ub / (p.Hq / 2) : ub / p.Hq;
+  const int h0 = p.pair_heads ? 2 * (ub % (p.Hq / 2)) : ub % p.Hq;
+  const int kvh = h0 / (p.Hq / p.Hkv);
   const int kv_plane = b * p.Hkv + kvh;
+  int plane_t[2], m0_t[2];  // [B*Hq] plane and first row of each Q tile
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    plane_t[t] = b * p.Hq + h0 + (p.pair_heads ? t : 0);
+    m0_t[t] = p.pair_heads ? mb * kTM : mb * kBlockM + t * kTM;
+  }
   int n_t[2], ms_t[2];
-  tile_extent(p, mb * kBlockM, n_t[0], ms_t[0]);
-  tile_extent(p, mb * kBlockM + kTM, n_t[1], ms_t[1]);
+  tile_extent(p, m0_t[0], n_t[0], ms_t[0]);
+  tile_extent(p, m0_t[1], n_t[1], ms_t[1]);
   const int n_kv = max(n_t[0], n_t[1]);
 
   if (threadIdx.x == 0) {
@@ -205,7 +214,8 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
       ptx::mbar_arrive_expect_tx_elect(bar_q + 8 * t, L::kTileBytes);
       for (int c = 0; c < L::kChunks; ++c)
         ptx::tma_load_3d_elect(dst + c * L::kBoxBytes, &tm_q, bar_q + 8 * t,
-                               c * 64, mb * kBlockM + t * kTM, q_plane);
+                               c * 64, t ? m0_t[1] : m0_t[0],
+                               t ? plane_t[1] : plane_t[0]);
     }
     bool ok = true;
     int issued = 0;  // ring items (K_0, V_0, K_1, ...) issued so far
@@ -350,7 +360,8 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
       const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
       const uint32_t t_s = tmem + lane_off + t * kTN;
       const uint32_t t_o = tmem + lane_off + 2 * kTN + t * D;
-      const int m0 = mb * kBlockM + t * kTM;
+      const int m0 = t ? m0_t[1] : m0_t[0];
+      const int q_plane = t ? plane_t[1] : plane_t[0];
       const int row_pos = p.input_pos + m0 + r;  // absolute query position
       const float c = p.scale_log2;
       float m_run = -INFINITY;  // running max of scaled scores (log2 units)

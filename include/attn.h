@@ -63,7 +63,7 @@ typedef enum {
  * causal    0: every key is visible and input_pos is ignored;
  *           non-zero: key j is visible to query row i iff j <= input_pos + i.
  *           Queries with input_pos + i >= Skv - 1 see every key.
- * input_pos >= 0, and input_pos + Sq must fit in a signed 32-bit int.
+ * input_pos >= 0, and input_pos + Sq + 512 must fit in a signed 32-bit int.
  * dtype     ATTN_F16 or ATTN_BF16 (Q, K, V and O share it).
  * stream    the CUDA stream the kernel is enqueued on.
  *
