@@ -3,6 +3,7 @@
 // allocated here; the caller owns every buffer.
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 #include <cstdlib>
 #include <mutex>
 
@@ -28,6 +29,7 @@ cudaError_t g_encode_err = cudaSuccess;
 
 std::mutex g_status_mu;
 unsigned int* g_status_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   std::call_once(g_encode_once, [] {
@@ -51,6 +53,20 @@ unsigned int* status_ptr(int dev) {
     g_status_ptr[dev] = static_cast<unsigned int*>(p);
   }
   return g_status_ptr[dev];
+}
+
+// Streaming multiprocessors of a device (looked up once).
+int num_sms(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  if (g_num_sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+        cudaSuccess)
+      return 0;
+    g_num_sms[dev] = n;
+  }
+  return g_num_sms[dev];
 }
 
 unsigned long long timeout_ns() {
@@ -197,13 +213,15 @@ attn_status_t attn_fwd(const void* Q, const void* K, const void* V, void* O,
   unsigned int* status = status_ptr(dev);
   if (status == nullptr) return ATTN_ERR_CUDA;
 
-  CUtensorMap tq, tk, tv, to;
+  const int sms = num_sms(dev);
+  if (sms <= 0) return ATTN_ERR_CUDA;
+
+  CUtensorMap tq, tk, tv;
   const long long q_planes = static_cast<long long>(B) * Hq;
   const long long kv_planes = static_cast<long long>(B) * Hkv;
   if (!make_map(&tq, Q, dtype, D, Sq, q_planes) ||
       !make_map(&tk, K, dtype, D, Skv, kv_planes) ||
-      !make_map(&tv, V, dtype, D, Skv, kv_planes) ||
-      !make_map(&to, O, dtype, D, Sq, q_planes))
+      !make_map(&tv, V, dtype, D, Skv, kv_planes))
     return ATTN_ERR_CUDA;
 
   attn::FwdParams p{};
@@ -218,16 +236,19 @@ attn_status_t attn_fwd(const void* Q, const void* K, const void* V, void* O,
   p.pair_heads = pair_heads(s);
   p.scale_log2 = std::fabs(scale) * 1.4426950408889634f;
   p.negate_scores = scale < 0.f;
+  p.o = O;
   p.lse = LSE;
+  p.num_units = static_cast<int>(grid_size(s));
   p.status = status;
   p.timeout_ns = timeout_ns();
 
-  const int grid = static_cast<int>(grid_size(s));
+  // Persistent launch: at most one CTA per SM, each walking its units.
+  const int grid = static_cast<int>(std::min<long long>(grid_size(s), sms));
   const bool bf16 = dtype == ATTN_BF16;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t err =
-      D == 64 ? attn::launch_fwd_d64(bf16, tq, tk, tv, to, p, grid, cs)
-              : attn::launch_fwd_d128(bf16, tq, tk, tv, to, p, grid, cs);
+      D == 64 ? attn::launch_fwd_d64(bf16, tq, tk, tv, p, grid, cs)
+              : attn::launch_fwd_d128(bf16, tq, tk, tv, p, grid, cs);
   return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -6,8 +6,8 @@ namespace {
 
 template <bool kBF16>
 cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k,
-                   const CUtensorMap& v, const CUtensorMap& o,
-                   const FwdParams& p, int grid, cudaStream_t stream) {
+                   const CUtensorMap& v, const FwdParams& p, int grid,
+                   cudaStream_t stream) {
   auto kernel = attn_fwd_sm103_kernel<128, kBF16>;
   const int smem = Layout<128>::kSmemBytes;
   // The attribute is per device; setting it again is cheap and idempotent.
@@ -27,17 +27,16 @@ cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k,
   cfg.blockDim = dim3(cfg::kThreads, 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, kernel, q, k, v, o, p);
+  return cudaLaunchKernelEx(&cfg, kernel, q, k, v, p);
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_d128(bool bf16, const CUtensorMap& q,
                            const CUtensorMap& k, const CUtensorMap& v,
-                           const CUtensorMap& o, const FwdParams& p, int grid,
-                           cudaStream_t stream) {
-  return bf16 ? launch<true>(q, k, v, o, p, grid, stream)
-              : launch<false>(q, k, v, o, p, grid, stream);
+                           const FwdParams& p, int grid, cudaStream_t stream) {
+  return bf16 ? launch<true>(q, k, v, p, grid, stream)
+              : launch<false>(q, k, v, p, grid, stream);
 }
 
 }  // namespace attn

@@ -12,7 +12,7 @@
 // to K/V heads by integer division (section "Grouped-query attention"), and
 // query rows sit at absolute positions input_pos + i (the KV-cache offset).
 //
-// One CTA owns 256 query rows of one (batch, head) as two 128-row Q tiles.
+// A persistent CTA per SM walks work units of two 128-row Q tiles.
 // Roles (384 threads):
 //   warp  0    TMEM allocator and single-thread tcgen05.mma issuer
 //   warp  1    TMA producer: Q tiles once, then K_j, V_j into a slot ring
@@ -44,7 +44,9 @@ struct FwdParams {
   int pair_heads;          // a unit = 2 heads x 128 rows (else 1 head x 256)
   float scale_log2;        // |scale| * log2(e)
   int negate_scores;       // scale < 0: S is computed as -(Q K^T)
+  void* o;                 // [B, Hq, Sq, D] output (16-bit elements)
   float* lse;              // [B, Hq, Sq] or nullptr
+  int num_units;           // work units (pairs of 128-row Q tiles)
   unsigned int* status;    // device status word (timeouts)
   unsigned long long timeout_ns;
 };
@@ -75,8 +77,8 @@ struct Layout {
   static constexpr int kRingOff = kQOff + 2 * kTileBytes;
   static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
   // barriers: q_full[2], full[S], empty[S], s_full[2], p_full[2], o_full[2],
-  // drain[1]
-  static constexpr int kNumBars = 2 + 2 * kSlots + 2 + 2 + 2 + 1;
+  // drain[1], q_free[2]
+  static constexpr int kNumBars = 2 + 2 * kSlots + 2 + 2 + 2 + 1 + 2;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kSmemBytes = kBytes + 1024;  // slack for 1 KB alignment
@@ -128,12 +130,56 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// One work unit: two 128-row Q tiles.  With an even GQA group the tiles
+// are two query heads of one K/V group at the same rows (identical causal
+// extents and masks, shared K/V tiles); otherwise two consecutive row blocks
+// of one head.  Unit 0 is the heaviest causal m-block (the page's reversed
+// block order); consecutive units are consecutive heads, so the heads of a
+// K/V group run together and find K/V in L2.
+struct Unit {
+  int plane[2];  // [B*Hq] plane of each Q tile
+  int m0[2];     // first row of each Q tile
+  int n[2];      // K/V tiles each Q tile visits
+  int ms[2];     // first K/V tile that needs the mask
+  int kv_plane;  // [B*Hkv] plane of the shared K/V head
+  int n_kv;      // K/V tiles the unit streams
+};
+
+__device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
+  Unit w;
+  const int per_m = p.pair_heads ? p.B * (p.Hq / 2) : p.B * p.Hq;
+  const int mb = p.num_m_blocks - 1 - u / per_m;
+  const int ub = u % per_m;
+  const int b = p.pair_heads ? ub / (p.Hq / 2) : ub / p.Hq;
+  const int h0 = p.pair_heads ? 2 * (ub % (p.Hq / 2)) : ub % p.Hq;
+  w.kv_plane = b * p.Hkv + h0 / (p.Hq / p.Hkv);
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    w.plane[t] = b * p.Hq + h0 + (p.pair_heads ? t : 0);
+    w.m0[t] = p.pair_heads ? mb * cfg::kTM : mb * cfg::kBlockM + t * cfg::kTM;
+    tile_extent(p, w.m0[t], w.n[t], w.ms[t]);
+  }
+  w.n_kv = max(w.n[0], w.n[1]);
+  return w;
+}
+
+// k-th unit of CTA `cta` among `ctas`: rounds of `ctas` units, the CTA order
+// reversed every other round.  With units sorted heaviest first this keeps
+// the per-CTA totals within a few percent of the mean for causal masks
+// (plain round-robin gives every CTA's first pick of each round to CTA 0).
+__device__ __forceinline__ int unit_index(int k, int cta, int ctas) {
+  return k * ctas + ((k & 1) ? (ctas - 1 - cta) : cta);
+}
+
+// Persistent kernel: one CTA per SM walks its units (unit_index) in
+// rounds.  Barrier phases, the K/V ring position and
+// TMEM carry over from unit to unit, so the next unit's Q load and first
+// MMAs overlap the current unit's last MMAs and epilogue.
 template <int D, bool kBF16>
 __global__ void __launch_bounds__(cfg::kThreads, 1)
     attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v,
-                          const __grid_constant__ CUtensorMap tm_o,
                           const FwdParams p) {
   using L = Layout<D>;
   using namespace cfg;
@@ -151,35 +197,14 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
   const uint32_t bar_p = bar_s + 8 * 2;                // [2]
   const uint32_t bar_o = bar_p + 8 * 2;                // [2]
   const uint32_t bar_drain = bar_o + 8 * 2;            // [1]
+  const uint32_t bar_qfree = bar_drain + 8;            // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<int*>(smem + L::kMiscOff + 4);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-
-  // Work unit: two 128-row Q tiles.  With an even GQA group the tiles are
-  // two query heads of one K/V group at the same rows (identical causal
-  // extents and masks, shared K/V tiles); otherwise two consecutive row
-  // blocks of one head.  Heaviest causal m-blocks first (the page's reversed
-  // block order); consecutive units are consecutive heads, so the heads of
-  // a K/V group run together and find K/V in L2.
-  const int units_per_m = p.pair_heads ? p.B * (p.Hq / 2) : p.B * p.Hq;
-  const int mb = p.num_m_blocks - 1 - static_cast<int>(blockIdx.x) / units_per_m;
-  const int ub = static_cast<int>(blockIdx.x) % units_per_m;
-  const int b = p.pair_heads ? ub / (p.Hq / 2) : ub / p.Hq;
-  const int h0 = p.pair_heads ? 2 * (ub % (p.Hq / 2)) : ub % p.Hq;
-  const int kvh = h0 / (p.Hq / p.Hkv);
-  const int kv_plane = b * p.Hkv + kvh;
-  int plane_t[2], m0_t[2];  // [B*Hq] plane and first row of each Q tile
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    plane_t[t] = b * p.Hq + h0 + (p.pair_heads ? t : 0);
-    m0_t[t] = p.pair_heads ? mb * kTM : mb * kBlockM + t * kTM;
-  }
-  int n_t[2], ms_t[2];
-  tile_extent(p, m0_t[0], n_t[0], ms_t[0]);
-  tile_extent(p, m0_t[1], n_t[1], ms_t[1]);
-  const int n_kv = max(n_t[0], n_t[1]);
+  const int u_first = static_cast<int>(blockIdx.x);
+  const int u_step = static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     // P-ready barriers collect one arrival per softmax thread; the others
@@ -208,107 +233,134 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
       ptx::prefetch_tensormap(&tm_k);
       ptx::prefetch_tensormap(&tm_v);
     }
-    for (int t = 0; t < 2; ++t) {
-      if (n_t[t] == 0) continue;
-      const uint32_t dst = s_q + t * L::kTileBytes;
-      ptx::mbar_arrive_expect_tx_elect(bar_q + 8 * t, L::kTileBytes);
-      for (int c = 0; c < L::kChunks; ++c)
-        ptx::tma_load_3d_elect(dst + c * L::kBoxBytes, &tm_q, bar_q + 8 * t,
-                               c * 64, t ? m0_t[1] : m0_t[0],
-                               t ? plane_t[1] : plane_t[0]);
-    }
     bool ok = true;
-    int issued = 0;  // ring items (K_0, V_0, K_1, ...) issued so far
-    for (int j = 0; j < n_kv && ok; ++j) {
-      for (int kv = 0; kv < 2; ++kv) {
-        const int it = 2 * j + kv;
-        const int slot = it % L::kSlots;
-        if (it >= L::kSlots) {
-          ok = wait_bounded(bar_empty + 8 * slot, ((it / L::kSlots) - 1) & 1,
-                            abort_flag, p, 1);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
-        }
-        const uint32_t dst = s_ring + slot * L::kTileBytes;
-        ptx::mbar_arrive_expect_tx_elect(bar_full + 8 * slot, L::kTileBytes);
+    int it = 0;               // ring items (K_0, V_0, K_1, ...) issued so far
+    int q_loads[2] = {0, 0};  // Q tile loads issued so far, per tile
+    for (int k = 0; k * u_step < p.num_units && ok; ++k) {
+      const int u = unit_index(k, u_first, u_step);
+      if (u >= p.num_units) continue;
+      const Unit w = decode_unit(p, u);
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (w.n[t] == 0 || !ok) continue;
+        // The buffer is free once the previous unit's last S MMA on it is
+        // done (committed by the MMA warp to q_free).
+        if (q_loads[t] > 0)
+          ok = __all_sync(0xffffffffu,
+                          wait_bounded(bar_qfree + 8 * t, (q_loads[t] - 1) & 1,
+                                       abort_flag, p, 1));
+        if (!ok) break;
+        const uint32_t dst = s_q + t * L::kTileBytes;
+        ptx::mbar_arrive_expect_tx_elect(bar_q + 8 * t, L::kTileBytes);
         for (int c = 0; c < L::kChunks; ++c)
-          ptx::tma_load_3d_elect(dst + c * L::kBoxBytes, kv ? &tm_v : &tm_k,
-                                 bar_full + 8 * slot, c * 64, j * kTN,
-                                 kv_plane);
-        issued = it + 1;
+          ptx::tma_load_3d_elect(dst + c * L::kBoxBytes, &tm_q, bar_q + 8 * t,
+                                 c * 64, w.m0[t], w.plane[t]);
+        ++q_loads[t];
+      }
+      for (int j = 0; j < w.n_kv && ok; ++j) {
+        for (int kv = 0; kv < 2; ++kv) {
+          const int slot = it % L::kSlots;
+          if (it >= L::kSlots) {
+            ok = __all_sync(0xffffffffu,
+                            wait_bounded(bar_empty + 8 * slot,
+                                         ((it / L::kSlots) - 1) & 1,
+                                         abort_flag, p, 1));
+            if (!ok) break;
+          }
+          const uint32_t dst = s_ring + slot * L::kTileBytes;
+          ptx::mbar_arrive_expect_tx_elect(bar_full + 8 * slot, L::kTileBytes);
+          for (int c = 0; c < L::kChunks; ++c)
+            ptx::tma_load_3d_elect(dst + c * L::kBoxBytes, kv ? &tm_v : &tm_k,
+                                   bar_full + 8 * slot, c * 64, j * kTN,
+                                   w.kv_plane);
+          ++it;
+        }
       }
     }
     if (!ok) {
       // Let every copy still in flight land before the CTA goes away.
       for (int t = 0; t < 2; ++t)
-        if (n_t[t] > 0) drain_wait(bar_q + 8 * t, 0, p);
-      const int first = max(0, issued - L::kSlots);
-      for (int it = first; it < issued; ++it)
-        drain_wait(bar_full + 8 * (it % L::kSlots), (it / L::kSlots) & 1, p);
+        if (q_loads[t] > 0) drain_wait(bar_q + 8 * t, (q_loads[t] - 1) & 1, p);
+      for (int i = max(0, it - L::kSlots); i < it; ++i)
+        drain_wait(bar_full + 8 * (i % L::kSlots), (i / L::kSlots) & 1, p);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------ MMA issuer
     // The whole warp runs this loop (warp-uniform); one elected lane issues.
-    {
-      const uint32_t idesc_qk =
-          ptx::idesc_f16(kBF16, kTM, kTN, false, p.negate_scores != 0);
-      const uint32_t idesc_pv = ptx::idesc_f16(kBF16, kTM, D, true, false);
-      bool ok = true;
-      bool issued_any = false;
+    const uint32_t idesc_qk =
+        ptx::idesc_f16(kBF16, kTM, kTN, false, p.negate_scores != 0);
+    const uint32_t idesc_pv = ptx::idesc_f16(kBF16, kTM, D, true, false);
+    bool ok = true;
+    bool issued_any = false;
 
-      // Descriptor low words, computed once; per MMA one add of a
-      // compile-time offset.  K-major tiles: LBO unused (16), SBO = 1024
-      // (8 rows of 128 B).  V (MN-major): LBO = 16 KB between the 64-column
-      // halves of D, SBO = 1024 between groups of 8 keys.
-      constexpr uint32_t kHi = ptx::sdesc_hi_sw128(1024);
-      const uint32_t q_lo = ptx::sdesc_lo(s_q, 16);
-      const uint32_t k_lo = ptx::sdesc_lo(s_ring, 16);
-      const uint32_t v_lo = ptx::sdesc_lo(s_ring, L::kBoxBytes);
-      constexpr uint32_t kTile16 = L::kTileBytes >> 4;
+    // Descriptor low words, computed once; per MMA one add of a
+    // compile-time offset.  K-major tiles: LBO unused (16), SBO = 1024
+    // (8 rows of 128 B).  V (MN-major): LBO = 16 KB between the 64-column
+    // halves of D, SBO = 1024 between groups of 8 keys.
+    constexpr uint32_t kHi = ptx::sdesc_hi_sw128(1024);
+    const uint32_t q_lo = ptx::sdesc_lo(s_q, 16);
+    const uint32_t k_lo = ptx::sdesc_lo(s_ring, 16);
+    const uint32_t v_lo = ptx::sdesc_lo(s_ring, L::kBoxBytes);
+    constexpr uint32_t kTile16 = L::kTileBytes >> 4;
 
-      // S_t = Q_t K_j^T : A = Q tile (K-major), B = K tile (K-major).
-      auto issue_qk = [&](int t, int slot) {
-        const uint32_t a0 = q_lo + t * kTile16;
-        const uint32_t b0 = k_lo + slot * kTile16;
-        const uint32_t d = tmem + t * kTN;
+    // S_t = Q_t K_j^T : A = Q tile (K-major), B = K tile (K-major).
+    auto issue_qk = [&](int t, int slot) {
+      const uint32_t a0 = q_lo + t * kTile16;
+      const uint32_t b0 = k_lo + slot * kTile16;
+      const uint32_t d = tmem + t * kTN;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk / 4) * L::kBoxBytes + (kk % 4) * 32) >> 4;
-          ptx::mma_ss_elect(d, a0 + off, b0 + off, kHi, idesc_qk,
-                            kk > 0 ? 1u : 0u);
-        }
-      };
-      // O_t (+)= P_t V_j : A = P_t in TMEM, B = V tile (MN-major).
-      auto issue_pv = [&](int t, int slot, bool acc) {
-        const uint32_t b0 = v_lo + slot * kTile16;
-        const uint32_t d = tmem + 2 * kTN + t * D;
-        const uint32_t a = tmem + t * kTN;
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk / 4) * L::kBoxBytes + (kk % 4) * 32) >> 4;
+        ptx::mma_ss_elect(d, a0 + off, b0 + off, kHi, idesc_qk,
+                          kk > 0 ? 1u : 0u);
+      }
+    };
+    // O_t (+)= P_t V_j : A = P_t in TMEM, B = V tile (MN-major).
+    auto issue_pv = [&](int t, int slot, bool acc) {
+      const uint32_t b0 = v_lo + slot * kTile16;
+      const uint32_t d = tmem + 2 * kTN + t * D;
+      const uint32_t a = tmem + t * kTN;
 #pragma unroll
-        for (int kk = 0; kk < kTN / 16; ++kk) {
-          ptx::mma_ts_elect(d, a + kk * 8, b0 + ((kk * 16 * 128) >> 4), kHi,
-                            idesc_pv, (acc || kk > 0) ? 1u : 0u);
-        }
-      };
+      for (int kk = 0; kk < kTN / 16; ++kk) {
+        ptx::mma_ts_elect(d, a + kk * 8, b0 + ((kk * 16 * 128) >> 4), kHi,
+                          idesc_pv, (acc || kk > 0) ? 1u : 0u);
+      }
+    };
 
-      ok = __all_sync(0xffffffffu, wait_bounded(bar_full, 0, abort_flag, p, 2));  // K_0
+    int it = 0;               // ring items consumed so far
+    int q_uses[2] = {0, 0};   // Q tile loads consumed, per tile
+    int p_waits[2] = {0, 0};  // P-ready phases consumed, per tile
+    for (int k = 0; k * u_step < p.num_units && ok; ++k) {
+      const int u = unit_index(k, u_first, u_step);
+      if (u >= p.num_units) continue;
+      const Unit w = decode_unit(p, u);
+      // S_t = Q_t K_0^T for both tiles.
+      ok = __all_sync(0xffffffffu,
+                      wait_bounded(bar_full + 8 * (it % L::kSlots),
+                                   (it / L::kSlots) & 1, abort_flag, p, 2));
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (!ok) break;
-        if (n_t[t] == 0) continue;
-        ok = __all_sync(0xffffffffu, wait_bounded(bar_q + 8 * t, 0, abort_flag, p, 2));
+        if (w.n[t] == 0) continue;
+        ok = __all_sync(0xffffffffu,
+                        wait_bounded(bar_q + 8 * t, q_uses[t] & 1, abort_flag,
+                                     p, 2));
         if (!ok) break;
+        ++q_uses[t];
         ptx::tc_fence_after();
-        issue_qk(t, 0);
+        issue_qk(t, it % L::kSlots);
         ptx::tc_commit_elect(bar_s + 8 * t);
+        if (w.n[t] == 1) ptx::tc_commit_elect(bar_qfree + 8 * t);
         issued_any = true;
       }
-      if (ok) ptx::tc_commit_elect(bar_empty + 0);
-
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int it_v = 2 * j + 1;
+      if (!ok) break;
+      ptx::tc_commit_elect(bar_empty + 8 * (it % L::kSlots));
+      const int it0 = it;
+      for (int j = 0; j < w.n_kv && ok; ++j) {
+        const int it_v = it0 + 2 * j + 1;
         const int slot_v = it_v % L::kSlots;
-        const int it_k = 2 * j + 2;
+        const int it_k = it0 + 2 * j + 2;
         const int slot_k = it_k % L::kSlots;
         ok = __all_sync(0xffffffffu,
                         wait_bounded(bar_full + 8 * slot_v,
@@ -318,13 +370,15 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok) break;
-          if (j >= n_t[t]) continue;
+          if (j >= w.n[t]) continue;
           ok = __all_sync(0xffffffffu,
-                          wait_bounded(bar_p + 8 * t, j & 1, abort_flag, p, 2));
+                          wait_bounded(bar_p + 8 * t, p_waits[t] & 1,
+                                       abort_flag, p, 2));
           if (!ok) break;
+          ++p_waits[t];
           ptx::tc_fence_after();
           issue_pv(t, slot_v, j > 0);
-          if (j == n_t[t] - 1) {
+          if (j == w.n[t] - 1) {
             ptx::tc_commit_elect(bar_o + 8 * t);
           } else {
             if (!k_ready) {
@@ -337,41 +391,52 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
             }
             issue_qk(t, slot_k);
             ptx::tc_commit_elect(bar_s + 8 * t);
+            // After the tile's last S MMA, its Q buffer can be refilled.
+            if (j + 1 == w.n[t] - 1) ptx::tc_commit_elect(bar_qfree + 8 * t);
           }
         }
         if (!ok) break;
         ptx::tc_commit_elect(bar_empty + 8 * slot_v);
-        if (j + 1 < n_kv) ptx::tc_commit_elect(bar_empty + 8 * slot_k);
+        if (j + 1 < w.n_kv) ptx::tc_commit_elect(bar_empty + 8 * slot_k);
       }
-      if (!ok && issued_any) {
-        // Wait for the MMAs already issued before TMEM is released.
-        ptx::tc_commit_elect(bar_drain);
-        drain_wait(bar_drain, 0, p);
-      }
+      it = it0 + 2 * w.n_kv;
+    }
+    if (!ok && issued_any) {
+      // Wait for the MMAs already issued before TMEM is released.
+      ptx::tc_commit_elect(bar_drain);
+      drain_wait(bar_drain, 0, p);
     }
     __syncwarp();
   } else if (warp >= kSoftmaxWarp0) {
     // ------------------------------------- softmax / correction / epilogue
     const int t = warp / 4 - 1;             // Q tile of this warpgroup
     const int r = threadIdx.x % 128;        // row within the tile
-    const int n = t == 0 ? n_t[0] : n_t[1];
-    const int ms = t == 0 ? ms_t[0] : ms_t[1];
-    if (n > 0) {
-      const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
-      const uint32_t t_s = tmem + lane_off + t * kTN;
-      const uint32_t t_o = tmem + lane_off + 2 * kTN + t * D;
-      const int m0 = t ? m0_t[1] : m0_t[0];
-      const int q_plane = t ? plane_t[1] : plane_t[0];
+    const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + t * kTN;
+    const uint32_t t_o = tmem + lane_off + 2 * kTN + t * D;
+    const float c = p.scale_log2;
+    bool ok = true;
+    int s_waits = 0;  // S-ready phases consumed
+    int o_waits = 0;  // O-done phases consumed
+
+    for (int k = 0; k * u_step < p.num_units && ok; ++k) {
+      const int u = unit_index(k, u_first, u_step);
+      if (u >= p.num_units) continue;
+      const Unit w = decode_unit(p, u);
+      const int n = t ? w.n[1] : w.n[0];
+      if (n == 0) continue;
+      const int ms = t ? w.ms[1] : w.ms[0];
+      const int m0 = t ? w.m0[1] : w.m0[0];
+      const int q_plane = t ? w.plane[1] : w.plane[0];
       const int row_pos = p.input_pos + m0 + r;  // absolute query position
-      const float c = p.scale_log2;
       float m_run = -INFINITY;  // running max of scaled scores (log2 units)
       float l_run = 0.f;        // running sum of 2^(s*c - m_run)
-      bool ok = true;
 
       for (int j = 0; j < n; ++j) {
-        ok = wait_bounded(bar_s + 8 * t, j & 1, abort_flag, p, 3);
-        ok = __all_sync(0xffffffffu, ok);
+        ok = __all_sync(0xffffffffu, wait_bounded(bar_s + 8 * t, s_waits & 1,
+                                                  abort_flag, p, 3));
         if (!ok) break;
+        ++s_waits;
         ptx::tc_fence_after();
 
         // Pass 1: row maximum of the scaled scores over the visible keys.
@@ -488,52 +553,40 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar_p + 8 * t);
       }
+      if (!ok) break;
 
       // ---------------------------------------------------------- epilogue
-      if (ok) {
-        ok = wait_bounded(bar_o + 8 * t, 0, abort_flag, p, 4);
-        ok = __all_sync(0xffffffffu, ok);
-      }
-      const uint32_t stage = s_q + t * L::kTileBytes;  // Q_t is no longer read
-      if (ok) {
-        ptx::tc_fence_after();
-        const float inv_l = ptx::rcp(l_run);
+      // O / l in 16 bits straight from registers to global memory: each
+      // thread owns one 2*D-byte row (rows >= Sq are not stored).  The next
+      // unit's MMAs into S_t may already run; the next PV into O_t waits for
+      // this warpgroup's next P, so the reads below come first.
+      ok = __all_sync(0xffffffffu, wait_bounded(bar_o + 8 * t, o_waits & 1,
+                                                abort_flag, p, 4));
+      if (!ok) break;
+      ++o_waits;
+      ptx::tc_fence_after();
+      const float inv_l = ptx::rcp(l_run);
+      const bool row_ok = m0 + r < p.Sq;
+      const long long row = static_cast<long long>(q_plane) * p.Sq + m0 + r;
+      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + row * D);
 #pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
-          uint32_t o[32];
-          ptx::tmem_ld32(t_o + 32 * q, o);
-          ptx::tmem_wait_ld();
+      for (int q = 0; q < D / 32; ++q) {
+        uint32_t o[32];
+        ptx::tmem_ld32(t_o + 32 * q, o);
+        ptx::tmem_wait_ld();
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint32_t w[4];
+        for (int v = 0; v < 4; ++v) {
+          uint32_t wv[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              w[e] = ptx::pack2<kBF16>(
-                  __uint_as_float(o[8 * v + 2 * e]) * inv_l,
-                  __uint_as_float(o[8 * v + 2 * e + 1]) * inv_l);
-            const int col = 32 * q + 8 * v;          // first element
-            const int box = col / 64;
-            const int unit = (col % 64) / 8;         // 16-byte unit in row
-            const uint32_t addr = stage + box * L::kBoxBytes + r * 128 +
-                                  ((unit ^ (r & 7)) * 16);
-            ptx::st_shared_v4(addr, w[0], w[1], w[2], w[3]);
-          }
-        }
-        if (p.lse != nullptr && m0 + r < p.Sq) {
-          const long long row =
-              (static_cast<long long>(q_plane) * p.Sq) + m0 + r;
-          p.lse[row] = (m_run + ptx::lg2(l_run)) * kLn2;
+          for (int e = 0; e < 4; ++e)
+            wv[e] = ptx::pack2<kBF16>(__uint_as_float(o[8 * v + 2 * e]) * inv_l,
+                                      __uint_as_float(o[8 * v + 2 * e + 1]) * inv_l);
+          if (row_ok) orow[4 * q + v] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
       }
-      ptx::fence_proxy_async_smem();
-      ptx::named_barrier_sync(1 + t, 128);
-      if (r == 0 && !*abort_flag) {
-        for (int cidx = 0; cidx < L::kChunks; ++cidx)
-          ptx::tma_store_3d(&tm_o, stage + cidx * L::kBoxBytes, cidx * 64, m0,
-                            q_plane);
-        ptx::bulk_commit_group();
-        ptx::bulk_wait_group_all();
-      }
+      if (p.lse != nullptr && row_ok)
+        p.lse[row] = (m_run + ptx::lg2(l_run)) * kLn2;
+      ptx::tc_fence_before();
     }
   }
 

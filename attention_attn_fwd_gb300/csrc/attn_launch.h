@@ -16,11 +16,9 @@ int fwd_stages(int D);
 
 cudaError_t launch_fwd_d64(bool bf16, const CUtensorMap& q,
                            const CUtensorMap& k, const CUtensorMap& v,
-                           const CUtensorMap& o, const FwdParams& p, int grid,
-                           cudaStream_t stream);
+                           const FwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_fwd_d128(bool bf16, const CUtensorMap& q,
                             const CUtensorMap& k, const CUtensorMap& v,
-                            const CUtensorMap& o, const FwdParams& p, int grid,
-                            cudaStream_t stream);
+                            const FwdParams& p, int grid, cudaStream_t stream);
 
 }  // namespace attn

@@ -95,7 +95,9 @@ attn_status_t attn_device_status(unsigned int* code);
  * arguments (host only, no GPU needed).  Fills, when non-NULL:
  *   block_m   query rows per CTA, block_n keys per K/V tile,
  *   stages    K/V tiles the shared-memory ring holds,
- *   grid      CTAs launched, smem_bytes dynamic shared memory per CTA.
+ *   grid      work units (each 2 x 128 query rows); the launch runs
+ *             min(grid, SM count) persistent CTAs that walk them,
+ *   smem_bytes dynamic shared memory per CTA.
  * Returns the same validation code attn_fwd would (pointers not checked).
  */
 attn_status_t attn_tile_config(int B, int Hq, int Hkv, int Sq, int Skv, int D,
