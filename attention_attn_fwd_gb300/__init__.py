@@ -15,8 +15,9 @@ import os
 import threading
 
 __all__ = [
-    "ATTN_F16", "ATTN_BF16", "AttnError", "attn_fwd", "attn_status_string",
-    "attn_device_status", "attn_tile_config", "attn_version", "fwd",
+    "ATTN_F16", "ATTN_BF16", "AttnError", "attn_fwd", "attn_fwd_splitkv",
+    "attn_splitkv_plan", "attn_status_string", "attn_device_status",
+    "attn_tile_config", "attn_version", "fwd", "fwd_splitkv",
     "library_path", "load_library",
 ]
 
@@ -73,6 +74,14 @@ def load_library():
         lib.attn_tile_config.restype = i
         lib.attn_version.argtypes = []
         lib.attn_version.restype = i
+        sz = ctypes.c_size_t
+        lib.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i,
+                                         ctypes.c_float, i, i, i, i, vp, sz,
+                                         vp]
+        lib.attn_fwd_splitkv.restype = i
+        lib.attn_splitkv_plan.argtypes = [i, i, i, i, i, i, i, i, i, ip,
+                                          ctypes.POINTER(sz)]
+        lib.attn_splitkv_plan.restype = i
         _lib = lib
         return lib
 
@@ -84,6 +93,30 @@ def attn_fwd(Q, K, V, O, LSE, B, Hq, Hkv, Sq, Skv, D, scale, causal,
         Q or None, K or None, V or None, O or None, LSE or None, B, Hq, Hkv,
         Sq, Skv, D, float(scale), int(causal), int(input_pos), int(dtype),
         stream or None))
+
+
+def attn_fwd_splitkv(Q, K, V, O, LSE, B, Hq, Hkv, Sq, Skv, D, scale, causal,
+                     input_pos, dtype, num_splits, workspace, workspace_bytes,
+                     stream) -> int:
+    """Raw C-ABI call of the split-KV forward; pointers are integers."""
+    return int(load_library().attn_fwd_splitkv(
+        Q or None, K or None, V or None, O or None, LSE or None, B, Hq, Hkv,
+        Sq, Skv, D, float(scale), int(causal), int(input_pos), int(dtype),
+        int(num_splits), workspace or None, int(workspace_bytes),
+        stream or None))
+
+
+def attn_splitkv_plan(B, Hq, Hkv, Sq, Skv, D, causal, input_pos, dtype,
+                      num_splits=0):
+    """(num_splits, workspace_bytes) attn_fwd_splitkv accepts."""
+    ns = ctypes.c_int(int(num_splits))
+    ws = ctypes.c_size_t(0)
+    st = int(load_library().attn_splitkv_plan(
+        B, Hq, Hkv, Sq, Skv, D, int(causal), int(input_pos), int(dtype),
+        ctypes.byref(ns), ctypes.byref(ws)))
+    if st != ATTN_OK:
+        raise AttnError("attn_splitkv_plan: " + attn_status_string(st), st)
+    return ns.value, ws.value
 
 
 def attn_status_string(status: int) -> str:
@@ -165,4 +198,49 @@ def fwd(q, k, v, scale=None, causal=True, input_pos=0, out=None, lse=None,
                       stream.cuda_stream)
     if st != ATTN_OK:
         raise AttnError("attn_fwd: " + attn_status_string(st), st)
+    return out, (lse if need_lse else None)
+
+
+def fwd_splitkv(q, k, v, scale=None, causal=True, input_pos=0, num_splits=0,
+                workspace=None, out=None, lse=None, need_lse=True,
+                stream=None):
+    """Split-KV attention forward (few query rows over a long key range).
+
+    Same tensors and result as ``fwd``.  ``num_splits`` <= 0 lets the
+    library choose; ``workspace`` (a CUDA tensor of at least the planned
+    size, 256-byte aligned) is allocated with torch when not given.
+    """
+    import torch
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise AttnError("q, k, v must be 4-D [B, H, S, D]",
+                        ATTN_ERR_INVALID_ARG)
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise AttnError("q, k, v must be contiguous CUDA tensors",
+                            ATTN_ERR_INVALID_ARG)
+    dt = _dtype_code(q)
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Skv, _ = k.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(q.device):
+        splits, ws_bytes = attn_splitkv_plan(B, Hq, Hkv, Sq, Skv, D, causal,
+                                             input_pos, dt, num_splits)
+        if workspace is None:
+            workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8,
+                                    device=q.device)
+        if out is None:
+            out = torch.empty_like(q)
+        if need_lse and lse is None:
+            lse = torch.empty((B, Hq, Sq), dtype=torch.float32,
+                              device=q.device)
+        if stream is None:
+            stream = torch.cuda.current_stream(q.device)
+        st = attn_fwd_splitkv(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+            lse.data_ptr() if need_lse else 0, B, Hq, Hkv, Sq, Skv, D, scale,
+            causal, input_pos, dt, splits, workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), stream.cuda_stream)
+    if st != ATTN_OK:
+        raise AttnError("attn_fwd_splitkv: " + attn_status_string(st), st)
     return out, (lse if need_lse else None)

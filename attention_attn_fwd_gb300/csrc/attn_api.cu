@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdint>
 #include <algorithm>
+#include <cstddef>
 #include <cstdlib>
 #include <mutex>
 
@@ -180,6 +181,114 @@ int fwd_stages(int D) {
 }
 }  // namespace attn
 
+namespace {
+
+constexpr int kMaxSplits = 128;
+constexpr size_t kWorkspaceAlign = 256;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Bytes of the split-KV workspace: fp32 partial outputs, then partial LSEs.
+size_t splitkv_bytes(const Shape& s, int splits) {
+  const size_t rows = static_cast<size_t>(s.B) * s.Hq * s.Sq;
+  return round_up(static_cast<size_t>(splits) * rows * s.D * 4, kWorkspaceAlign) +
+         round_up(static_cast<size_t>(splits) * rows * 4, kWorkspaceAlign);
+}
+
+// Split count and K/V tiles per split.  `splits` <= 0 picks enough splits
+// to give every SM a unit (at most kMaxSplits, at least one tile each).
+void splitkv_shape(const Shape& s, int splits, int sms, int* out_splits,
+                   int* out_tiles) {
+  const int tiles = (s.Skv + attn::cfg::kTN - 1) / attn::cfg::kTN;
+  if (splits <= 0) {
+    const long long units = grid_size(s);
+    splits = units >= sms ? 1 : static_cast<int>((sms + units - 1) / units);
+  }
+  splits = std::max(1, std::min({splits, tiles, kMaxSplits}));
+  const int per = (tiles + splits - 1) / splits;
+  *out_tiles = per;
+  *out_splits = (tiles + per - 1) / per;  // no empty trailing range
+}
+
+// Checks shared by the entry points; fills the device, status word and SMs.
+attn_status_t check_call(const Shape& s, float scale, attn_dtype_t dtype,
+                         const void* Q, const void* K, const void* V, void* O,
+                         float* LSE, int* dev, unsigned int** status,
+                         int* sms) {
+  attn_status_t st = check_scalars(s, scale, dtype);
+  if (st != ATTN_OK) return st;
+  if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  auto misaligned = [](const void* p, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(p) % a) != 0;
+  };
+  if (misaligned(Q, 16) || misaligned(K, 16) || misaligned(V, 16) ||
+      misaligned(O, 16) || (LSE != nullptr && misaligned(LSE, 4)))
+    return ATTN_ERR_ALIGNMENT;
+  const size_t q_bytes = static_cast<size_t>(s.B) * s.Hq * s.Sq * s.D * 2;
+  const size_t kv_bytes = static_cast<size_t>(s.B) * s.Hkv * s.Skv * s.D * 2;
+  if (overlaps(O, q_bytes, Q, q_bytes) || overlaps(O, q_bytes, K, kv_bytes) ||
+      overlaps(O, q_bytes, V, kv_bytes))
+    return ATTN_ERR_INVALID_ARG;
+  if (cudaGetDevice(dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (!is_device_ptr(Q, *dev) || !is_device_ptr(K, *dev) ||
+      !is_device_ptr(V, *dev) || !is_device_ptr(O, *dev) ||
+      (LSE != nullptr && !is_device_ptr(LSE, *dev)))
+    return ATTN_ERR_INVALID_ARG;
+  *status = status_ptr(*dev);
+  if (*status == nullptr) return ATTN_ERR_CUDA;
+  *sms = num_sms(*dev);
+  if (*sms <= 0) return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+// Builds the tensor maps and parameters and launches the forward kernel.
+attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
+                             const void* V, void* O, float* LSE, float scale,
+                             attn_dtype_t dtype, unsigned int* status, int sms,
+                             int splits, int split_tiles, float* o_part,
+                             float* lse_part, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv;
+  const long long q_planes = static_cast<long long>(s.B) * s.Hq;
+  const long long kv_planes = static_cast<long long>(s.B) * s.Hkv;
+  if (!make_map(&tq, Q, dtype, s.D, s.Sq, q_planes) ||
+      !make_map(&tk, K, dtype, s.D, s.Skv, kv_planes) ||
+      !make_map(&tv, V, dtype, s.D, s.Skv, kv_planes))
+    return ATTN_ERR_CUDA;
+
+  attn::FwdParams p{};
+  p.B = s.B;
+  p.Hq = s.Hq;
+  p.Hkv = s.Hkv;
+  p.Sq = s.Sq;
+  p.Skv = s.Skv;
+  p.causal = s.causal != 0;
+  p.input_pos = s.causal != 0 ? s.input_pos : 0;
+  p.num_m_blocks = static_cast<int>(m_blocks(s));
+  p.pair_heads = pair_heads(s);
+  p.scale_log2 = std::fabs(scale) * 1.4426950408889634f;
+  p.negate_scores = scale < 0.f;
+  p.o = O;
+  p.lse = LSE;
+  p.num_splits = splits;
+  p.split_tiles = split_tiles;
+  p.o_part = o_part;
+  p.lse_part = lse_part;
+  p.num_units = static_cast<int>(grid_size(s) * splits);
+  p.status = status;
+  p.timeout_ns = timeout_ns();
+
+  // Persistent launch: at most one CTA per SM, each walking its units.
+  const int grid = static_cast<int>(std::min<long long>(p.num_units, sms));
+  const bool bf16 = dtype == ATTN_BF16;
+  const cudaError_t err =
+      s.D == 64 ? attn::launch_fwd_d64(bf16, tq, tk, tv, p, grid, stream)
+                : attn::launch_fwd_d128(bf16, tq, tk, tv, p, grid, stream);
+  return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
 extern "C" {
 
 attn_status_t attn_fwd(const void* Q, const void* K, const void* V, void* O,
@@ -190,65 +299,73 @@ attn_status_t attn_fwd(const void* Q, const void* K, const void* V, void* O,
   attn_status_t st = check_scalars(s, scale, dtype);
   if (st != ATTN_OK) return st;
   if (B == 0 || Sq == 0) return ATTN_OK;
-  if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr)
-    return ATTN_ERR_INVALID_ARG;
-  auto misaligned = [](const void* p, uintptr_t a) {
-    return (reinterpret_cast<uintptr_t>(p) % a) != 0;
-  };
-  if (misaligned(Q, 16) || misaligned(K, 16) || misaligned(V, 16) ||
-      misaligned(O, 16) || (LSE != nullptr && misaligned(LSE, 4)))
+  int dev = 0, sms = 0;
+  unsigned int* status = nullptr;
+  st = check_call(s, scale, dtype, Q, K, V, O, LSE, &dev, &status, &sms);
+  if (st != ATTN_OK) return st;
+  const int tiles = (Skv + attn::cfg::kTN - 1) / attn::cfg::kTN;
+  return launch_forward(s, Q, K, V, O, LSE, scale, dtype, status, sms, 1,
+                        tiles, nullptr, nullptr,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_splitkv_plan(int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                                int causal, int input_pos, attn_dtype_t dtype,
+                                int* num_splits, size_t* workspace_bytes) {
+  const Shape s{B, Hq, Hkv, Sq, Skv, D, causal != 0, input_pos};
+  const attn_status_t st = check_scalars(s, 1.0f, dtype);
+  if (st != ATTN_OK) return st;
+  if (num_splits == nullptr) return ATTN_ERR_INVALID_ARG;
+  int sms = 0;
+  if (*num_splits <= 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    sms = num_sms(dev);
+    if (sms <= 0) return ATTN_ERR_CUDA;
+  }
+  int splits = 0, tiles = 0;
+  splitkv_shape(s, *num_splits, sms, &splits, &tiles);
+  *num_splits = splits;
+  if (workspace_bytes != nullptr) *workspace_bytes = splitkv_bytes(s, splits);
+  return ATTN_OK;
+}
+
+attn_status_t attn_fwd_splitkv(const void* Q, const void* K, const void* V,
+                               void* O, float* LSE, int B, int Hq, int Hkv,
+                               int Sq, int Skv, int D, float scale, int causal,
+                               int input_pos, attn_dtype_t dtype,
+                               int num_splits, void* workspace,
+                               size_t workspace_bytes, attn_stream_t stream) {
+  const Shape s{B, Hq, Hkv, Sq, Skv, D, causal != 0, input_pos};
+  attn_status_t st = check_scalars(s, scale, dtype);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || Sq == 0) return ATTN_OK;
+  if (num_splits < 1 || num_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  unsigned int* status = nullptr;
+  st = check_call(s, scale, dtype, Q, K, V, O, LSE, &dev, &status, &sms);
+  if (st != ATTN_OK) return st;
+  int splits = 0, tiles = 0;
+  splitkv_shape(s, num_splits, sms, &splits, &tiles);
+  if (splits != num_splits) return ATTN_ERR_INVALID_ARG;  // not a planned count
+  if (workspace == nullptr ||
+      reinterpret_cast<uintptr_t>(workspace) % kWorkspaceAlign != 0)
     return ATTN_ERR_ALIGNMENT;
-  const size_t q_bytes = static_cast<size_t>(B) * Hq * Sq * D * 2;
-  const size_t kv_bytes = static_cast<size_t>(B) * Hkv * Skv * D * 2;
-  if (overlaps(O, q_bytes, Q, q_bytes) || overlaps(O, q_bytes, K, kv_bytes) ||
-      overlaps(O, q_bytes, V, kv_bytes))
-    return ATTN_ERR_INVALID_ARG;
-
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
-  if (!is_device_ptr(Q, dev) || !is_device_ptr(K, dev) ||
-      !is_device_ptr(V, dev) || !is_device_ptr(O, dev) ||
-      (LSE != nullptr && !is_device_ptr(LSE, dev)))
-    return ATTN_ERR_INVALID_ARG;
-  unsigned int* status = status_ptr(dev);
-  if (status == nullptr) return ATTN_ERR_CUDA;
-
-  const int sms = num_sms(dev);
-  if (sms <= 0) return ATTN_ERR_CUDA;
-
-  CUtensorMap tq, tk, tv;
-  const long long q_planes = static_cast<long long>(B) * Hq;
-  const long long kv_planes = static_cast<long long>(B) * Hkv;
-  if (!make_map(&tq, Q, dtype, D, Sq, q_planes) ||
-      !make_map(&tk, K, dtype, D, Skv, kv_planes) ||
-      !make_map(&tv, V, dtype, D, Skv, kv_planes))
-    return ATTN_ERR_CUDA;
-
-  attn::FwdParams p{};
-  p.B = B;
-  p.Hq = Hq;
-  p.Hkv = Hkv;
-  p.Sq = Sq;
-  p.Skv = Skv;
-  p.causal = causal != 0;
-  p.input_pos = causal != 0 ? input_pos : 0;
-  p.num_m_blocks = static_cast<int>(m_blocks(s));
-  p.pair_heads = pair_heads(s);
-  p.scale_log2 = std::fabs(scale) * 1.4426950408889634f;
-  p.negate_scores = scale < 0.f;
-  p.o = O;
-  p.lse = LSE;
-  p.num_units = static_cast<int>(grid_size(s));
-  p.status = status;
-  p.timeout_ns = timeout_ns();
-
-  // Persistent launch: at most one CTA per SM, each walking its units.
-  const int grid = static_cast<int>(std::min<long long>(grid_size(s), sms));
-  const bool bf16 = dtype == ATTN_BF16;
+  if (workspace_bytes < splitkv_bytes(s, splits)) return ATTN_ERR_INVALID_ARG;
+  if (!is_device_ptr(workspace, dev)) return ATTN_ERR_INVALID_ARG;
+  const size_t rows = static_cast<size_t>(B) * Hq * Sq;
+  float* o_part = static_cast<float*>(workspace);
+  float* lse_part = reinterpret_cast<float*>(
+      static_cast<char*>(workspace) +
+      round_up(static_cast<size_t>(splits) * rows * D * 4, kWorkspaceAlign));
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  const cudaError_t err =
-      D == 64 ? attn::launch_fwd_d64(bf16, tq, tk, tv, p, grid, cs)
-              : attn::launch_fwd_d128(bf16, tq, tk, tv, p, grid, cs);
+  st = launch_forward(s, Q, K, V, O, LSE, scale, dtype, status, sms, splits,
+                      tiles, o_part, lse_part, cs);
+  if (st != ATTN_OK) return st;
+  const cudaError_t err = attn::launch_splitkv_combine(
+      D, dtype == ATTN_BF16, o_part, lse_part, O, LSE,
+      static_cast<long long>(rows), Sq, splits, tiles * attn::cfg::kTN, Skv,
+      causal != 0, causal != 0 ? input_pos : 0, cs);
   return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -46,7 +46,15 @@ struct FwdParams {
   int negate_scores;       // scale < 0: S is computed as -(Q K^T)
   void* o;                 // [B, Hq, Sq, D] output (16-bit elements)
   float* lse;              // [B, Hq, Sq] or nullptr
-  int num_units;           // work units (pairs of 128-row Q tiles)
+  int num_units;           // work units (pairs of 128-row Q tiles x splits)
+  // Split-KV: the keys are cut into num_splits ranges of split_tiles K/V
+  // tiles; unit (tiles, split) writes normalised fp32 partial outputs and
+  // natural-log LSEs of its key range to o_part / lse_part (num_splits == 1
+  // and o_part == nullptr: the plain forward pass writing O and LSE).
+  int num_splits;
+  int split_tiles;
+  float* o_part;           // [num_splits, B*Hq, Sq, D]
+  float* lse_part;         // [num_splits, B*Hq, Sq]
   unsigned int* status;    // device status word (timeouts)
   unsigned long long timeout_ns;
 };
@@ -84,17 +92,18 @@ struct Layout {
   static constexpr int kSmemBytes = kBytes + 1024;  // slack for 1 KB alignment
 };
 
-// Keys [0, n*128) are visited; tiles j >= ms need the mask.
-__device__ __forceinline__ void tile_extent(const FwdParams& p, int m0, int& n,
+// K/V tiles [kt0, kt0 + n) of the key range [kt0, kt1) are visited by the
+// 128-row Q tile starting at m0; tiles with index >= ms need the mask.
+__device__ __forceinline__ void tile_extent(const FwdParams& p, int m0,
+                                            int kt0, int kt1, int& n,
                                             int& ms) {
-  if (m0 >= p.Sq) {
-    n = 0;
-    ms = 0;
-    return;
-  }
+  n = 0;
+  ms = 0;
+  if (m0 >= p.Sq) return;
   const int rows_end = min(m0 + cfg::kTM, p.Sq);
   const int kend = p.causal ? min(p.input_pos + rows_end, p.Skv) : p.Skv;
-  n = (kend + cfg::kTN - 1) / cfg::kTN;
+  const int t_end = min((kend + cfg::kTN - 1) / cfg::kTN, kt1);
+  n = max(0, t_end - kt0);
   const int full_tiles = p.Skv / cfg::kTN;
   ms = p.causal ? min((p.input_pos + m0 + 1) / cfg::kTN, full_tiles)
                 : full_tiles;
@@ -137,6 +146,8 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity,
 // block order); consecutive units are consecutive heads, so the heads of a
 // K/V group run together and find K/V in L2.
 struct Unit {
+  int kt0;       // first K/V tile of the unit's key range
+  int split;     // key-range index (0 without split-KV)
   int plane[2];  // [B*Hq] plane of each Q tile
   int m0[2];     // first row of each Q tile
   int n[2];      // K/V tiles each Q tile visits
@@ -147,6 +158,10 @@ struct Unit {
 
 __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   Unit w;
+  w.split = u % p.num_splits;
+  u /= p.num_splits;
+  w.kt0 = w.split * p.split_tiles;
+  const int kt1 = w.kt0 + p.split_tiles;
   const int per_m = p.pair_heads ? p.B * (p.Hq / 2) : p.B * p.Hq;
   const int mb = p.num_m_blocks - 1 - u / per_m;
   const int ub = u % per_m;
@@ -157,7 +172,7 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   for (int t = 0; t < 2; ++t) {
     w.plane[t] = b * p.Hq + h0 + (p.pair_heads ? t : 0);
     w.m0[t] = p.pair_heads ? mb * cfg::kTM : mb * cfg::kBlockM + t * cfg::kTM;
-    tile_extent(p, w.m0[t], w.n[t], w.ms[t]);
+    tile_extent(p, w.m0[t], w.kt0, kt1, w.n[t], w.ms[t]);
   }
   w.n_kv = max(w.n[0], w.n[1]);
   return w;
@@ -271,8 +286,8 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
           ptx::mbar_arrive_expect_tx_elect(bar_full + 8 * slot, L::kTileBytes);
           for (int c = 0; c < L::kChunks; ++c)
             ptx::tma_load_3d_elect(dst + c * L::kBoxBytes, kv ? &tm_v : &tm_k,
-                                   bar_full + 8 * slot, c * 64, j * kTN,
-                                   w.kv_plane);
+                                   bar_full + 8 * slot, c * 64,
+                                   (w.kt0 + j) * kTN, w.kv_plane);
           ++it;
         }
       }
@@ -335,6 +350,9 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
       const int u = unit_index(k, u_first, u_step);
       if (u >= p.num_units) continue;
       const Unit w = decode_unit(p, u);
+      // A key range wholly past the causal horizon of both tiles has no
+      // work (split-KV only); the producer and softmax warps skip it too.
+      if (w.n_kv == 0) continue;
       // S_t = Q_t K_0^T for both tiles.
       ok = __all_sync(0xffffffffu,
                       wait_bounded(bar_full + 8 * (it % L::kSlots),
@@ -441,11 +459,11 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
 
         // Pass 1: row maximum of the scaled scores over the visible keys.
         // Visible keys of this row in the tile are the columns < lim: key <
-        // Skv, and key <= row_pos when causal (only tiles j >= ms can cut).
-        const bool masked = j >= ms;
+        // Skv, and key <= row_pos when causal (only tiles >= ms can cut).
+        const bool masked = w.kt0 + j >= ms;
         int lim = kTN;
         if (masked) {
-          const int kbase = j * kTN;
+          const int kbase = (w.kt0 + j) * kTN;
           lim = min(kTN, p.Skv - kbase);
           if (p.causal) lim = min(lim, row_pos - kbase + 1);
         }
@@ -565,27 +583,57 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
       if (!ok) break;
       ++o_waits;
       ptx::tc_fence_after();
-      const float inv_l = ptx::rcp(l_run);
       const bool row_ok = m0 + r < p.Sq;
-      const long long row = static_cast<long long>(q_plane) * p.Sq + m0 + r;
-      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + row * D);
+      if (p.o_part == nullptr) {
+        const float inv_l = ptx::rcp(l_run);
+        const long long row = static_cast<long long>(q_plane) * p.Sq + m0 + r;
+        uint4* orow =
+            reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + row * D);
 #pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
-        uint32_t o[32];
-        ptx::tmem_ld32(t_o + 32 * q, o);
-        ptx::tmem_wait_ld();
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t o[32];
+          ptx::tmem_ld32(t_o + 32 * q, o);
+          ptx::tmem_wait_ld();
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          uint32_t wv[4];
+          for (int v = 0; v < 4; ++v) {
+            uint32_t wv[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            wv[e] = ptx::pack2<kBF16>(__uint_as_float(o[8 * v + 2 * e]) * inv_l,
-                                      __uint_as_float(o[8 * v + 2 * e + 1]) * inv_l);
-          if (row_ok) orow[4 * q + v] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            for (int e = 0; e < 4; ++e)
+              wv[e] = ptx::pack2<kBF16>(
+                  __uint_as_float(o[8 * v + 2 * e]) * inv_l,
+                  __uint_as_float(o[8 * v + 2 * e + 1]) * inv_l);
+            if (row_ok) orow[4 * q + v] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          }
         }
+        if (p.lse != nullptr && row_ok)
+          p.lse[row] = (m_run + ptx::lg2(l_run)) * kLn2;
+      } else {
+        // Split-KV partial: O over this key range normalised by its own l,
+        // in fp32, and the range's natural-log LSE; a row that sees no key
+        // of the range gets O = 0 and LSE = -inf.
+        const bool empty = !(l_run > 0.f);
+        const float inv_l = empty ? 0.f : ptx::rcp(l_run);
+        const long long prow =
+            (static_cast<long long>(w.split) * p.B * p.Hq + q_plane) * p.Sq +
+            m0 + r;
+        float4* orow = reinterpret_cast<float4*>(p.o_part + prow * D);
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t o[32];
+          ptx::tmem_ld32(t_o + 32 * q, o);
+          ptx::tmem_wait_ld();
+          if (row_ok) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              orow[8 * q + v] = make_float4(__uint_as_float(o[4 * v]) * inv_l,
+                                            __uint_as_float(o[4 * v + 1]) * inv_l,
+                                            __uint_as_float(o[4 * v + 2]) * inv_l,
+                                            __uint_as_float(o[4 * v + 3]) * inv_l);
+          }
+        }
+        if (row_ok)
+          p.lse_part[prow] = empty ? -INFINITY : (m_run + ptx::lg2(l_run)) * kLn2;
       }
-      if (p.lse != nullptr && row_ok)
-        p.lse[row] = (m_run + ptx::lg2(l_run)) * kLn2;
       ptx::tc_fence_before();
     }
   }

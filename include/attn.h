@@ -23,6 +23,8 @@
 #ifndef ATTN_FWD_GB300_ATTN_H
 #define ATTN_FWD_GB300_ATTN_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -77,6 +79,47 @@ attn_status_t attn_fwd(const void* Q, const void* K, const void* V, void* O,
                        float* LSE, int B, int Hq, int Hkv, int Sq, int Skv,
                        int D, float scale, int causal, int input_pos,
                        attn_dtype_t dtype, attn_stream_t stream);
+
+/*
+ * attn_fwd_splitkv — the same operation as attn_fwd, with the key range cut
+ * into num_splits pieces of equal length (multiples of 128 keys) that are
+ * processed in parallel, then merged by their log-sum-exps: for a row with
+ * partial results (O_c, lse_c), O = sum_c w_c O_c / sum_c w_c and
+ * LSE = M + ln(sum_c w_c) with w_c = exp(lse_c - M), M = max_c lse_c.
+ * This is the KV-cache decoding shape (few query rows, long key range)
+ * where attn_fwd alone would leave most SMs idle; it is the online-softmax
+ * rescaling of "Flash Attention in CUDA Tile (cuTile)", section "The online
+ * softmax algorithm", applied across key ranges.
+ *
+ * Arguments as attn_fwd, plus:
+ * num_splits       1..128, a value returned by attn_splitkv_plan for the
+ *                  same shape (other counts give ATTN_ERR_INVALID_ARG);
+ * workspace        device memory owned by the caller, 256-byte aligned,
+ *                  of at least the size attn_splitkv_plan reports: fp32
+ *                  partial outputs [num_splits, B, Hq, Sq, D] followed by
+ *                  fp32 partial LSEs [num_splits, B, Hq, Sq];
+ * workspace_bytes  its size.
+ * Two kernels are enqueued on `stream` (partials, then the merge).  The
+ * workspace must not be used by another call until both have run.
+ */
+attn_status_t attn_fwd_splitkv(const void* Q, const void* K, const void* V,
+                               void* O, float* LSE, int B, int Hq, int Hkv,
+                               int Sq, int Skv, int D, float scale, int causal,
+                               int input_pos, attn_dtype_t dtype,
+                               int num_splits, void* workspace,
+                               size_t workspace_bytes, attn_stream_t stream);
+
+/*
+ * attn_splitkv_plan — split count and workspace size for attn_fwd_splitkv.
+ * *num_splits in: the requested count, or <= 0 to choose one that gives
+ * every SM of the current device work (this form needs a CUDA device); out:
+ * the count attn_fwd_splitkv accepts (requests are clamped to the number of
+ * 128-key tiles, and trailing empty ranges are dropped).
+ * *workspace_bytes (may be NULL) receives the workspace size.
+ */
+attn_status_t attn_splitkv_plan(int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                                int causal, int input_pos, attn_dtype_t dtype,
+                                int* num_splits, size_t* workspace_bytes);
 
 /* Short English description of a status code (static storage). */
 const char* attn_status_string(attn_status_t status);

@@ -111,6 +111,34 @@ def test_tile_config(lib):
         attn.attn_tile_config(1, 3, 2, 8, 8, 64, 0, 0, attn.ATTN_F16)
 
 
+def test_splitkv_plan_host_only(lib):
+    """An explicit split request is planned without a GPU."""
+    ns, ws = attn.attn_splitkv_plan(2, 8, 2, 1, 1000, 128, 1, 999,
+                                    attn.ATTN_BF16, 5)
+    assert ns == 4           # 8 tiles in 5 requested ranges: 2 tiles each
+    rows = 2 * 8 * 1
+    assert ws == (-(-(ns * rows * 128 * 4) // 256) * 256 +
+                  -(-(ns * rows * 4) // 256) * 256)
+    ns1, _ = attn.attn_splitkv_plan(1, 2, 2, 4, 100, 64, 0, 0,
+                                    attn.ATTN_F16, 8)
+    assert ns1 == 1          # 100 keys: a single tile
+    with pytest.raises(attn.AttnError):
+        attn.attn_splitkv_plan(1, 3, 2, 4, 100, 64, 0, 0, attn.ATTN_F16, 2)
+
+
+def test_splitkv_argument_checks(lib):
+    a = dict(Q=BAD, K=BAD + 0x100000, V=BAD + 0x200000, O=BAD + 0x300000,
+             LSE=0, B=1, Hq=2, Hkv=2, Sq=1, Skv=1000, D=128, scale=0.1,
+             causal=1, input_pos=999, dtype=attn.ATTN_BF16, num_splits=2,
+             workspace=BAD + 0x400000, workspace_bytes=1 << 20, stream=0)
+    assert attn.attn_fwd_splitkv(**dict(a, num_splits=0)) == \
+        attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_fwd_splitkv(**dict(a, num_splits=500)) == \
+        attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_fwd_splitkv(**dict(a, D=80)) == attn.ATTN_ERR_UNSUPPORTED
+    assert attn.attn_fwd_splitkv(**dict(a, Sq=0)) == attn.ATTN_OK
+
+
 def test_no_device_is_an_error_not_a_crash(lib):
     """Without a GPU a well-formed call fails cleanly with ATTN_ERR_CUDA or
     ATTN_ERR_INVALID_ARG (pointers are not device memory)."""
