@@ -16,7 +16,8 @@ import threading
 
 __all__ = [
     "ATTN_F16", "ATTN_BF16", "AttnError", "attn_fwd", "attn_fwd_splitkv",
-    "attn_splitkv_plan", "attn_status_string", "attn_device_status",
+    "attn_splitkv_plan", "attn_fwd_splitkv_noalloc",
+    "attn_noalloc_scratch_bytes", "attn_status_string", "attn_device_status",
     "attn_tile_config", "attn_version", "fwd", "fwd_splitkv",
     "library_path", "load_library",
 ]
@@ -82,6 +83,12 @@ def load_library():
         lib.attn_splitkv_plan.argtypes = [i, i, i, i, i, i, i, i, i, ip,
                                           ctypes.POINTER(sz)]
         lib.attn_splitkv_plan.restype = i
+        lib.attn_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i,
+                                                 i, i, i, ctypes.c_float, i,
+                                                 i, i, i, vp]
+        lib.attn_fwd_splitkv_noalloc.restype = i
+        lib.attn_noalloc_scratch_bytes.argtypes = []
+        lib.attn_noalloc_scratch_bytes.restype = sz
         _lib = lib
         return lib
 
@@ -104,6 +111,22 @@ def attn_fwd_splitkv(Q, K, V, O, LSE, B, Hq, Hkv, Sq, Skv, D, scale, causal,
         Sq, Skv, D, float(scale), int(causal), int(input_pos), int(dtype),
         int(num_splits), workspace or None, int(workspace_bytes),
         stream or None))
+
+
+def attn_fwd_splitkv_noalloc(Q, K, V, O, LSE, B, Hq, Hkv, Sq, Skv, D, scale,
+                             causal, input_pos, dtype, num_splits,
+                             stream) -> int:
+    """Raw C-ABI call of the split-KV forward that uses the library's fixed
+    scratch array instead of a workspace (for callers that cannot allocate
+    device memory); pointers are integers."""
+    return int(load_library().attn_fwd_splitkv_noalloc(
+        Q or None, K or None, V or None, O or None, LSE or None, B, Hq, Hkv,
+        Sq, Skv, D, float(scale), int(causal), int(input_pos), int(dtype),
+        int(num_splits), stream or None))
+
+
+def attn_noalloc_scratch_bytes() -> int:
+    return int(load_library().attn_noalloc_scratch_bytes())
 
 
 def attn_splitkv_plan(B, Hq, Hkv, Sq, Skv, D, causal, input_pos, dtype,

@@ -121,6 +121,35 @@ attn_status_t attn_splitkv_plan(int B, int Hq, int Hkv, int Sq, int Skv, int D,
                                 int causal, int input_pos, attn_dtype_t dtype,
                                 int* num_splits, size_t* workspace_bytes);
 
+/*
+ * attn_fwd_splitkv_noalloc — attn_fwd_splitkv for callers that cannot
+ * allocate device memory (code running where the allocator must not be
+ * entered, or inside a host that owns every allocation): the partial
+ * results go to a fixed scratch array compiled into this library (its size
+ * is attn_noalloc_scratch_bytes(), 16 MiB, held on every GPU that loads the
+ * library until the process exits) instead of a caller workspace.  The
+ * pages have no counterpart; this is a deployment convenience.
+ *
+ * Arguments as attn_fwd_splitkv without the workspace; num_splits <= 0
+ * lets the library choose.  Returns ATTN_ERR_UNSUPPORTED when the partial
+ * results of the planned split count (see attn_splitkv_plan) need more
+ * than the scratch holds.  The first call on a device looks up the
+ * scratch address on that device (no allocation); make that first call
+ * before any stream capture.  All calls share the one scratch array and it
+ * keeps the last call's contents (nothing in it has to start at zero):
+ * calls whose kernels overlap on the GPU race on it, so issue them on one
+ * stream or otherwise order them.
+ */
+attn_status_t attn_fwd_splitkv_noalloc(const void* Q, const void* K,
+                                       const void* V, void* O, float* LSE,
+                                       int B, int Hq, int Hkv, int Sq, int Skv,
+                                       int D, float scale, int causal,
+                                       int input_pos, attn_dtype_t dtype,
+                                       int num_splits, attn_stream_t stream);
+
+/* Bytes of the fixed scratch array attn_fwd_splitkv_noalloc uses. */
+size_t attn_noalloc_scratch_bytes(void);
+
 /* Short English description of a status code (static storage). */
 const char* attn_status_string(attn_status_t status);
 
