@@ -71,6 +71,12 @@ PREFILL_CHUNK = Workload("prefill_B8_Hq32_Hkv8_Sq512_pos3584_Skv4096_D128_bf16",
                          8, 32, 8, 512, 4096, 128, "bf16", True, 3584)
 
 
+# One new token per sequence against a full 4096-key cache (the decode step
+# after the prefill chunk above); the split-KV path's workload.
+DECODE = Workload("decode_B8_Hq32_Hkv8_Sq1_pos4095_Skv4096_D128_bf16",
+                  8, 32, 8, 1, 4096, 128, "bf16", True, 4095)
+
+
 def sweep():
     """B=4, H=16 non-causal sweep over S, D and dtype."""
     out = []

@@ -388,6 +388,84 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+# ------------------------------------------------------- split-KV decode
+def run_decode(args):
+    """Split-KV decode step: HBM-bound, reported in GB/s of algorithmic
+    traffic (Q, K, V read once; O and LSE written once) against the measured
+    copy bandwidth.  Two kernels per step (partials, merge)."""
+    import torch
+
+    import attention_attn_fwd_gb300 as attn
+    from attention_attn_fwd_gb300.inputs import DECODE, make_qkv
+
+    ws, rank, local = dist_info()
+    if ws > 1:
+        torch.cuda.set_device(local)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = DECODE
+    q, k, v = (t.to(dev) for t in make_qkv(w, seed=0))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    dt = attn.ATTN_BF16
+    splits, ws_bytes = attn.attn_splitkv_plan(w.B, w.Hq, w.Hkv, w.Sq, w.Skv,
+                                              w.D, 1, w.input_pos, dt,
+                                              args.splits)
+    work = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+
+    def step():
+        st = attn.attn_fwd_splitkv(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+            lse.data_ptr(), w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.scale, 1,
+            w.input_pos, dt, splits, work.data_ptr(), ws_bytes,
+            stream.cuda_stream)
+        if st != attn.ATTN_OK:
+            raise RuntimeError("attn_fwd_splitkv: " +
+                               attn.attn_status_string(st))
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(dev.index) as clocks:
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    st, code = attn.attn_device_status()
+    if st != attn.ATTN_OK:
+        raise RuntimeError("device status %d code %#x" % (st, code))
+    ms = sum(s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)) / args.steps
+    gbs = w.io_bytes() / (ms * 1e-3) / 1e9
+    _, hbm, src = peaks()
+    out = {
+        "metric": "attention decode (split-KV) GB/s of algorithmic traffic",
+        "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic: Q/K/V ~ N(0,1) from a seeded CPU generator",
+        "config": config_dict(w, {
+            "num_splits": splits, "workspace_bytes": ws_bytes,
+            "l2": "flushed between timed steps (256 MiB write, untimed)",
+            "algorithmic_bytes_per_step": w.io_bytes(),
+            "tflops_formula": round(w.flops() / (ms * 1e-3) / 1e12, 2)}),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
+                     "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                     "peak_source": "%s copy bandwidth" % src,
+                     "traffic": None},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -397,11 +475,19 @@ def main():
     ap.add_argument("--cpu-s", type=float, default=15.0,
                     help="CPU-oracle baseline budget in seconds")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["gqa8k", "decode"],
+                    default="gqa8k",
+                    help="gqa8k: the headline causal GQA forward (default); "
+                         "decode: the split-KV decode step")
+    ap.add_argument("--splits", type=int, default=0,
+                    help="split count for --workload decode (0: automatic)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "decode":
+        run_decode(args)
     else:
         run_ours(args)
 
