@@ -86,9 +86,15 @@ struct Shape {
   int B, Hq, Hkv, Sq, Skv, D, causal, input_pos;
 };
 
-// A CTA owns two 128-row Q tiles: two query heads of one K/V group at the
+// Tile dispatch.  Few query rows with grouped K/V heads (group * Sq <= 128):
+// one Q tile packs the rows of all query heads of a K/V head.  Otherwise a
+// CTA owns two 128-row Q tiles: two query heads of one K/V group at the
 // same rows when the group size is even, else 256 consecutive rows of one
 // head.
+bool pack_gqa(const Shape& s) {
+  const int g = s.Hq / s.Hkv;
+  return g >= 2 && static_cast<long long>(g) * s.Sq <= attn::cfg::kTM;
+}
 bool pair_heads(const Shape& s) { return (s.Hq / s.Hkv) % 2 == 0; }
 
 long long m_blocks(const Shape& s) {
@@ -97,6 +103,7 @@ long long m_blocks(const Shape& s) {
 }
 
 long long grid_size(const Shape& s) {
+  if (pack_gqa(s)) return static_cast<long long>(s.B) * s.Hkv;
   const long long units = pair_heads(s) ? static_cast<long long>(s.B) * (s.Hq / 2)
                                         : static_cast<long long>(s.B) * s.Hq;
   return m_blocks(s) * units;
@@ -120,15 +127,16 @@ attn_status_t check_scalars(const Shape& s, float scale, attn_dtype_t dtype) {
   return ATTN_OK;
 }
 
-// Dispatch table keyed on (D, causal, S, dtype).  One tile shape serves every
-// entry for now: 2 x 128 query rows per CTA, 128-key K/V tiles; the ring
-// depth depends on D (shared-memory budget).
+// Dispatch table keyed on (D, causal, S, dtype, group): 2 x 128 query rows
+// per CTA with 128-key K/V tiles, or group*Sq packed rows for short query
+// blocks; the ring depth depends on D (shared-memory budget).
 struct TileChoice {
   int block_m, block_n, stages, smem_bytes;
 };
 
 TileChoice choose_tiles(const Shape& s) {
-  return TileChoice{attn::cfg::kBlockM, attn::cfg::kTN, attn::fwd_stages(s.D),
+  const int block_m = pack_gqa(s) ? (s.Hq / s.Hkv) * s.Sq : attn::cfg::kBlockM;
+  return TileChoice{block_m, attn::cfg::kTN, attn::fwd_stages(s.D),
                     attn::fwd_smem_bytes(s.D)};
 }
 
@@ -143,8 +151,11 @@ bool is_device_ptr(const void* p, int dev) {
   return a.device == dev;
 }
 
+// 3-D map (D, S, planes) of a [planes, S, D] tensor; boxes of 64 x box_rows
+// x box_planes elements with 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, attn_dtype_t dtype, int D,
-              int S, long long planes) {
+              int S, long long planes, int box_rows = 128,
+              int box_planes = 1) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
   if (enc == nullptr) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D),
@@ -152,7 +163,8 @@ bool make_map(CUtensorMap* m, const void* base, attn_dtype_t dtype, int D,
                               static_cast<cuuint64_t>(planes)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
                                  static_cast<cuuint64_t>(S) * D * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows),
+                             static_cast<cuuint32_t>(box_planes)};
   const cuuint32_t estride[3] = {1, 1, 1};
   const CUresult r = enc(
       m, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -201,8 +213,20 @@ void splitkv_shape(const Shape& s, int splits, int sms, int* out_splits,
                    int* out_tiles) {
   const int tiles = (s.Skv + attn::cfg::kTN - 1) / attn::cfg::kTN;
   if (splits <= 0) {
+    // Pick the count with the shortest estimated critical path: waves of
+    // units over the SMs times key tiles per range, plus one tile's worth
+    // for the merge launch.  Ties go to fewer ranges (less partial traffic).
     const long long units = grid_size(s);
-    splits = units >= sms ? 1 : static_cast<int>((sms + units - 1) / units);
+    long long best = -1;
+    const int cap = std::max(1, std::min(tiles, kMaxSplits));
+    for (int c = 1; c <= cap; ++c) {
+      const long long waves = (units * c + sms - 1) / sms;
+      const long long cost = waves * ((tiles + c - 1) / c) + (c > 1 ? 1 : 0);
+      if (best < 0 || cost < best) {
+        best = cost;
+        splits = c;
+      }
+    }
   }
   splits = std::max(1, std::min({splits, tiles, kMaxSplits}));
   const int per = (tiles + splits - 1) / splits;
@@ -251,8 +275,12 @@ attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
   CUtensorMap tq, tk, tv;
   const long long q_planes = static_cast<long long>(s.B) * s.Hq;
   const long long kv_planes = static_cast<long long>(s.B) * s.Hkv;
-  if (!make_map(&tq, Q, dtype, s.D, s.Sq, q_planes) ||
-      !make_map(&tk, K, dtype, s.D, s.Skv, kv_planes) ||
+  const bool pack = pack_gqa(s);
+  const int group = s.Hq / s.Hkv;
+  const bool q_ok = pack ? make_map(&tq, Q, dtype, s.D, s.Sq, q_planes, s.Sq,
+                                    group)
+                         : make_map(&tq, Q, dtype, s.D, s.Sq, q_planes);
+  if (!q_ok || !make_map(&tk, K, dtype, s.D, s.Skv, kv_planes) ||
       !make_map(&tv, V, dtype, s.D, s.Skv, kv_planes))
     return ATTN_ERR_CUDA;
 
@@ -266,6 +294,10 @@ attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
   p.input_pos = s.causal != 0 ? s.input_pos : 0;
   p.num_m_blocks = static_cast<int>(m_blocks(s));
   p.pair_heads = pair_heads(s);
+  p.pack_gqa = pack;
+  p.group = group;
+  // 128-byte rows: 128 per tile, or group*Sq packed, per 64-column box.
+  p.q_tile_bytes = (s.D / 64) * 128 * (pack ? group * s.Sq : attn::cfg::kTM);
   p.scale_log2 = std::fabs(scale) * 1.4426950408889634f;
   p.negate_scores = scale < 0.f;
   p.o = O;

@@ -42,6 +42,12 @@ struct FwdParams {
   int input_pos;
   int num_m_blocks;        // m-blocks per head (of 128 or 256 rows)
   int pair_heads;          // a unit = 2 heads x 128 rows (else 1 head x 256)
+  // GQA packing (few query rows): one Q tile holds the Sq rows of all
+  // `group` query heads of a K/V head, row r = head (r / Sq), position
+  // (r % Sq); the second tile is unused.
+  int pack_gqa;
+  int group;               // Hq / Hkv
+  int q_tile_bytes;        // bytes one Q tile load brings in
   float scale_log2;        // |scale| * log2(e)
   int negate_scores;       // scale < 0: S is computed as -(Q K^T)
   void* o;                 // [B, Hq, Sq, D] output (16-bit elements)
@@ -162,6 +168,20 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   u /= p.num_splits;
   w.kt0 = w.split * p.split_tiles;
   const int kt1 = w.kt0 + p.split_tiles;
+  if (p.pack_gqa) {
+    // Unit = one (batch, K/V head): tile 0 holds all its query rows.
+    const int b = u / p.Hkv;
+    const int kvh = u % p.Hkv;
+    w.kv_plane = b * p.Hkv + kvh;
+    w.plane[0] = b * p.Hq + kvh * p.group;  // first head of the group
+    w.plane[1] = w.plane[0];
+    w.m0[0] = w.m0[1] = 0;
+    tile_extent(p, 0, w.kt0, kt1, w.n[0], w.ms[0]);
+    w.n[1] = 0;
+    w.ms[1] = 0;
+    w.n_kv = w.n[0];
+    return w;
+  }
   const int per_m = p.pair_heads ? p.B * (p.Hq / 2) : p.B * p.Hq;
   const int mb = p.num_m_blocks - 1 - u / per_m;
   const int ub = u % per_m;
@@ -221,6 +241,13 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
   const int u_first = static_cast<int>(blockIdx.x);
   const int u_step = static_cast<int>(gridDim.x);
 
+  if (p.pack_gqa) {
+    // A packed Q load fills only group*Sq rows of the tile: keep the other
+    // rows zero so their (discarded) scores stay finite.
+    for (int i = threadIdx.x; i < 2 * L::kTileBytes / 16; i += kThreads)
+      ptx::st_shared_v4(s_q + 16 * i, 0u, 0u, 0u, 0u);
+    ptx::fence_proxy_async_smem();
+  }
   if (threadIdx.x == 0) {
     // P-ready barriers collect one arrival per softmax thread; the others
     // one arrival (an expect-tx, a tcgen05.commit).
@@ -266,7 +293,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
                                        abort_flag, p, 1));
         if (!ok) break;
         const uint32_t dst = s_q + t * L::kTileBytes;
-        ptx::mbar_arrive_expect_tx_elect(bar_q + 8 * t, L::kTileBytes);
+        ptx::mbar_arrive_expect_tx_elect(bar_q + 8 * t, p.q_tile_bytes);
         for (int c = 0; c < L::kChunks; ++c)
           ptx::tma_load_3d_elect(dst + c * L::kBoxBytes, &tm_q, bar_q + 8 * t,
                                  c * 64, w.m0[t], w.plane[t]);
@@ -445,8 +472,16 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
       if (n == 0) continue;
       const int ms = t ? w.ms[1] : w.ms[0];
       const int m0 = t ? w.m0[1] : w.m0[0];
-      const int q_plane = t ? w.plane[1] : w.plane[0];
-      const int row_pos = p.input_pos + m0 + r;  // absolute query position
+      // This thread's query row: head plane and row index within the head.
+      int q_plane = t ? w.plane[1] : w.plane[0];
+      int q_row = m0 + r;
+      bool row_ok = q_row < p.Sq;
+      if (p.pack_gqa) {
+        q_plane += r / p.Sq;
+        q_row = r % p.Sq;
+        row_ok = r < p.group * p.Sq;
+      }
+      const int row_pos = p.input_pos + q_row;  // absolute query position
       float m_run = -INFINITY;  // running max of scaled scores (log2 units)
       float l_run = 0.f;        // running sum of 2^(s*c - m_run)
 
@@ -583,10 +618,10 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
       if (!ok) break;
       ++o_waits;
       ptx::tc_fence_after();
-      const bool row_ok = m0 + r < p.Sq;
+
       if (p.o_part == nullptr) {
         const float inv_l = ptx::rcp(l_run);
-        const long long row = static_cast<long long>(q_plane) * p.Sq + m0 + r;
+        const long long row = static_cast<long long>(q_plane) * p.Sq + q_row;
         uint4* orow =
             reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + row * D);
 #pragma unroll
@@ -615,7 +650,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
         const float inv_l = empty ? 0.f : ptx::rcp(l_run);
         const long long prow =
             (static_cast<long long>(w.split) * p.B * p.Hq + q_plane) * p.Sq +
-            m0 + r;
+            q_row;
         float4* orow = reinterpret_cast<float4*>(p.o_part + prow * D);
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) {

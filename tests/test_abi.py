@@ -107,6 +107,9 @@ def test_tile_config(lib):
     assert c["stages"] >= 2
     c64 = attn.attn_tile_config(4, 16, 16, 1000, 1000, 64, 0, 0, attn.ATTN_F16)
     assert c64["grid"] == 4 * 16 * 4
+    # Decode shape: the 4 query heads of each K/V head share one tile.
+    cd = attn.attn_tile_config(8, 32, 8, 1, 4096, 128, 1, 4095, attn.ATTN_BF16)
+    assert cd["block_m"] == 4 and cd["grid"] == 8 * 8
     with pytest.raises(attn.AttnError):
         attn.attn_tile_config(1, 3, 2, 8, 8, 64, 0, 0, attn.ATTN_F16)
 

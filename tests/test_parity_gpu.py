@@ -49,6 +49,11 @@ EDGE = [
     W("skv_tile_plus_one_causal", 1, 2, 2, 129, 257, 64, "f16", True, 128),
     W("long_keys_short_q", 1, 4, 4, 40, 2049, 128, "f16", False),
     W("sq_gt_skv_causal", 1, 2, 2, 600, 200, 64, "bf16", True),
+    # Few query rows with grouped K/V heads: all heads of a group in one tile.
+    W("packed_full_tile", 1, 32, 4, 16, 900, 128, "bf16", True, 884),
+    W("packed_ragged", 2, 8, 2, 30, 333, 64, "f16", True, 303),
+    W("packed_noncausal", 1, 8, 2, 5, 700, 128, "bf16", False),
+    W("packed_one_row", 3, 4, 2, 1, 130, 64, "f16", True, 129),
 ]
 
 
