@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdint>
 #include <algorithm>
+#include <atomic>
 #include <cstddef>
 #include <cstdlib>
 #include <mutex>
@@ -200,11 +201,22 @@ constexpr size_t kWorkspaceAlign = 256;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Bytes of the split-KV workspace: fp32 partial outputs, then partial LSEs.
+// Bytes of the split-KV workspace: fp32 partial outputs, partial LSEs,
+// then one 64-bit merge counter per (row block, Q tile).
 size_t splitkv_bytes(const Shape& s, int splits) {
   const size_t rows = static_cast<size_t>(s.B) * s.Hq * s.Sq;
   return round_up(static_cast<size_t>(splits) * rows * s.D * 4, kWorkspaceAlign) +
-         round_up(static_cast<size_t>(splits) * rows * 4, kWorkspaceAlign);
+         round_up(static_cast<size_t>(splits) * rows * 4, kWorkspaceAlign) +
+         round_up(static_cast<size_t>(grid_size(s)) * 2 * 8, kWorkspaceAlign);
+}
+
+// Tag of one split-KV call: marks its merge-counter arrivals, so counters
+// left by earlier calls in a reused workspace are recognised as stale.
+unsigned int next_merge_seq() {
+  static std::atomic<unsigned int> seq{0};
+  unsigned int v = ++seq;
+  if (v == 0) v = ++seq;  // skip 0 on wrap-around
+  return v;
 }
 
 // Split count and K/V tiles per split.  `splits` <= 0 picks enough splits
@@ -214,14 +226,18 @@ void splitkv_shape(const Shape& s, int splits, int sms, int* out_splits,
   const int tiles = (s.Skv + attn::cfg::kTN - 1) / attn::cfg::kTN;
   if (splits <= 0) {
     // Pick the count with the shortest estimated critical path: waves of
-    // units over the SMs times key tiles per range, plus one tile's worth
-    // for the merge launch.  Ties go to fewer ranges (less partial traffic).
+    // units over the SMs times (key tiles per range + a fixed per-unit cost
+    // of Q load, pipeline fill and epilogue, about kUnitTiles tiles), plus
+    // one tile's worth for the merge launch.  Ties go to fewer ranges (less
+    // partial traffic).
+    constexpr int kUnitTiles = 3;
     const long long units = grid_size(s);
     long long best = -1;
     const int cap = std::max(1, std::min(tiles, kMaxSplits));
     for (int c = 1; c <= cap; ++c) {
       const long long waves = (units * c + sms - 1) / sms;
-      const long long cost = waves * ((tiles + c - 1) / c) + (c > 1 ? 1 : 0);
+      const long long cost =
+          waves * ((tiles + c - 1) / c + kUnitTiles) + (c > 1 ? 1 : 0);
       if (best < 0 || cost < best) {
         best = cost;
         splits = c;
@@ -271,7 +287,8 @@ attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
                              const void* V, void* O, float* LSE, float scale,
                              attn_dtype_t dtype, unsigned int* status, int sms,
                              int splits, int split_tiles, float* o_part,
-                             float* lse_part, cudaStream_t stream) {
+                             float* lse_part, unsigned long long* merge_ctr,
+                             cudaStream_t stream) {
   CUtensorMap tq, tk, tv;
   const long long q_planes = static_cast<long long>(s.B) * s.Hq;
   const long long kv_planes = static_cast<long long>(s.B) * s.Hkv;
@@ -306,6 +323,8 @@ attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
   p.split_tiles = split_tiles;
   p.o_part = o_part;
   p.lse_part = lse_part;
+  p.merge_ctr = merge_ctr;
+  p.merge_seq = merge_ctr != nullptr ? next_merge_seq() : 0u;
   p.num_units = static_cast<int>(grid_size(s) * splits);
   p.status = status;
   p.timeout_ns = timeout_ns();
@@ -337,7 +356,7 @@ attn_status_t attn_fwd(const void* Q, const void* K, const void* V, void* O,
   if (st != ATTN_OK) return st;
   const int tiles = (Skv + attn::cfg::kTN - 1) / attn::cfg::kTN;
   return launch_forward(s, Q, K, V, O, LSE, scale, dtype, status, sms, 1,
-                        tiles, nullptr, nullptr,
+                        tiles, nullptr, nullptr, nullptr,
                         reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -386,19 +405,17 @@ attn_status_t attn_fwd_splitkv(const void* Q, const void* K, const void* V,
   if (workspace_bytes < splitkv_bytes(s, splits)) return ATTN_ERR_INVALID_ARG;
   if (!is_device_ptr(workspace, dev)) return ATTN_ERR_INVALID_ARG;
   const size_t rows = static_cast<size_t>(B) * Hq * Sq;
-  float* o_part = static_cast<float*>(workspace);
-  float* lse_part = reinterpret_cast<float*>(
-      static_cast<char*>(workspace) +
-      round_up(static_cast<size_t>(splits) * rows * D * 4, kWorkspaceAlign));
-  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  st = launch_forward(s, Q, K, V, O, LSE, scale, dtype, status, sms, splits,
-                      tiles, o_part, lse_part, cs);
-  if (st != ATTN_OK) return st;
-  const cudaError_t err = attn::launch_splitkv_combine(
-      D, dtype == ATTN_BF16, o_part, lse_part, O, LSE,
-      static_cast<long long>(rows), Sq, splits, tiles * attn::cfg::kTN, Skv,
-      causal != 0, causal != 0 ? input_pos : 0, cs);
-  return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  const size_t o_bytes =
+      round_up(static_cast<size_t>(splits) * rows * D * 4, kWorkspaceAlign);
+  const size_t lse_bytes =
+      round_up(static_cast<size_t>(splits) * rows * 4, kWorkspaceAlign);
+  char* ws = static_cast<char*>(workspace);
+  // One launch: the forward kernel also merges the key ranges.
+  return launch_forward(
+      s, Q, K, V, O, LSE, scale, dtype, status, sms, splits, tiles,
+      reinterpret_cast<float*>(ws), reinterpret_cast<float*>(ws + o_bytes),
+      reinterpret_cast<unsigned long long*>(ws + o_bytes + lse_bytes),
+      reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char* attn_status_string(attn_status_t status) {

@@ -21,7 +21,9 @@
 //   warps 8-11 the same for Q tile 1
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 and O1 (D columns each)
 // from 256.  P_t (16-bit) overwrites the first 64 columns of S_t and is the
-// A operand of O_t += P_t V straight from TMEM.
+// A operand of O_t += P_t V straight from TMEM.  With the query heads of a
+// GQA group packed into tile 0 (few query rows), tile 1 is unused and its S
+// region double-buffers the scores of tile 0 instead.
 //
 // Every mbarrier wait is bounded: on timeout the waiter raises a CTA-wide
 // abort flag and a device status word, every role stops issuing work, waits
@@ -61,6 +63,11 @@ struct FwdParams {
   int split_tiles;
   float* o_part;           // [num_splits, B*Hq, Sq, D]
   float* lse_part;         // [num_splits, B*Hq, Sq]
+  // Split-KV merge: one arrival counter per (row block, Q tile), tagged with
+  // this call's sequence number in the high 32 bits; the unit whose arrival
+  // completes the set merges the key ranges of that tile's rows into O/LSE.
+  unsigned long long* merge_ctr;  // [num_units / num_splits, 2]
+  unsigned int merge_seq;         // nonzero, distinct per call
   unsigned int* status;    // device status word (timeouts)
   unsigned long long timeout_ns;
 };
@@ -93,6 +100,7 @@ struct Layout {
   // barriers: q_full[2], full[S], empty[S], s_full[2], p_full[2], o_full[2],
   // drain[1], q_free[2]
   static constexpr int kNumBars = 2 + 2 * kSlots + 2 + 2 + 2 + 1 + 2;
+  // misc: TMEM base, abort flag, per-tile "merge here" flags
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kSmemBytes = kBytes + 1024;  // slack for 1 KB alignment
@@ -196,6 +204,96 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   }
   w.n_kv = max(w.n[0], w.n[1]);
   return w;
+}
+
+// Number of key ranges (split-KV) that reach the 128-row Q tile at m0:
+// ranges starting past the tile's causal horizon are never visited.
+__device__ __forceinline__ int ranges_visited(const FwdParams& p, int m0) {
+  int n, ms;
+  tile_extent(p, m0, 0, 1 << 30, n, ms);
+  return min(p.num_splits, (n + p.split_tiles - 1) / p.split_tiles);
+}
+
+// Counts this unit's arrival on a tile's merge counter; true for the
+// arrival that completes the expected set of this call.  A counter left by
+// an earlier call (another sequence number) restarts at one, so the
+// workspace needs no clearing.  Lock-free: a CAS fails only when another
+// arrival succeeded, so the loop ends within `expect` rounds; the cap only
+// guards against a corrupted counter.
+__device__ __forceinline__ bool merge_arrive(unsigned long long* ctr,
+                                             unsigned int seq, int expect,
+                                             const FwdParams& p) {
+  unsigned long long cur = atomicAdd(ctr, 0ull);
+  for (int i = 0; i < (1 << 16); ++i) {
+    const unsigned int cnt =
+        static_cast<unsigned int>(cur >> 32) == seq
+            ? static_cast<unsigned int>(cur) + 1u
+            : 1u;
+    const unsigned long long nv =
+        (static_cast<unsigned long long>(seq) << 32) | cnt;
+    const unsigned long long prev = atomicCAS(ctr, cur, nv);
+    if (prev == cur) return cnt == static_cast<unsigned int>(expect);
+    cur = prev;
+  }
+  atomicOr(p.status, 1u | (5u << 8));
+  return false;
+}
+
+// Split-KV merge of the rows of one Q tile by its 128 softmax threads
+// (index tid).  Key range c of a row contributes its normalised partial
+// output O_c and log-sum-exp lse_c; with M = max_c lse_c and
+// w_c = e^(lse_c - M),  O = sum_c w_c O_c / sum_c w_c  and
+// LSE = M + ln(sum_c w_c) -- the online-softmax rescale applied once more,
+// across ranges.  Ranges past a row's causal horizon hold nothing for it
+// and are not read.  Thread tid takes 4 columns of one row, so the 32 (or
+// 16) threads of a row read its partials as contiguous 512 (256) bytes.
+template <int D, bool kBF16>
+__device__ __forceinline__ void merge_tile(const FwdParams& p, int plane0,
+                                           int m0, int tid) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  constexpr int kGroups = D / 4;               // 4-column groups per row
+  constexpr int kRowsPerPass = cfg::kTM / kGroups;
+  const long long rows = static_cast<long long>(p.B) * p.Hq * p.Sq;
+  const int split_keys = p.split_tiles * cfg::kTN;
+  const int nrows =
+      p.pack_gqa ? p.group * p.Sq : min(cfg::kTM, p.Sq - m0);
+  const int cg = tid % kGroups;
+  for (int r = tid / kGroups; r < nrows; r += kRowsPerPass) {
+    int q_plane = plane0, q_row = m0 + r;
+    if (p.pack_gqa) {
+      q_plane += r / p.Sq;
+      q_row = r % p.Sq;
+    }
+    const long long row = static_cast<long long>(q_plane) * p.Sq + q_row;
+    const int vis_end =
+        p.causal ? min(p.Skv, p.input_pos + q_row + 1) : p.Skv;
+    const int ns = min(p.num_splits, (vis_end + split_keys - 1) / split_keys);
+    float mx = -INFINITY;
+    for (int c = 0; c < ns; ++c)
+      mx = fmaxf(mx, __ldcg(p.lse_part + c * rows + row));
+    float wsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int c = 0; c < ns; ++c) {
+      const float wc =
+          ptx::ex2((__ldcg(p.lse_part + c * rows + row) - mx) * kLog2e);
+      const float4 x = __ldcg(
+          reinterpret_cast<const float4*>(p.o_part + (c * rows + row) * D) +
+          cg);
+      wsum += wc;
+      acc.x += wc * x.x;
+      acc.y += wc * x.y;
+      acc.z += wc * x.z;
+      acc.w += wc * x.w;
+    }
+    const float inv = ptx::rcp(wsum);
+    uint2 out;
+    out.x = ptx::pack2<kBF16>(acc.x * inv, acc.y * inv);
+    out.y = ptx::pack2<kBF16>(acc.z * inv, acc.w * inv);
+    reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.o) + row * D)[cg] = out;
+    if (cg == 0 && p.lse != nullptr)
+      p.lse[row] = mx + ptx::lg2(wsum) * cfg::kLn2;
+  }
 }
 
 // k-th unit of CTA `cta` among `ctas`: rounds of `ctas` units, the CTA order
@@ -346,11 +444,12 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
     const uint32_t v_lo = ptx::sdesc_lo(s_ring, L::kBoxBytes);
     constexpr uint32_t kTile16 = L::kTileBytes >> 4;
 
-    // S_t = Q_t K_j^T : A = Q tile (K-major), B = K tile (K-major).
-    auto issue_qk = [&](int t, int slot) {
+    // S = Q_t K_j^T into S region `sb`: A = Q tile (K-major), B = K tile
+    // (K-major).
+    auto issue_qk = [&](int t, int sb, int slot) {
       const uint32_t a0 = q_lo + t * kTile16;
       const uint32_t b0 = k_lo + slot * kTile16;
-      const uint32_t d = tmem + t * kTN;
+      const uint32_t d = tmem + sb * kTN;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk / 4) * L::kBoxBytes + (kk % 4) * 32) >> 4;
@@ -358,11 +457,12 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
                           kk > 0 ? 1u : 0u);
       }
     };
-    // O_t (+)= P_t V_j : A = P_t in TMEM, B = V tile (MN-major).
-    auto issue_pv = [&](int t, int slot, bool acc) {
+    // O_t (+)= P V_j : A = P in S region `sb` of TMEM, B = V tile
+    // (MN-major).
+    auto issue_pv = [&](int t, int sb, int slot, bool acc) {
       const uint32_t b0 = v_lo + slot * kTile16;
       const uint32_t d = tmem + 2 * kTN + t * D;
-      const uint32_t a = tmem + t * kTN;
+      const uint32_t a = tmem + sb * kTN;
 #pragma unroll
       for (int kk = 0; kk < kTN / 16; ++kk) {
         ptx::mma_ts_elect(d, a + kk * 8, b0 + ((kk * 16 * 128) >> 4), kHi,
@@ -380,6 +480,66 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
       // A key range wholly past the causal horizon of both tiles has no
       // work (split-KV only); the producer and softmax warps skip it too.
       if (w.n_kv == 0) continue;
+      if (p.pack_gqa) {
+        // One Q tile whose scores alternate between the two S regions:
+        // S(j+1) is computed while the softmax warps work on S(j), and
+        // S(j+2) reuses region j%2 once PV(j) (issued just before it, and
+        // executed in order) has read P(j).  Every PV but the unit's last
+        // commits to o_full[1] so the softmax warps know when O may be
+        // rescaled; the last commits to o_full[0] for the epilogue.
+        const int n = w.n_kv;
+        const int it0 = it;
+        ok = __all_sync(0xffffffffu, wait_bounded(bar_q, q_uses[0] & 1,
+                                                  abort_flag, p, 2));
+        if (!ok) break;
+        ++q_uses[0];
+        for (int sb = 0; sb < 2 && sb < n && ok; ++sb) {
+          const int it_k = it0 + 2 * sb;
+          ok = __all_sync(0xffffffffu,
+                          wait_bounded(bar_full + 8 * (it_k % L::kSlots),
+                                       (it_k / L::kSlots) & 1, abort_flag, p,
+                                       2));
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_qk(0, sb, it_k % L::kSlots);
+          ptx::tc_commit_elect(bar_s + 8 * sb);
+          ptx::tc_commit_elect(bar_empty + 8 * (it_k % L::kSlots));
+          if (sb == n - 1) ptx::tc_commit_elect(bar_qfree);
+          issued_any = true;
+        }
+        for (int j = 0; j < n && ok; ++j) {
+          const int sb = j & 1;
+          const int it_v = it0 + 2 * j + 1;
+          ok = __all_sync(0xffffffffu,
+                          wait_bounded(bar_full + 8 * (it_v % L::kSlots),
+                                       (it_v / L::kSlots) & 1, abort_flag, p,
+                                       2));
+          if (!ok) break;
+          const int pw = sb ? p_waits[1] : p_waits[0];
+          ok = __all_sync(0xffffffffu, wait_bounded(bar_p + 8 * sb, pw & 1,
+                                                    abort_flag, p, 2));
+          if (!ok) break;
+          if (sb) ++p_waits[1]; else ++p_waits[0];
+          ptx::tc_fence_after();
+          issue_pv(0, sb, it_v % L::kSlots, j > 0);
+          ptx::tc_commit_elect(j == n - 1 ? bar_o : bar_o + 8);
+          ptx::tc_commit_elect(bar_empty + 8 * (it_v % L::kSlots));
+          if (j + 2 < n) {
+            const int it_k = it0 + 2 * (j + 2);
+            ok = __all_sync(0xffffffffu,
+                            wait_bounded(bar_full + 8 * (it_k % L::kSlots),
+                                         (it_k / L::kSlots) & 1, abort_flag,
+                                         p, 2));
+            if (!ok) break;
+            issue_qk(0, sb, it_k % L::kSlots);
+            ptx::tc_commit_elect(bar_s + 8 * sb);
+            ptx::tc_commit_elect(bar_empty + 8 * (it_k % L::kSlots));
+            if (j + 2 == n - 1) ptx::tc_commit_elect(bar_qfree);
+          }
+        }
+        it = it0 + 2 * n;
+        continue;
+      }
       // S_t = Q_t K_0^T for both tiles.
       ok = __all_sync(0xffffffffu,
                       wait_bounded(bar_full + 8 * (it % L::kSlots),
@@ -394,7 +554,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
         if (!ok) break;
         ++q_uses[t];
         ptx::tc_fence_after();
-        issue_qk(t, it % L::kSlots);
+        issue_qk(t, t, it % L::kSlots);
         ptx::tc_commit_elect(bar_s + 8 * t);
         if (w.n[t] == 1) ptx::tc_commit_elect(bar_qfree + 8 * t);
         issued_any = true;
@@ -422,7 +582,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
           if (!ok) break;
           ++p_waits[t];
           ptx::tc_fence_after();
-          issue_pv(t, slot_v, j > 0);
+          issue_pv(t, t, slot_v, j > 0);
           if (j == w.n[t] - 1) {
             ptx::tc_commit_elect(bar_o + 8 * t);
           } else {
@@ -434,7 +594,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
               if (!ok) break;
               k_ready = true;
             }
-            issue_qk(t, slot_k);
+            issue_qk(t, t, slot_k);
             ptx::tc_commit_elect(bar_s + 8 * t);
             // After the tile's last S MMA, its Q buffer can be refilled.
             if (j + 1 == w.n[t] - 1) ptx::tc_commit_elect(bar_qfree + 8 * t);
@@ -457,12 +617,19 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
     const int t = warp / 4 - 1;             // Q tile of this warpgroup
     const int r = threadIdx.x % 128;        // row within the tile
     const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
-    const uint32_t t_s = tmem + lane_off + t * kTN;
     const uint32_t t_o = tmem + lane_off + 2 * kTN + t * D;
     const float c = p.scale_log2;
+    // Packed query heads fill only group*Sq rows of the tile: a warp whose
+    // 32 rows are all padding keeps in step (waits, arrivals) but computes
+    // nothing.  Its P rows stay whatever S left there, which only reaches
+    // the matching O rows (row i of P V is row i of P times V), and those
+    // are never stored.
+    const bool live = !p.pack_gqa || (warp % 4) * 32 < p.group * p.Sq;
     bool ok = true;
-    int s_waits = 0;  // S-ready phases consumed
-    int o_waits = 0;  // O-done phases consumed
+    int s_waits = 0;   // S-ready phases consumed (packed: S region 0)
+    int s_waits1 = 0;  // packed: S-ready phases of S region 1
+    int o_waits = 0;   // O-done phases consumed
+    int pv_waits = 0;  // packed: per-step PV-done phases consumed
 
     for (int k = 0; k * u_step < p.num_units && ok; ++k) {
       const int u = unit_index(k, u_first, u_step);
@@ -486,11 +653,22 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
       float l_run = 0.f;        // running sum of 2^(s*c - m_run)
 
       for (int j = 0; j < n; ++j) {
-        ok = __all_sync(0xffffffffu, wait_bounded(bar_s + 8 * t, s_waits & 1,
-                                                  abort_flag, p, 3));
+        // S region of this step: the tile's own, or (packed) alternating.
+        const int sb = p.pack_gqa ? (j & 1) : t;
+        const uint32_t t_s = tmem + lane_off + sb * kTN;
+        const bool odd = p.pack_gqa && sb == 1;
+        ok = __all_sync(0xffffffffu,
+                        wait_bounded(bar_s + 8 * sb,
+                                     (odd ? s_waits1 : s_waits) & 1,
+                                     abort_flag, p, 3));
         if (!ok) break;
-        ++s_waits;
+        if (odd) ++s_waits1; else ++s_waits;
         ptx::tc_fence_after();
+        if (!live) {
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar_p + 8 * sb);
+          continue;
+        }
 
         // Pass 1: row maximum of the scaled scores over the visible keys.
         // Visible keys of this row in the tile are the columns < lim: key <
@@ -585,9 +763,21 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
           }
         }
 
+        if (p.pack_gqa && j > 0) {
+          // Packed: S_j was issued before PV_{j-1}, so wait for that PV's
+          // own commit before O may be touched (every step, to keep the
+          // phases in step).
+          ok = __all_sync(0xffffffffu,
+                          wait_bounded(bar_o + 8, pv_waits & 1, abort_flag,
+                                       p, 3));
+          if (!ok) break;
+          ++pv_waits;
+          ptx::tc_fence_after();
+        }
         if (j > 0 && __any_sync(0xffffffffu, m_new != m_run)) {
           // Correction: O_t *= alpha.  The previous PV into O_t is complete:
-          // it was issued before this tile's S_t, whose commit we waited on.
+          // it was issued before this tile's S_t, whose commit we waited on
+          // (packed: its own commit, waited on just above).
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) {
             uint32_t o[32];
@@ -604,7 +794,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
         l_run += (sm[0] + sm[1]) + (sm[2] + sm[3]);
         m_run = m_new;
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar_p + 8 * t);
+        ptx::mbar_arrive(bar_p + 8 * sb);
       }
       if (!ok) break;
 
@@ -619,7 +809,9 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
       ++o_waits;
       ptx::tc_fence_after();
 
-      if (p.o_part == nullptr) {
+      if (!live) {
+        // Padding rows only: nothing to store.
+      } else if (p.o_part == nullptr) {
         const float inv_l = ptx::rcp(l_run);
         const long long row = static_cast<long long>(q_plane) * p.Sq + q_row;
         uint4* orow =
@@ -668,6 +860,24 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
         }
         if (row_ok)
           p.lse_part[prow] = empty ? -INFINITY : (m_run + ptx::lg2(l_run)) * kLn2;
+      }
+      if (p.o_part != nullptr) {
+        // The unit that lands last among the key ranges of this tile's rows
+        // merges them (no second launch).  Partials are published with a
+        // device-scope fence before the arrival and read through L2 after.
+        volatile int* merge_flag =
+            reinterpret_cast<volatile int*>(smem + L::kMiscOff + 8 + 4 * t);
+        __threadfence();
+        ptx::named_barrier_sync(1 + t, kTM);
+        if (r == 0)
+          *merge_flag = merge_arrive(
+              p.merge_ctr + 2 * (u / p.num_splits) + t, p.merge_seq,
+              ranges_visited(p, m0), p);
+        ptx::named_barrier_sync(1 + t, kTM);
+        if (*merge_flag) {
+          __threadfence();
+          merge_tile<D, kBF16>(p, t ? w.plane[1] : w.plane[0], m0, r);
+        }
       }
       ptx::tc_fence_before();
     }

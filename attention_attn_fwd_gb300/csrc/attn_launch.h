@@ -21,11 +21,4 @@ cudaError_t launch_fwd_d128(bool bf16, const CUtensorMap& q,
                             const CUtensorMap& k, const CUtensorMap& v,
                             const FwdParams& p, int grid, cudaStream_t stream);
 
-// Split-KV merge of per-key-range partials into O and LSE (attn_combine.cu).
-cudaError_t launch_splitkv_combine(int D, bool bf16, const float* o_part,
-                                   const float* lse_part, void* O, float* LSE,
-                                   long long rows, int Sq, int num_splits,
-                                   int split_keys, int Skv, int causal,
-                                   int input_pos, cudaStream_t stream);
-
 }  // namespace attn

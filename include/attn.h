@@ -96,11 +96,15 @@ attn_status_t attn_fwd(const void* Q, const void* K, const void* V, void* O,
  *                  same shape (other counts give ATTN_ERR_INVALID_ARG);
  * workspace        device memory owned by the caller, 256-byte aligned,
  *                  of at least the size attn_splitkv_plan reports: fp32
- *                  partial outputs [num_splits, B, Hq, Sq, D] followed by
- *                  fp32 partial LSEs [num_splits, B, Hq, Sq];
+ *                  partial outputs [num_splits, B, Hq, Sq, D], fp32
+ *                  partial LSEs [num_splits, B, Hq, Sq], then 64-bit
+ *                  merge counters; its contents need no initialisation
+ *                  (each call tags its counter updates with a number of
+ *                  its own);
  * workspace_bytes  its size.
- * Two kernels are enqueued on `stream` (partials, then the merge).  The
- * workspace must not be used by another call until both have run.
+ * One kernel is enqueued on `stream`: the unit that finishes a row block's
+ * last key range merges that row block.  The workspace must not be used by
+ * another call until this one has run.
  */
 attn_status_t attn_fwd_splitkv(const void* Q, const void* K, const void* V,
                                void* O, float* LSE, int B, int Hq, int Hkv,

@@ -120,8 +120,11 @@ def test_splitkv_plan_host_only(lib):
                                     attn.ATTN_BF16, 5)
     assert ns == 4           # 8 tiles in 5 requested ranges: 2 tiles each
     rows = 2 * 8 * 1
+    # Packed GQA: one row block per (batch, K/V head), two counters each.
+    counters = 2 * 2 * 2
     assert ws == (-(-(ns * rows * 128 * 4) // 256) * 256 +
-                  -(-(ns * rows * 4) // 256) * 256)
+                  -(-(ns * rows * 4) // 256) * 256 +
+                  -(-(counters * 8) // 256) * 256)
     ns1, _ = attn.attn_splitkv_plan(1, 2, 2, 4, 100, 64, 0, 0,
                                     attn.ATTN_F16, 8)
     assert ns1 == 1          # 100 keys: a single tile

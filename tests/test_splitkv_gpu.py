@@ -122,3 +122,31 @@ def test_decode_workload_full():
         TOL_O[w.dtype]
     assert float(np.max(np.abs(lse.double().cpu().numpy() - lse_ref))) <= \
         TOL_LSE
+
+
+@pytest.mark.parametrize("fill", [0x00, 0xA5, 0xFF])
+def test_workspace_contents_and_reuse(fill):
+    """The workspace needs no clearing: it starts as arbitrary bytes and is
+    reused by calls of different shapes and split counts in a row."""
+    a = W("reuse_a", 2, 8, 2, 1, 1500, 128, "bf16", True, 1499)
+    b = W("reuse_b", 1, 4, 2, 40, 900, 64, "f16", True, 860)
+    c = W("reuse_c", 1, 3, 1, 130, 513, 64, "bf16", True, 383)  # not packed
+    plans = [(a, 4), (b, 3), (c, 2), (a, 6), (a, 4), (c, 2)]
+    need = max(attn.attn_splitkv_plan(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, 1,
+                                      w.input_pos,
+                                      attn.ATTN_BF16 if w.dtype == "bf16"
+                                      else attn.ATTN_F16, s)[1]
+               for w, s in plans)
+    buf = torch.full((need,), fill, dtype=torch.uint8, device="cuda")
+    for w, s in plans:
+        q, k, v = make_qkv(w, seed=24)
+        o, lse = attn.fwd_splitkv(q.cuda(), k.cuda(), v.cuda(), scale=w.scale,
+                                  causal=True, input_pos=w.input_pos,
+                                  num_splits=s, workspace=buf)
+        torch.cuda.synchronize()
+        assert attn.attn_device_status() == (0, 0)
+        o_ref, lse_ref = oracle.attention(q, k, v, w.scale, True, w.input_pos)
+        assert float(np.max(np.abs(o.double().cpu().numpy() - o_ref))) <= \
+            TOL_O[w.dtype], (w.name, s)
+        assert float(np.max(np.abs(lse.double().cpu().numpy() - lse_ref))) <= \
+            TOL_LSE, (w.name, s)
