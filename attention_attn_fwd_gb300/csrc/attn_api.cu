@@ -333,8 +333,11 @@ attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
   const int grid = static_cast<int>(std::min<long long>(p.num_units, sms));
   const bool bf16 = dtype == ATTN_BF16;
   const cudaError_t err =
-      s.D == 64 ? attn::launch_fwd_d64(bf16, tq, tk, tv, p, grid, stream)
-                : attn::launch_fwd_d128(bf16, tq, tk, tv, p, grid, stream);
+      s.D == 64
+          ? (pack ? attn::launch_fwd_d64_packed(bf16, tq, tk, tv, p, grid, stream)
+                  : attn::launch_fwd_d64(bf16, tq, tk, tv, p, grid, stream))
+          : (pack ? attn::launch_fwd_d128_packed(bf16, tq, tk, tv, p, grid, stream)
+                  : attn::launch_fwd_d128(bf16, tq, tk, tv, p, grid, stream));
   return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -94,12 +94,15 @@ struct Layout {
   static constexpr int kBoxBytes = 128 * 128;            // 128 rows x 128 B
   static constexpr int kTileBytes = kChunks * kBoxBytes; // one Q/K/V tile
   static constexpr int kSlots = (D == 128) ? 4 : 8;      // K/V ring slots
+  // Packed GQA tiles leave Q buffer 1 unused; it sits right before the
+  // ring and becomes one more slot there.
+  static constexpr int kMaxSlots = kSlots + 1;
   static constexpr int kQOff = 0;
   static constexpr int kRingOff = kQOff + 2 * kTileBytes;
   static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
-  // barriers: q_full[2], full[S], empty[S], s_full[2], p_full[2], o_full[2],
-  // drain[1], q_free[2]
-  static constexpr int kNumBars = 2 + 2 * kSlots + 2 + 2 + 2 + 1 + 2;
+  // barriers: q_full[2], full[S+1], empty[S+1], s_full[2], p_full[2],
+  // o_full[2], drain[1], q_free[2]
+  static constexpr int kNumBars = 2 + 2 * kMaxSlots + 2 + 2 + 2 + 1 + 2;
   // misc: TMEM base, abort flag, per-tile "merge here" flags
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
   static constexpr int kBytes = kMiscOff + 16;
@@ -170,13 +173,14 @@ struct Unit {
   int n_kv;      // K/V tiles the unit streams
 };
 
+template <bool kPack>
 __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   Unit w;
   w.split = u % p.num_splits;
   u /= p.num_splits;
   w.kt0 = w.split * p.split_tiles;
   const int kt1 = w.kt0 + p.split_tiles;
-  if (p.pack_gqa) {
+  if constexpr (kPack) {
     // Unit = one (batch, K/V head): tile 0 holds all its query rows.
     const int b = u / p.Hkv;
     const int kvh = u % p.Hkv;
@@ -247,7 +251,7 @@ __device__ __forceinline__ bool merge_arrive(unsigned long long* ctr,
 // across ranges.  Ranges past a row's causal horizon hold nothing for it
 // and are not read.  Thread tid takes 4 columns of one row, so the 32 (or
 // 16) threads of a row read its partials as contiguous 512 (256) bytes.
-template <int D, bool kBF16>
+template <int D, bool kBF16, bool kPack>
 __device__ __forceinline__ void merge_tile(const FwdParams& p, int plane0,
                                            int m0, int tid) {
   constexpr float kLog2e = 1.4426950408889634f;
@@ -256,11 +260,11 @@ __device__ __forceinline__ void merge_tile(const FwdParams& p, int plane0,
   const long long rows = static_cast<long long>(p.B) * p.Hq * p.Sq;
   const int split_keys = p.split_tiles * cfg::kTN;
   const int nrows =
-      p.pack_gqa ? p.group * p.Sq : min(cfg::kTM, p.Sq - m0);
+      kPack ? p.group * p.Sq : min(cfg::kTM, p.Sq - m0);
   const int cg = tid % kGroups;
   for (int r = tid / kGroups; r < nrows; r += kRowsPerPass) {
     int q_plane = plane0, q_row = m0 + r;
-    if (p.pack_gqa) {
+    if constexpr (kPack) {
       q_plane += r / p.Sq;
       q_row = r % p.Sq;
     }
@@ -308,7 +312,11 @@ __device__ __forceinline__ int unit_index(int k, int cta, int ctas) {
 // rounds.  Barrier phases, the K/V ring position and
 // TMEM carry over from unit to unit, so the next unit's Q load and first
 // MMAs overlap the current unit's last MMAs and epilogue.
-template <int D, bool kBF16>
+// kPack: the query heads of a GQA group share tile 0 (few query rows).
+// kSplit: split-KV launch (o_part set) -- compiles the in-kernel merge of
+// the per-range partial results; the partial writes themselves follow
+// o_part at run time.
+template <int D, bool kBF16, bool kPack, bool kSplit>
 __global__ void __launch_bounds__(cfg::kThreads, 1)
     attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
@@ -324,9 +332,9 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
   const uint32_t s_ring = s_base + L::kRingOff;
   const uint32_t bar0 = s_base + L::kBarOff;
   const uint32_t bar_q = bar0;                         // [2]
-  const uint32_t bar_full = bar0 + 8 * 2;              // [kSlots]
-  const uint32_t bar_empty = bar_full + 8 * L::kSlots; // [kSlots]
-  const uint32_t bar_s = bar_empty + 8 * L::kSlots;    // [2]
+  const uint32_t bar_full = bar0 + 8 * 2;                 // [kMaxSlots]
+  const uint32_t bar_empty = bar_full + 8 * L::kMaxSlots; // [kMaxSlots]
+  const uint32_t bar_s = bar_empty + 8 * L::kMaxSlots;    // [2]
   const uint32_t bar_p = bar_s + 8 * 2;                // [2]
   const uint32_t bar_o = bar_p + 8 * 2;                // [2]
   const uint32_t bar_drain = bar_o + 8 * 2;            // [1]
@@ -336,13 +344,17 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  // K/V ring: kSlots slots after the Q buffers, or (packed) one more
+  // starting at Q buffer 1.
+  constexpr int nslots = kPack ? L::kMaxSlots : L::kSlots;
+  const uint32_t s_ring0 = kPack ? s_ring - L::kTileBytes : s_ring;
   const int u_first = static_cast<int>(blockIdx.x);
   const int u_step = static_cast<int>(gridDim.x);
 
-  if (p.pack_gqa) {
+  if constexpr (kPack) {
     // A packed Q load fills only group*Sq rows of the tile: keep the other
     // rows zero so their (discarded) scores stay finite.
-    for (int i = threadIdx.x; i < 2 * L::kTileBytes / 16; i += kThreads)
+    for (int i = threadIdx.x; i < L::kTileBytes / 16; i += kThreads)
       ptx::st_shared_v4(s_q + 16 * i, 0u, 0u, 0u, 0u);
     ptx::fence_proxy_async_smem();
   }
@@ -379,7 +391,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
     for (int k = 0; k * u_step < p.num_units && ok; ++k) {
       const int u = unit_index(k, u_first, u_step);
       if (u >= p.num_units) continue;
-      const Unit w = decode_unit(p, u);
+      const Unit w = decode_unit<kPack>(p, u);
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (w.n[t] == 0 || !ok) continue;
@@ -399,15 +411,15 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
       }
       for (int j = 0; j < w.n_kv && ok; ++j) {
         for (int kv = 0; kv < 2; ++kv) {
-          const int slot = it % L::kSlots;
-          if (it >= L::kSlots) {
+          const int slot = it % nslots;
+          if (it >= nslots) {
             ok = __all_sync(0xffffffffu,
                             wait_bounded(bar_empty + 8 * slot,
-                                         ((it / L::kSlots) - 1) & 1,
+                                         ((it / nslots) - 1) & 1,
                                          abort_flag, p, 1));
             if (!ok) break;
           }
-          const uint32_t dst = s_ring + slot * L::kTileBytes;
+          const uint32_t dst = s_ring0 + slot * L::kTileBytes;
           ptx::mbar_arrive_expect_tx_elect(bar_full + 8 * slot, L::kTileBytes);
           for (int c = 0; c < L::kChunks; ++c)
             ptx::tma_load_3d_elect(dst + c * L::kBoxBytes, kv ? &tm_v : &tm_k,
@@ -421,8 +433,8 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
       // Let every copy still in flight land before the CTA goes away.
       for (int t = 0; t < 2; ++t)
         if (q_loads[t] > 0) drain_wait(bar_q + 8 * t, (q_loads[t] - 1) & 1, p);
-      for (int i = max(0, it - L::kSlots); i < it; ++i)
-        drain_wait(bar_full + 8 * (i % L::kSlots), (i / L::kSlots) & 1, p);
+      for (int i = max(0, it - nslots); i < it; ++i)
+        drain_wait(bar_full + 8 * (i % nslots), (i / nslots) & 1, p);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -440,8 +452,8 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
     // halves of D, SBO = 1024 between groups of 8 keys.
     constexpr uint32_t kHi = ptx::sdesc_hi_sw128(1024);
     const uint32_t q_lo = ptx::sdesc_lo(s_q, 16);
-    const uint32_t k_lo = ptx::sdesc_lo(s_ring, 16);
-    const uint32_t v_lo = ptx::sdesc_lo(s_ring, L::kBoxBytes);
+    const uint32_t k_lo = ptx::sdesc_lo(s_ring0, 16);
+    const uint32_t v_lo = ptx::sdesc_lo(s_ring0, L::kBoxBytes);
     constexpr uint32_t kTile16 = L::kTileBytes >> 4;
 
     // S = Q_t K_j^T into S region `sb`: A = Q tile (K-major), B = K tile
@@ -476,11 +488,11 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
     for (int k = 0; k * u_step < p.num_units && ok; ++k) {
       const int u = unit_index(k, u_first, u_step);
       if (u >= p.num_units) continue;
-      const Unit w = decode_unit(p, u);
+      const Unit w = decode_unit<kPack>(p, u);
       // A key range wholly past the causal horizon of both tiles has no
       // work (split-KV only); the producer and softmax warps skip it too.
       if (w.n_kv == 0) continue;
-      if (p.pack_gqa) {
+      if constexpr (kPack) {
         // One Q tile whose scores alternate between the two S regions:
         // S(j+1) is computed while the softmax warps work on S(j), and
         // S(j+2) reuses region j%2 once PV(j) (issued just before it, and
@@ -496,14 +508,14 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
         for (int sb = 0; sb < 2 && sb < n && ok; ++sb) {
           const int it_k = it0 + 2 * sb;
           ok = __all_sync(0xffffffffu,
-                          wait_bounded(bar_full + 8 * (it_k % L::kSlots),
-                                       (it_k / L::kSlots) & 1, abort_flag, p,
+                          wait_bounded(bar_full + 8 * (it_k % nslots),
+                                       (it_k / nslots) & 1, abort_flag, p,
                                        2));
           if (!ok) break;
           ptx::tc_fence_after();
-          issue_qk(0, sb, it_k % L::kSlots);
+          issue_qk(0, sb, it_k % nslots);
           ptx::tc_commit_elect(bar_s + 8 * sb);
-          ptx::tc_commit_elect(bar_empty + 8 * (it_k % L::kSlots));
+          ptx::tc_commit_elect(bar_empty + 8 * (it_k % nslots));
           if (sb == n - 1) ptx::tc_commit_elect(bar_qfree);
           issued_any = true;
         }
@@ -511,8 +523,8 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
           const int sb = j & 1;
           const int it_v = it0 + 2 * j + 1;
           ok = __all_sync(0xffffffffu,
-                          wait_bounded(bar_full + 8 * (it_v % L::kSlots),
-                                       (it_v / L::kSlots) & 1, abort_flag, p,
+                          wait_bounded(bar_full + 8 * (it_v % nslots),
+                                       (it_v / nslots) & 1, abort_flag, p,
                                        2));
           if (!ok) break;
           const int pw = sb ? p_waits[1] : p_waits[0];
@@ -521,19 +533,19 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
           if (!ok) break;
           if (sb) ++p_waits[1]; else ++p_waits[0];
           ptx::tc_fence_after();
-          issue_pv(0, sb, it_v % L::kSlots, j > 0);
+          issue_pv(0, sb, it_v % nslots, j > 0);
           ptx::tc_commit_elect(j == n - 1 ? bar_o : bar_o + 8);
-          ptx::tc_commit_elect(bar_empty + 8 * (it_v % L::kSlots));
+          ptx::tc_commit_elect(bar_empty + 8 * (it_v % nslots));
           if (j + 2 < n) {
             const int it_k = it0 + 2 * (j + 2);
             ok = __all_sync(0xffffffffu,
-                            wait_bounded(bar_full + 8 * (it_k % L::kSlots),
-                                         (it_k / L::kSlots) & 1, abort_flag,
+                            wait_bounded(bar_full + 8 * (it_k % nslots),
+                                         (it_k / nslots) & 1, abort_flag,
                                          p, 2));
             if (!ok) break;
-            issue_qk(0, sb, it_k % L::kSlots);
+            issue_qk(0, sb, it_k % nslots);
             ptx::tc_commit_elect(bar_s + 8 * sb);
-            ptx::tc_commit_elect(bar_empty + 8 * (it_k % L::kSlots));
+            ptx::tc_commit_elect(bar_empty + 8 * (it_k % nslots));
             if (j + 2 == n - 1) ptx::tc_commit_elect(bar_qfree);
           }
         }
@@ -624,7 +636,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
     // nothing.  Its P rows stay whatever S left there, which only reaches
     // the matching O rows (row i of P V is row i of P times V), and those
     // are never stored.
-    const bool live = !p.pack_gqa || (warp % 4) * 32 < p.group * p.Sq;
+    const bool live = !kPack || (warp % 4) * 32 < p.group * p.Sq;
     bool ok = true;
     int s_waits = 0;   // S-ready phases consumed (packed: S region 0)
     int s_waits1 = 0;  // packed: S-ready phases of S region 1
@@ -634,7 +646,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
     for (int k = 0; k * u_step < p.num_units && ok; ++k) {
       const int u = unit_index(k, u_first, u_step);
       if (u >= p.num_units) continue;
-      const Unit w = decode_unit(p, u);
+      const Unit w = decode_unit<kPack>(p, u);
       const int n = t ? w.n[1] : w.n[0];
       if (n == 0) continue;
       const int ms = t ? w.ms[1] : w.ms[0];
@@ -643,7 +655,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
       int q_plane = t ? w.plane[1] : w.plane[0];
       int q_row = m0 + r;
       bool row_ok = q_row < p.Sq;
-      if (p.pack_gqa) {
+      if constexpr (kPack) {
         q_plane += r / p.Sq;
         q_row = r % p.Sq;
         row_ok = r < p.group * p.Sq;
@@ -654,9 +666,9 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
 
       for (int j = 0; j < n; ++j) {
         // S region of this step: the tile's own, or (packed) alternating.
-        const int sb = p.pack_gqa ? (j & 1) : t;
+        const int sb = kPack ? (j & 1) : t;
         const uint32_t t_s = tmem + lane_off + sb * kTN;
-        const bool odd = p.pack_gqa && sb == 1;
+        const bool odd = kPack && sb == 1;
         ok = __all_sync(0xffffffffu,
                         wait_bounded(bar_s + 8 * sb,
                                      (odd ? s_waits1 : s_waits) & 1,
@@ -763,7 +775,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
           }
         }
 
-        if (p.pack_gqa && j > 0) {
+        if (kPack && j > 0) {
           // Packed: S_j was issued before PV_{j-1}, so wait for that PV's
           // own commit before O may be touched (every step, to keep the
           // phases in step).
@@ -861,7 +873,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
         if (row_ok)
           p.lse_part[prow] = empty ? -INFINITY : (m_run + ptx::lg2(l_run)) * kLn2;
       }
-      if (p.o_part != nullptr) {
+      if constexpr (kSplit) {
         // The unit that lands last among the key ranges of this tile's rows
         // merges them (no second launch).  Partials are published with a
         // device-scope fence before the arrival and read through L2 after.
@@ -876,7 +888,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
         ptx::named_barrier_sync(1 + t, kTM);
         if (*merge_flag) {
           __threadfence();
-          merge_tile<D, kBF16>(p, t ? w.plane[1] : w.plane[0], m0, r);
+          merge_tile<D, kBF16, kPack>(p, t ? w.plane[1] : w.plane[0], m0, r);
         }
       }
       ptx::tc_fence_before();

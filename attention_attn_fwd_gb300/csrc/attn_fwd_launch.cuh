@@ -1,0 +1,52 @@
+// Launch of one instantiation of the forward kernel; included by the
+// per-variant translation units (compiled in parallel).
+#pragma once
+
+#include "attn_launch.h"
+
+namespace attn {
+// Internal linkage: each translation unit (and each loaded copy of the
+// library) keeps its own "attribute set" flag per kernel.
+namespace {
+
+template <int D, bool kBF16, bool kPack, bool kSplit>
+cudaError_t launch_variant(const CUtensorMap& q, const CUtensorMap& k,
+                           const CUtensorMap& v, const FwdParams& p, int grid,
+                           cudaStream_t stream) {
+  auto kernel = attn_fwd_sm103_kernel<D, kBF16, kPack, kSplit>;
+  const int smem = Layout<D>::kSmemBytes;
+  // The attribute is per device; setting it again is cheap and idempotent.
+  static thread_local int configured_device = -1;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (configured_device != dev) {
+    err = cudaFuncSetAttribute(kernel,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               smem);
+    if (err != cudaSuccess) return err;
+    configured_device = dev;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(cfg::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, kernel, q, k, v, p);
+}
+
+// Dtype and split-KV dispatch of one (D, tile mode) variant; split-KV when
+// the parameters carry partial-result buffers.
+template <int D, bool kPack>
+cudaError_t launch_mode(bool bf16, const CUtensorMap& q, const CUtensorMap& k,
+                        const CUtensorMap& v, const FwdParams& p, int grid,
+                        cudaStream_t stream) {
+  if (p.o_part != nullptr)
+    return bf16 ? launch_variant<D, true, kPack, true>(q, k, v, p, grid, stream)
+                : launch_variant<D, false, kPack, true>(q, k, v, p, grid, stream);
+  return bf16 ? launch_variant<D, true, kPack, false>(q, k, v, p, grid, stream)
+              : launch_variant<D, false, kPack, false>(q, k, v, p, grid, stream);
+}
+
+}  // namespace
+}  // namespace attn

@@ -14,11 +14,21 @@ int fwd_smem_bytes(int D);
 // Ring slots (K/V tiles in flight) of the D-variant.
 int fwd_stages(int D);
 
+// One entry per kernel translation unit: head dimension x tile mode (two
+// 128-row Q tiles, or the query heads of a GQA group packed into one).
 cudaError_t launch_fwd_d64(bool bf16, const CUtensorMap& q,
                            const CUtensorMap& k, const CUtensorMap& v,
                            const FwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_fwd_d128(bool bf16, const CUtensorMap& q,
                             const CUtensorMap& k, const CUtensorMap& v,
                             const FwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_d64_packed(bool bf16, const CUtensorMap& q,
+                                  const CUtensorMap& k, const CUtensorMap& v,
+                                  const FwdParams& p, int grid,
+                                  cudaStream_t stream);
+cudaError_t launch_fwd_d128_packed(bool bf16, const CUtensorMap& q,
+                                   const CUtensorMap& k, const CUtensorMap& v,
+                                   const FwdParams& p, int grid,
+                                   cudaStream_t stream);
 
 }  // namespace attn
