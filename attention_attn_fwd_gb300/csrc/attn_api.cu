@@ -136,9 +136,10 @@ struct TileChoice {
 };
 
 TileChoice choose_tiles(const Shape& s) {
-  const int block_m = pack_gqa(s) ? (s.Hq / s.Hkv) * s.Sq : attn::cfg::kBlockM;
-  return TileChoice{block_m, attn::cfg::kTN, attn::fwd_stages(s.D),
-                    attn::fwd_smem_bytes(s.D)};
+  const bool pack = pack_gqa(s);
+  const int block_m = pack ? (s.Hq / s.Hkv) * s.Sq : attn::cfg::kBlockM;
+  return TileChoice{block_m, attn::cfg::kTN, attn::fwd_stages(s.D, pack),
+                    attn::fwd_smem_bytes(s.D, pack)};
 }
 
 bool is_device_ptr(const void* p, int dev) {
@@ -185,11 +186,14 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }  // namespace
 
 namespace attn {
-int fwd_smem_bytes(int D) {
+int fwd_smem_bytes(int D, bool pack) {
+  if (pack)
+    return D == 64 ? Layout<64, true>::kSmemBytes : Layout<128, true>::kSmemBytes;
   return D == 64 ? Layout<64>::kSmemBytes : Layout<128>::kSmemBytes;
 }
-int fwd_stages(int D) {
+int fwd_stages(int D, bool pack) {
   // Each slot holds one K or one V tile; a stage is a K and a V tile.
+  if (pack) return (D == 64 ? Layout<64, true>::kSlots : Layout<128, true>::kSlots) / 2;
   return (D == 64 ? Layout<64>::kSlots : Layout<128>::kSlots) / 2;
 }
 }  // namespace attn

@@ -22,8 +22,9 @@
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 and O1 (D columns each)
 // from 256.  P_t (16-bit) overwrites the first 64 columns of S_t and is the
 // A operand of O_t += P_t V straight from TMEM.  With the query heads of a
-// GQA group packed into tile 0 (few query rows), tile 1 is unused and its S
-// region double-buffers the scores of tile 0 instead.
+// GQA group packed into tile 0 (few query rows), there is no tile 1: its S
+// region double-buffers the scores of tile 0 and its shared memory goes to
+// the K/V ring.
 //
 // Every mbarrier wait is bounded: on timeout the waiter raises a CTA-wide
 // abort flag and a device status word, every role stops issuing work, waits
@@ -88,25 +89,28 @@ constexpr float kRescaleTau = 8.0f;  // lazy rescale threshold (log2 units)
 constexpr float kLn2 = 0.6931471805599453f;
 }  // namespace cfg
 
-template <int D>
+// Shared memory of one CTA: Q tiles, the K/V slot ring, mbarriers.  The
+// packed variant has one Q tile and fills the rest of the 227 KB with ring
+// slots (a decode step is bound by the K/V bytes in flight per SM).
+template <int D, bool kPack = false>
 struct Layout {
   static constexpr int kChunks = D / 64;                 // 128-byte boxes/row
   static constexpr int kBoxBytes = 128 * 128;            // 128 rows x 128 B
   static constexpr int kTileBytes = kChunks * kBoxBytes; // one Q/K/V tile
-  static constexpr int kSlots = (D == 128) ? 4 : 8;      // K/V ring slots
-  // Packed GQA tiles leave Q buffer 1 unused; it sits right before the
-  // ring and becomes one more slot there.
-  static constexpr int kMaxSlots = kSlots + 1;
+  static constexpr int kQTiles = kPack ? 1 : 2;
+  static constexpr int kSlots =                           // K/V ring slots
+      kPack ? (D == 128 ? 6 : 13) : (D == 128 ? 4 : 8);
   static constexpr int kQOff = 0;
-  static constexpr int kRingOff = kQOff + 2 * kTileBytes;
+  static constexpr int kRingOff = kQOff + kQTiles * kTileBytes;
   static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
-  // barriers: q_full[2], full[S+1], empty[S+1], s_full[2], p_full[2],
-  // o_full[2], drain[1], q_free[2]
-  static constexpr int kNumBars = 2 + 2 * kMaxSlots + 2 + 2 + 2 + 1 + 2;
+  // barriers: q_full[2], full[S], empty[S], s_full[2], p_full[2], o_full[2],
+  // drain[1], q_free[2]
+  static constexpr int kNumBars = 2 + 2 * kSlots + 2 + 2 + 2 + 1 + 2;
   // misc: TMEM base, abort flag, per-tile "merge here" flags
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kSmemBytes = kBytes + 1024;  // slack for 1 KB alignment
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 };
 
 // K/V tiles [kt0, kt0 + n) of the key range [kt0, kt1) are visited by the
@@ -221,13 +225,18 @@ __device__ __forceinline__ int ranges_visited(const FwdParams& p, int m0) {
 // Counts this unit's arrival on a tile's merge counter; true for the
 // arrival that completes the expected set of this call.  A counter left by
 // an earlier call (another sequence number) restarts at one, so the
-// workspace needs no clearing.  Lock-free: a CAS fails only when another
-// arrival succeeded, so the loop ends within `expect` rounds; the cap only
-// guards against a corrupted counter.
+// workspace needs no clearing.  The first CAS guesses that every other
+// range has arrived, so the arrival that completes the set usually needs
+// one round trip.  Lock-free: a CAS fails only when the guess was stale or
+// another arrival succeeded, so the loop ends within `expect` + 1 rounds;
+// the cap only guards against a corrupted counter.  Acquire-release: the
+// caller's CTA barrier orders its warpgroup's partial writes before this
+// operation, which publishes them; the completing arrival acquires all.
 __device__ __forceinline__ bool merge_arrive(unsigned long long* ctr,
                                              unsigned int seq, int expect,
                                              const FwdParams& p) {
-  unsigned long long cur = atomicAdd(ctr, 0ull);
+  unsigned long long cur = (static_cast<unsigned long long>(seq) << 32) |
+                           static_cast<unsigned int>(expect - 1);
   for (int i = 0; i < (1 << 16); ++i) {
     const unsigned int cnt =
         static_cast<unsigned int>(cur >> 32) == seq
@@ -235,7 +244,7 @@ __device__ __forceinline__ bool merge_arrive(unsigned long long* ctr,
             : 1u;
     const unsigned long long nv =
         (static_cast<unsigned long long>(seq) << 32) | cnt;
-    const unsigned long long prev = atomicCAS(ctr, cur, nv);
+    const unsigned long long prev = ptx::atom_cas_acq_rel_gpu(ctr, cur, nv);
     if (prev == cur) return cnt == static_cast<unsigned int>(expect);
     cur = prev;
   }
@@ -322,7 +331,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
                           const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v,
                           const FwdParams p) {
-  using L = Layout<D>;
+  using L = Layout<D, kPack>;
   using namespace cfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -332,9 +341,9 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
   const uint32_t s_ring = s_base + L::kRingOff;
   const uint32_t bar0 = s_base + L::kBarOff;
   const uint32_t bar_q = bar0;                         // [2]
-  const uint32_t bar_full = bar0 + 8 * 2;                 // [kMaxSlots]
-  const uint32_t bar_empty = bar_full + 8 * L::kMaxSlots; // [kMaxSlots]
-  const uint32_t bar_s = bar_empty + 8 * L::kMaxSlots;    // [2]
+  const uint32_t bar_full = bar0 + 8 * 2;              // [kSlots]
+  const uint32_t bar_empty = bar_full + 8 * L::kSlots; // [kSlots]
+  const uint32_t bar_s = bar_empty + 8 * L::kSlots;    // [2]
   const uint32_t bar_p = bar_s + 8 * 2;                // [2]
   const uint32_t bar_o = bar_p + 8 * 2;                // [2]
   const uint32_t bar_drain = bar_o + 8 * 2;            // [1]
@@ -344,10 +353,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  // K/V ring: kSlots slots after the Q buffers, or (packed) one more
-  // starting at Q buffer 1.
-  constexpr int nslots = kPack ? L::kMaxSlots : L::kSlots;
-  const uint32_t s_ring0 = kPack ? s_ring - L::kTileBytes : s_ring;
+  constexpr int nslots = L::kSlots;
   const int u_first = static_cast<int>(blockIdx.x);
   const int u_step = static_cast<int>(gridDim.x);
 
@@ -419,7 +425,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
                                          abort_flag, p, 1));
             if (!ok) break;
           }
-          const uint32_t dst = s_ring0 + slot * L::kTileBytes;
+          const uint32_t dst = s_ring + slot * L::kTileBytes;
           ptx::mbar_arrive_expect_tx_elect(bar_full + 8 * slot, L::kTileBytes);
           for (int c = 0; c < L::kChunks; ++c)
             ptx::tma_load_3d_elect(dst + c * L::kBoxBytes, kv ? &tm_v : &tm_k,
@@ -452,8 +458,8 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
     // halves of D, SBO = 1024 between groups of 8 keys.
     constexpr uint32_t kHi = ptx::sdesc_hi_sw128(1024);
     const uint32_t q_lo = ptx::sdesc_lo(s_q, 16);
-    const uint32_t k_lo = ptx::sdesc_lo(s_ring0, 16);
-    const uint32_t v_lo = ptx::sdesc_lo(s_ring0, L::kBoxBytes);
+    const uint32_t k_lo = ptx::sdesc_lo(s_ring, 16);
+    const uint32_t v_lo = ptx::sdesc_lo(s_ring, L::kBoxBytes);
     constexpr uint32_t kTile16 = L::kTileBytes >> 4;
 
     // S = Q_t K_j^T into S region `sb`: A = Q tile (K-major), B = K tile
@@ -875,11 +881,13 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
       }
       if constexpr (kSplit) {
         // The unit that lands last among the key ranges of this tile's rows
-        // merges them (no second launch).  Partials are published with a
-        // device-scope fence before the arrival and read through L2 after.
+        // merges them (no second launch).  The warpgroup barrier orders all
+        // its partial writes before the counter update (a release at GPU
+        // scope); the completing update acquires the other units' partials,
+        // and the second barrier hands that on to the merging threads, which
+        // read through L2.
         volatile int* merge_flag =
             reinterpret_cast<volatile int*>(smem + L::kMiscOff + 8 + 4 * t);
-        __threadfence();
         ptx::named_barrier_sync(1 + t, kTM);
         if (r == 0)
           *merge_flag = merge_arrive(
@@ -887,7 +895,6 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
               ranges_visited(p, m0), p);
         ptx::named_barrier_sync(1 + t, kTM);
         if (*merge_flag) {
-          __threadfence();
           merge_tile<D, kBF16, kPack>(p, t ? w.plane[1] : w.plane[0], m0, r);
         }
       }

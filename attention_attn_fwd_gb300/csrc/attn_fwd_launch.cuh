@@ -14,7 +14,7 @@ cudaError_t launch_variant(const CUtensorMap& q, const CUtensorMap& k,
                            const CUtensorMap& v, const FwdParams& p, int grid,
                            cudaStream_t stream) {
   auto kernel = attn_fwd_sm103_kernel<D, kBF16, kPack, kSplit>;
-  const int smem = Layout<D>::kSmemBytes;
+  const int smem = Layout<D, kPack>::kSmemBytes;
   // The attribute is per device; setting it again is cheap and idempotent.
   static thread_local int configured_device = -1;
   int dev = 0;

@@ -9,10 +9,10 @@
 
 namespace attn {
 
-// Dynamic shared memory one CTA of the D-variant needs.
-int fwd_smem_bytes(int D);
-// Ring slots (K/V tiles in flight) of the D-variant.
-int fwd_stages(int D);
+// Dynamic shared memory one CTA of the (D, packed) variant needs.
+int fwd_smem_bytes(int D, bool pack);
+// K/V stages (pairs of ring slots) of the (D, packed) variant.
+int fwd_stages(int D, bool pack);
 
 // One entry per kernel translation unit: head dimension x tile mode (two
 // 128-row Q tiles, or the query heads of a GQA group packed into one).

@@ -21,6 +21,20 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// 64-bit compare-and-swap in global memory at GPU scope, acquire-release:
+// publishes the writes ordered before it (also other threads' writes that
+// a CTA barrier ordered before it) and acquires those published by the
+// operations it reads from.
+__device__ __forceinline__ unsigned long long atom_cas_acq_rel_gpu(
+    unsigned long long* ptr, unsigned long long cmp, unsigned long long val) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;"
+               : "=l"(old)
+               : "l"(ptr), "l"(cmp), "l"(val)
+               : "memory");
+  return old;
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count)
