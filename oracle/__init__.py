@@ -43,35 +43,40 @@ class Oracle:
         dp = ctypes.POINTER(ctypes.c_double)
         L = ctypes.c_long
         lib.attn_oracle_fwd.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, L, L,
-                                        ctypes.c_double, ctypes.c_int, L]
+                                        ctypes.c_double, ctypes.c_int, L, L]
         lib.attn_oracle_fwd.restype = ctypes.c_int
         lib.attn_oracle_rows.argtypes = [dp, dp, dp, L, L, L, L, L, L,
-                                         ctypes.c_double, ctypes.c_int, L,
+                                         ctypes.c_double, ctypes.c_int, L, L,
                                          ctypes.POINTER(ctypes.c_int64), L,
                                          dp, dp]
         lib.attn_oracle_rows.restype = ctypes.c_int
         lib.attn_oracle_prob_row.argtypes = [dp, dp, dp, L, L, L, L, L, L,
                                              ctypes.c_double, ctypes.c_int, L,
-                                             L, L, L, dp]
+                                             L, L, L, L, dp]
         lib.attn_oracle_prob_row.restype = ctypes.c_int
         lib.attn_oracle_threads.argtypes = []
         lib.attn_oracle_threads.restype = ctypes.c_int
         self._lib = lib
 
-    def attention(self, q, k, v, scale, causal=False, input_pos=0):
-        """Full forward: (O [B,Hq,Sq,D], LSE [B,Hq,Sq]) in float64."""
+    def attention(self, q, k, v, scale, causal=False, input_pos=0, window=0):
+        """Full forward: (O [B,Hq,Sq,D], LSE [B,Hq,Sq]) in float64.
+
+        ``window`` > 0 (causal only): each query sees its last ``window``
+        positions."""
         q, k, v = _f64(q), _f64(k), _f64(v)
         B, Hq, Hkv, Sq, Skv, D = _shapes(q, k, v)
         o = np.zeros((B, Hq, Sq, D), np.float64)
         lse = np.zeros((B, Hq, Sq), np.float64)
         rc = self._lib.attn_oracle_fwd(
             _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq,
-            Skv, D, float(scale), int(bool(causal)), int(input_pos))
+            Skv, D, float(scale), int(bool(causal)), int(input_pos),
+            int(window))
         if rc != 0:
             raise ValueError("oracle rejected the arguments (code %d)" % rc)
         return o, lse
 
-    def attention_rows(self, q, k, v, scale, causal, input_pos, rows):
+    def attention_rows(self, q, k, v, scale, causal, input_pos, rows,
+                       window=0):
         """Rows (b, h, i) given as an (n, 3) int array: (O [n,D], LSE [n])."""
         q, k, v = _f64(q), _f64(k), _f64(v)
         B, Hq, Hkv, Sq, Skv, D = _shapes(q, k, v)
@@ -82,21 +87,21 @@ class Oracle:
         lse = np.zeros((n,), np.float64)
         rc = self._lib.attn_oracle_rows(
             _ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Sq, Skv, D, float(scale),
-            int(bool(causal)), int(input_pos),
+            int(bool(causal)), int(input_pos), int(window),
             rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n, _ptr(o),
             _ptr(lse))
         if rc != 0:
             raise ValueError("oracle rejected the arguments (code %d)" % rc)
         return o, lse
 
-    def prob_row(self, q, k, v, scale, causal, input_pos, b, h, i):
+    def prob_row(self, q, k, v, scale, causal, input_pos, b, h, i, window=0):
         """Softmax weights of query (b, h, i) over all keys, float64 [Skv]."""
         q, k, v = _f64(q), _f64(k), _f64(v)
         B, Hq, Hkv, Sq, Skv, D = _shapes(q, k, v)
         p = np.zeros((Skv,), np.float64)
         rc = self._lib.attn_oracle_prob_row(
             _ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Sq, Skv, D, float(scale),
-            int(bool(causal)), int(input_pos), b, h, i, _ptr(p))
+            int(bool(causal)), int(input_pos), int(window), b, h, i, _ptr(p))
         if rc != 0:
             raise ValueError("oracle rejected the arguments (code %d)" % rc)
         return p
@@ -116,16 +121,18 @@ def default() -> Oracle:
     return _default
 
 
-def attention(q, k, v, scale, causal=False, input_pos=0):
-    return default().attention(q, k, v, scale, causal, input_pos)
+def attention(q, k, v, scale, causal=False, input_pos=0, window=0):
+    return default().attention(q, k, v, scale, causal, input_pos, window)
 
 
-def attention_rows(q, k, v, scale, causal, input_pos, rows):
-    return default().attention_rows(q, k, v, scale, causal, input_pos, rows)
+def attention_rows(q, k, v, scale, causal, input_pos, rows, window=0):
+    return default().attention_rows(q, k, v, scale, causal, input_pos, rows,
+                                    window)
 
 
-def prob_row(q, k, v, scale, causal, input_pos, b, h, i):
-    return default().prob_row(q, k, v, scale, causal, input_pos, b, h, i)
+def prob_row(q, k, v, scale, causal, input_pos, b, h, i, window=0):
+    return default().prob_row(q, k, v, scale, causal, input_pos, b, h, i,
+                              window)
 
 
 def threads() -> int:

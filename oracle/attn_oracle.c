@@ -24,6 +24,16 @@
  *                                                 input_pos to the query
  *                                                 offsets and keeps keys with
  *                                                 query offset >= key offset)
+ *     and, with a sliding window of W >= 1 keys (causal only),
+ *     j > input_pos + i - W                      (the last W positions up to
+ *                                                 and including the query's:
+ *                                                 "Sliding window attention"
+ *                                                 is named as future work on
+ *                                                 "Flash Attention from
+ *                                                 Scratch", section "What's
+ *                                                 Next", without a definition;
+ *                                                 this is the reading taken.
+ *                                                 W = 0: no window)
  *     M     = max over visible j of s_j
  *     p_j   = exp(s_j - M) if visible else 0      (safe softmax)
  *     L     = sum_j p_j
@@ -54,11 +64,23 @@
 #define ORACLE_NO_MEMORY 2
 
 static int check_shape(long B, long Hq, long Hkv, long Sq, long Skv, long D,
-                       long input_pos) {
+                       int causal, long input_pos, long window) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Skv <= 0 || D <= 0) return 0;
   if (Hq % Hkv != 0) return 0;
   if (input_pos < 0) return 0;
+  if (window < 0 || (window > 0 && !causal)) return 0;
+  /* Every row must see a key: the last row's window must reach Skv - 1. */
+  if (window > 0 && Sq > 0 && input_pos + (Sq - 1) - window >= Skv - 1)
+    return 0;
   return 1;
+}
+
+/* Key j is visible to query row i (absolute position input_pos + i). */
+static int key_visible(int causal, long input_pos, long window, long i,
+                       long j) {
+  if (!causal) return 1;
+  if (!(j <= input_pos + i)) return 0;              /* no future keys */
+  return window <= 0 || j > input_pos + i - window;  /* sliding window */
 }
 
 /*
@@ -68,7 +90,7 @@ static int check_shape(long B, long Hq, long Hkv, long Sq, long Skv, long D,
  */
 static void oracle_row(const double* Q, const double* K, const double* V,
                        long Hq, long Hkv, long Sq, long Skv, long D,
-                       double scale, int causal, long input_pos,
+                       double scale, int causal, long input_pos, long window,
                        long b, long h, long i,
                        double* score, double* prob, double* out, double* lse) {
   const long group = Hq / Hkv;
@@ -87,14 +109,14 @@ static void oracle_row(const double* Q, const double* K, const double* V,
   /* Visibility and the row maximum over visible keys. */
   double M = -INFINITY;
   for (long j = 0; j < Skv; ++j) {
-    const int visible = !causal || j <= input_pos + i;
+    const int visible = key_visible(causal, input_pos, window, i, j);
     if (visible && score[j] > M) M = score[j];
   }
 
   /* Safe softmax: exponentials shifted by the maximum, then normalised. */
   double L = 0.0;
   for (long j = 0; j < Skv; ++j) {
-    const int visible = !causal || j <= input_pos + i;
+    const int visible = key_visible(causal, input_pos, window, i, j);
     prob[j] = visible ? exp(score[j] - M) : 0.0;
     L += prob[j];
   }
@@ -112,8 +134,10 @@ static void oracle_row(const double* Q, const double* K, const double* V,
 /* Full forward pass: every (b, h, i) row.  LSE may be NULL. */
 int attn_oracle_fwd(const double* Q, const double* K, const double* V,
                     double* O, double* LSE, long B, long Hq, long Hkv, long Sq,
-                    long Skv, long D, double scale, int causal, long input_pos) {
-  if (!check_shape(B, Hq, Hkv, Sq, Skv, D, input_pos)) return ORACLE_BAD_ARG;
+                    long Skv, long D, double scale, int causal, long input_pos,
+                    long window) {
+  if (!check_shape(B, Hq, Hkv, Sq, Skv, D, causal, input_pos, window))
+    return ORACLE_BAD_ARG;
   const long rows = B * Hq * Sq;
   int failed = 0;
 #pragma omp parallel
@@ -130,8 +154,8 @@ int attn_oracle_fwd(const double* Q, const double* K, const double* V,
         const long h = (r / Sq) % Hq;
         const long i = r % Sq;
         double lse;
-        oracle_row(Q, K, V, Hq, Hkv, Sq, Skv, D, scale, causal, input_pos, b,
-                   h, i, score, prob, O + r * D, &lse);
+        oracle_row(Q, K, V, Hq, Hkv, Sq, Skv, D, scale, causal, input_pos,
+                   window, b, h, i, score, prob, O + r * D, &lse);
         if (LSE) LSE[r] = lse;
       }
     }
@@ -148,10 +172,11 @@ int attn_oracle_fwd(const double* Q, const double* K, const double* V,
  */
 int attn_oracle_rows(const double* Q, const double* K, const double* V,
                      long B, long Hq, long Hkv, long Sq, long Skv, long D,
-                     double scale, int causal, long input_pos,
+                     double scale, int causal, long input_pos, long window,
                      const int64_t* rows_bhi, long n, double* O_rows,
                      double* LSE_rows) {
-  if (!check_shape(B, Hq, Hkv, Sq, Skv, D, input_pos)) return ORACLE_BAD_ARG;
+  if (!check_shape(B, Hq, Hkv, Sq, Skv, D, causal, input_pos, window))
+    return ORACLE_BAD_ARG;
   for (long r = 0; r < n; ++r) {
     const int64_t b = rows_bhi[3 * r], h = rows_bhi[3 * r + 1],
                   i = rows_bhi[3 * r + 2];
@@ -170,7 +195,8 @@ int attn_oracle_rows(const double* Q, const double* K, const double* V,
 #pragma omp for schedule(dynamic, 4)
       for (long r = 0; r < n; ++r) {
         oracle_row(Q, K, V, Hq, Hkv, Sq, Skv, D, scale, causal, input_pos,
-                   rows_bhi[3 * r], rows_bhi[3 * r + 1], rows_bhi[3 * r + 2],
+                   window, rows_bhi[3 * r], rows_bhi[3 * r + 1],
+                   rows_bhi[3 * r + 2],
                    score, prob, O_rows + r * D, &LSE_rows[r]);
       }
     }
@@ -183,9 +209,10 @@ int attn_oracle_rows(const double* Q, const double* K, const double* V,
 /* The softmax weight row p_j / L of one query (b, h, i): prob[0..Skv). */
 int attn_oracle_prob_row(const double* Q, const double* K, const double* V,
                          long B, long Hq, long Hkv, long Sq, long Skv, long D,
-                         double scale, int causal, long input_pos, long b,
-                         long h, long i, double* prob) {
-  if (!check_shape(B, Hq, Hkv, Sq, Skv, D, input_pos)) return ORACLE_BAD_ARG;
+                         double scale, int causal, long input_pos,
+                         long window, long b, long h, long i, double* prob) {
+  if (!check_shape(B, Hq, Hkv, Sq, Skv, D, causal, input_pos, window))
+    return ORACLE_BAD_ARG;
   if (b < 0 || b >= B || h < 0 || h >= Hq || i < 0 || i >= Sq)
     return ORACLE_BAD_ARG;
   double* score = (double*)malloc(sizeof(double) * (size_t)Skv);
@@ -196,8 +223,8 @@ int attn_oracle_prob_row(const double* Q, const double* K, const double* V,
     return ORACLE_NO_MEMORY;
   }
   double lse;
-  oracle_row(Q, K, V, Hq, Hkv, Sq, Skv, D, scale, causal, input_pos, b, h, i,
-             score, prob, out, &lse);
+  oracle_row(Q, K, V, Hq, Hkv, Sq, Skv, D, scale, causal, input_pos, window,
+             b, h, i, score, prob, out, &lse);
   free(score);
   free(out);
   return ORACLE_OK;

@@ -239,9 +239,90 @@ def pin_torch_sdpa(orc):
                                    rtol=0, atol=1e-12)
 
 
+def pin_window_single_key(orc):
+    """Window W = 1: each query sees only its own position, so O = V at that
+    position and LSE = scale * q . k there (a one-term softmax)."""
+    rng = np.random.default_rng(21)
+    B, Hq, Hkv, Sq, Skv, D, pos = 2, 4, 2, 5, 12, 8, 6
+    q = _rand((B, Hq, Sq, D), rng)
+    k = _rand((B, Hkv, Skv, D), rng)
+    v = _rand((B, Hkv, Skv, D), rng)
+    o, lse = orc.attention(q, k, v, 0.4, True, pos, window=1)
+    for b in range(B):
+        for h in range(Hq):
+            kvh = h // (Hq // Hkv)
+            for i in range(Sq):
+                j = min(pos + i, Skv - 1)
+                if pos + i > Skv - 1:
+                    continue
+                np.testing.assert_allclose(o[b, h, i], v[b, kvh, j],
+                                           rtol=0, atol=1e-12)
+                np.testing.assert_allclose(
+                    lse[b, h, i], 0.4 * float(q[b, h, i] @ k[b, kvh, j]),
+                    rtol=0, atol=1e-12)
+
+
+def pin_window_uniform_scores(orc):
+    """scale = 0 with a window: O is the mean of V over the window's keys
+    (positions pos-W+1 .. pos, clipped to the cache) and LSE = ln(count)."""
+    rng = np.random.default_rng(22)
+    B, Hq, Hkv, Sq, Skv, D = 1, 2, 1, 6, 20, 4
+    q = _rand((B, Hq, Sq, D), rng)
+    k = _rand((B, Hkv, Skv, D), rng)
+    v = _rand((B, Hkv, Skv, D), rng)
+    for pos, W in ((0, 3), (4, 5), (13, 2), (10, 30)):
+        o, lse = orc.attention(q, k, v, 0.0, True, pos, window=W)
+        for i in range(Sq):
+            lo, hi = max(0, pos + i - W + 1), min(pos + i, Skv - 1)
+            np.testing.assert_allclose(o[0, :, i],
+                                       np.broadcast_to(v[0, 0, lo:hi + 1]
+                                                       .mean(axis=0), (Hq, D)),
+                                       rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lse[0, :, i], math.log(hi - lo + 1),
+                                       rtol=0, atol=1e-12)
+
+
+def pin_window_wide_is_causal(orc):
+    """A window at least as long as every query's prefix changes nothing."""
+    rng = np.random.default_rng(23)
+    q = _rand((1, 2, 7, 8), rng)
+    k = _rand((1, 2, 15, 8), rng)
+    v = _rand((1, 2, 15, 8), rng)
+    o, lse = orc.attention(q, k, v, 0.5, True, 3)
+    for W in (10, 11, 40):
+        ow, lw = orc.attention(q, k, v, 0.5, True, 3, window=W)
+        np.testing.assert_array_equal(ow, o)
+        np.testing.assert_array_equal(lw, lse)
+
+
+def pin_window_decode_slice(orc):
+    """Library pin: one query at position pos with window W equals torch's
+    float64 softmax attention (no mask) over the contiguous key slice
+    [pos-W+1, pos] -- the window as a slice of the cache, not a predicate."""
+    F = torch.nn.functional
+    rng = np.random.default_rng(24)
+    B, Hq, Hkv, Skv, D = 2, 4, 2, 40, 16
+    k = _rand((B, Hkv, Skv, D), rng)
+    v = _rand((B, Hkv, Skv, D), rng)
+    for pos, W in ((39, 7), (25, 1), (30, 31), (12, 5)):
+        q = _rand((B, Hq, 1, D), rng)
+        o, lse = orc.attention(q, k, v, 0.3, True, pos, window=W)
+        lo = max(0, pos - W + 1)
+        g = Hq // Hkv
+        tq = torch.from_numpy(q)
+        tk = torch.from_numpy(k[:, :, lo:pos + 1]).repeat_interleave(g, dim=1)
+        tv = torch.from_numpy(v[:, :, lo:pos + 1]).repeat_interleave(g, dim=1)
+        ref = F.scaled_dot_product_attention(tq, tk, tv, scale=0.3)
+        np.testing.assert_allclose(o, ref.numpy(), rtol=0, atol=1e-12)
+        s = torch.matmul(tq, tk.transpose(-1, -2)) * 0.3
+        np.testing.assert_allclose(lse, torch.logsumexp(s, dim=-1).numpy(),
+                                   rtol=0, atol=1e-12)
+
+
 ALL_PINS = [
     pin_hand_cases, pin_single_key, pin_uniform_scores, pin_prob_rows,
     pin_gqa_equivalence, pin_causal_first_row, pin_permutation_invariance,
     pin_causal_prefix, pin_shift_invariance, pin_negated_scale,
-    pin_torch_sdpa,
+    pin_torch_sdpa, pin_window_single_key, pin_window_uniform_scores,
+    pin_window_wide_is_causal, pin_window_decode_slice,
 ]

@@ -33,6 +33,12 @@ MUTANTS = {
                              "if (score[j] > M)"),
     "wrong_query_row": ("(b * Hq + h) * Sq + i) * D",
                         "(b * Hq + h) * Sq + 0) * D"),
+    "window_off_by_one": ("j > input_pos + i - window",
+                          "j >= input_pos + i - window"),
+    "window_ignored": ("return window <= 0 || j > input_pos + i - window;",
+                       "return 1;"),
+    "window_without_offset": ("j > input_pos + i - window",
+                              "j > i - window"),
 }
 
 

@@ -33,6 +33,16 @@ def test_rejects_bad_shapes():
         oracle.attention(q, k, k, 1.0)          # Hq % Hkv != 0
     with pytest.raises(ValueError):
         oracle.attention(np.zeros((1, 2, 2, 4)), k, k, 1.0, True, -1)
+    q2 = np.zeros((1, 2, 2, 4))
+    with pytest.raises(ValueError):
+        oracle.attention(q2, k, k, 1.0, False, 0, window=2)  # window: causal only
+    with pytest.raises(ValueError):
+        oracle.attention(q2, k, k, 1.0, True, 0, window=-1)
+    with pytest.raises(ValueError):
+        # keys 0..1; the last query (position 2) with window 1 sees only key 2
+        oracle.attention(q2, k, k, 1.0, True, 1, window=1)
+    oracle.attention(q2, k, k, 1.0, True, 0, window=1)  # positions 0, 1: fine
+
 
 
 def test_threads_positive():
