@@ -15,7 +15,8 @@ import os
 import threading
 
 __all__ = [
-    "ATTN_F16", "ATTN_BF16", "AttnError", "attn_fwd", "attn_fwd_splitkv",
+    "ATTN_F16", "ATTN_BF16", "AttnError", "attn_fwd", "attn_fwd_window",
+    "attn_fwd_splitkv", "attn_fwd_splitkv_window",
     "attn_splitkv_plan", "attn_fwd_splitkv_noalloc",
     "attn_noalloc_scratch_bytes", "attn_status_string", "attn_device_status",
     "attn_tile_config", "attn_version", "fwd", "fwd_splitkv",
@@ -66,6 +67,9 @@ def load_library():
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i,
                                  ctypes.c_float, i, i, i, vp]
         lib.attn_fwd.restype = i
+        lib.attn_fwd_window.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i,
+                                        ctypes.c_float, i, i, i, i, vp]
+        lib.attn_fwd_window.restype = i
         lib.attn_status_string.argtypes = [i]
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
@@ -80,6 +84,10 @@ def load_library():
                                          ctypes.c_float, i, i, i, i, vp, sz,
                                          vp]
         lib.attn_fwd_splitkv.restype = i
+        lib.attn_fwd_splitkv_window.argtypes = [vp, vp, vp, vp, vp, i, i, i,
+                                                i, i, i, ctypes.c_float, i, i,
+                                                i, i, i, vp, sz, vp]
+        lib.attn_fwd_splitkv_window.restype = i
         lib.attn_splitkv_plan.argtypes = [i, i, i, i, i, i, i, i, i, ip,
                                           ctypes.POINTER(sz)]
         lib.attn_splitkv_plan.restype = i
@@ -99,6 +107,26 @@ def attn_fwd(Q, K, V, O, LSE, B, Hq, Hkv, Sq, Skv, D, scale, causal,
     return int(load_library().attn_fwd(
         Q or None, K or None, V or None, O or None, LSE or None, B, Hq, Hkv,
         Sq, Skv, D, float(scale), int(causal), int(input_pos), int(dtype),
+        stream or None))
+
+
+def attn_fwd_window(Q, K, V, O, LSE, B, Hq, Hkv, Sq, Skv, D, scale, causal,
+                    input_pos, window, dtype, stream) -> int:
+    """Raw C-ABI call with a causal sliding window of ``window`` keys."""
+    return int(load_library().attn_fwd_window(
+        Q or None, K or None, V or None, O or None, LSE or None, B, Hq, Hkv,
+        Sq, Skv, D, float(scale), int(causal), int(input_pos), int(window),
+        int(dtype), stream or None))
+
+
+def attn_fwd_splitkv_window(Q, K, V, O, LSE, B, Hq, Hkv, Sq, Skv, D, scale,
+                            causal, input_pos, window, dtype, num_splits,
+                            workspace, workspace_bytes, stream) -> int:
+    """Raw C-ABI call of the split-KV forward with a sliding window."""
+    return int(load_library().attn_fwd_splitkv_window(
+        Q or None, K or None, V or None, O or None, LSE or None, B, Hq, Hkv,
+        Sq, Skv, D, float(scale), int(causal), int(input_pos), int(window),
+        int(dtype), int(num_splits), workspace or None, int(workspace_bytes),
         stream or None))
 
 
@@ -180,13 +208,15 @@ def _dtype_code(t):
 
 
 def fwd(q, k, v, scale=None, causal=True, input_pos=0, out=None, lse=None,
-        need_lse=True, stream=None):
+        need_lse=True, stream=None, window=0):
     """Attention forward on CUDA tensors.
 
     q [B, Hq, Sq, D], k and v [B, Hkv, Skv, D] (contiguous, same dtype,
     float16 or bfloat16).  ``scale`` defaults to 1/sqrt(D).  Returns
     (O, LSE) with LSE float32 [B, Hq, Sq] (None if ``need_lse`` is False).
-    The kernel is enqueued on ``stream`` (default: torch's current stream).
+    ``window`` > 0 (causal only): the query at position p sees keys
+    p - window + 1 .. p.  The kernel is enqueued on ``stream`` (default:
+    torch's current stream).
     """
     import torch
     for name, t in (("q", q), ("k", k), ("v", v)):
@@ -215,10 +245,16 @@ def fwd(q, k, v, scale=None, causal=True, input_pos=0, out=None, lse=None,
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     with torch.cuda.device(q.device):
-        st = attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                      out.data_ptr(), lse.data_ptr() if need_lse else 0,
-                      B, Hq, Hkv, Sq, Skv, D, scale, causal, input_pos, dt,
-                      stream.cuda_stream)
+        if window:
+            st = attn_fwd_window(
+                q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                lse.data_ptr() if need_lse else 0, B, Hq, Hkv, Sq, Skv, D,
+                scale, causal, input_pos, window, dt, stream.cuda_stream)
+        else:
+            st = attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                          out.data_ptr(), lse.data_ptr() if need_lse else 0,
+                          B, Hq, Hkv, Sq, Skv, D, scale, causal, input_pos, dt,
+                          stream.cuda_stream)
     if st != ATTN_OK:
         raise AttnError("attn_fwd: " + attn_status_string(st), st)
     return out, (lse if need_lse else None)
@@ -226,12 +262,13 @@ def fwd(q, k, v, scale=None, causal=True, input_pos=0, out=None, lse=None,
 
 def fwd_splitkv(q, k, v, scale=None, causal=True, input_pos=0, num_splits=0,
                 workspace=None, out=None, lse=None, need_lse=True,
-                stream=None):
+                stream=None, window=0):
     """Split-KV attention forward (few query rows over a long key range).
 
-    Same tensors and result as ``fwd``.  ``num_splits`` <= 0 lets the
-    library choose; ``workspace`` (a CUDA tensor of at least the planned
-    size, 256-byte aligned) is allocated with torch when not given.
+    Same tensors and result as ``fwd`` (``window`` included).
+    ``num_splits`` <= 0 lets the library choose; ``workspace`` (a CUDA
+    tensor of at least the planned size, 256-byte aligned) is allocated
+    with torch when not given.
     """
     import torch
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
@@ -259,11 +296,19 @@ def fwd_splitkv(q, k, v, scale=None, causal=True, input_pos=0, num_splits=0,
                               device=q.device)
         if stream is None:
             stream = torch.cuda.current_stream(q.device)
-        st = attn_fwd_splitkv(
-            q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-            lse.data_ptr() if need_lse else 0, B, Hq, Hkv, Sq, Skv, D, scale,
-            causal, input_pos, dt, splits, workspace.data_ptr(),
-            workspace.numel() * workspace.element_size(), stream.cuda_stream)
+        ws_args = (splits, workspace.data_ptr(),
+                   workspace.numel() * workspace.element_size(),
+                   stream.cuda_stream)
+        if window:
+            st = attn_fwd_splitkv_window(
+                q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                lse.data_ptr() if need_lse else 0, B, Hq, Hkv, Sq, Skv, D,
+                scale, causal, input_pos, window, dt, *ws_args)
+        else:
+            st = attn_fwd_splitkv(
+                q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                lse.data_ptr() if need_lse else 0, B, Hq, Hkv, Sq, Skv, D,
+                scale, causal, input_pos, dt, *ws_args)
     if st != ATTN_OK:
         raise AttnError("attn_fwd_splitkv: " + attn_status_string(st), st)
     return out, (lse if need_lse else None)

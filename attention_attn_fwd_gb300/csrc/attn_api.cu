@@ -85,6 +85,7 @@ unsigned long long timeout_ns() {
 
 struct Shape {
   int B, Hq, Hkv, Sq, Skv, D, causal, input_pos;
+  int window = 0;  // sliding window in keys (causal only), 0: none
 };
 
 // Tile dispatch.  Few query rows with grouped K/V heads (group * Sq <= 128):
@@ -116,6 +117,13 @@ attn_status_t check_scalars(const Shape& s, float scale, attn_dtype_t dtype) {
     return ATTN_ERR_INVALID_ARG;
   if (s.Hq % s.Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  // A window is defined for causal attention only, and every query row
+  // must see a key: the last row (position input_pos + Sq - 1) sees keys
+  // from input_pos + Sq - window on.
+  if (s.window < 0 || (s.window > 0 && !s.causal)) return ATTN_ERR_INVALID_ARG;
+  if (s.window > 0 && s.Sq > 0 &&
+      static_cast<long long>(s.input_pos) + s.Sq - s.window >= s.Skv)
+    return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   // Row positions of the last (partial) tile must stay within int32.
   if (static_cast<long long>(s.input_pos) + s.Sq + 2 * attn::cfg::kBlockM >
@@ -313,6 +321,7 @@ attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
   p.Skv = s.Skv;
   p.causal = s.causal != 0;
   p.input_pos = s.causal != 0 ? s.input_pos : 0;
+  p.window = s.causal != 0 ? s.window : 0;
   p.num_m_blocks = static_cast<int>(m_blocks(s));
   p.pair_heads = pair_heads(s);
   p.pack_gqa = pack;
@@ -345,6 +354,58 @@ attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
   return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// attn_fwd / attn_fwd_window.
+attn_status_t fwd_impl(const Shape& s, const void* Q, const void* K,
+                       const void* V, void* O, float* LSE, float scale,
+                       attn_dtype_t dtype, attn_stream_t stream) {
+  attn_status_t st = check_scalars(s, scale, dtype);
+  if (st != ATTN_OK) return st;
+  if (s.B == 0 || s.Sq == 0) return ATTN_OK;
+  int dev = 0, sms = 0;
+  unsigned int* status = nullptr;
+  st = check_call(s, scale, dtype, Q, K, V, O, LSE, &dev, &status, &sms);
+  if (st != ATTN_OK) return st;
+  const int tiles = (s.Skv + attn::cfg::kTN - 1) / attn::cfg::kTN;
+  return launch_forward(s, Q, K, V, O, LSE, scale, dtype, status, sms, 1,
+                        tiles, nullptr, nullptr, nullptr,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+// attn_fwd_splitkv / attn_fwd_splitkv_window.
+attn_status_t splitkv_impl(const Shape& s, const void* Q, const void* K,
+                           const void* V, void* O, float* LSE, float scale,
+                           attn_dtype_t dtype, int num_splits, void* workspace,
+                           size_t workspace_bytes, attn_stream_t stream) {
+  attn_status_t st = check_scalars(s, scale, dtype);
+  if (st != ATTN_OK) return st;
+  if (s.B == 0 || s.Sq == 0) return ATTN_OK;
+  if (num_splits < 1 || num_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  unsigned int* status = nullptr;
+  st = check_call(s, scale, dtype, Q, K, V, O, LSE, &dev, &status, &sms);
+  if (st != ATTN_OK) return st;
+  int splits = 0, tiles = 0;
+  splitkv_shape(s, num_splits, sms, &splits, &tiles);
+  if (splits != num_splits) return ATTN_ERR_INVALID_ARG;  // not a planned count
+  if (workspace == nullptr ||
+      reinterpret_cast<uintptr_t>(workspace) % kWorkspaceAlign != 0)
+    return ATTN_ERR_ALIGNMENT;
+  if (workspace_bytes < splitkv_bytes(s, splits)) return ATTN_ERR_INVALID_ARG;
+  if (!is_device_ptr(workspace, dev)) return ATTN_ERR_INVALID_ARG;
+  const size_t rows = static_cast<size_t>(s.B) * s.Hq * s.Sq;
+  const size_t o_bytes =
+      round_up(static_cast<size_t>(splits) * rows * s.D * 4, kWorkspaceAlign);
+  const size_t lse_bytes =
+      round_up(static_cast<size_t>(splits) * rows * 4, kWorkspaceAlign);
+  char* ws = static_cast<char*>(workspace);
+  // One launch: the forward kernel also merges the key ranges.
+  return launch_forward(
+      s, Q, K, V, O, LSE, scale, dtype, status, sms, splits, tiles,
+      reinterpret_cast<float*>(ws), reinterpret_cast<float*>(ws + o_bytes),
+      reinterpret_cast<unsigned long long*>(ws + o_bytes + lse_bytes),
+      reinterpret_cast<cudaStream_t>(stream));
+}
+
 }  // namespace
 
 extern "C" {
@@ -354,17 +415,16 @@ attn_status_t attn_fwd(const void* Q, const void* K, const void* V, void* O,
                        int D, float scale, int causal, int input_pos,
                        attn_dtype_t dtype, attn_stream_t stream) {
   const Shape s{B, Hq, Hkv, Sq, Skv, D, causal != 0, input_pos};
-  attn_status_t st = check_scalars(s, scale, dtype);
-  if (st != ATTN_OK) return st;
-  if (B == 0 || Sq == 0) return ATTN_OK;
-  int dev = 0, sms = 0;
-  unsigned int* status = nullptr;
-  st = check_call(s, scale, dtype, Q, K, V, O, LSE, &dev, &status, &sms);
-  if (st != ATTN_OK) return st;
-  const int tiles = (Skv + attn::cfg::kTN - 1) / attn::cfg::kTN;
-  return launch_forward(s, Q, K, V, O, LSE, scale, dtype, status, sms, 1,
-                        tiles, nullptr, nullptr, nullptr,
-                        reinterpret_cast<cudaStream_t>(stream));
+  return fwd_impl(s, Q, K, V, O, LSE, scale, dtype, stream);
+}
+
+attn_status_t attn_fwd_window(const void* Q, const void* K, const void* V,
+                              void* O, float* LSE, int B, int Hq, int Hkv,
+                              int Sq, int Skv, int D, float scale, int causal,
+                              int input_pos, int window, attn_dtype_t dtype,
+                              attn_stream_t stream) {
+  const Shape s{B, Hq, Hkv, Sq, Skv, D, causal != 0, input_pos, window};
+  return fwd_impl(s, Q, K, V, O, LSE, scale, dtype, stream);
 }
 
 attn_status_t attn_splitkv_plan(int B, int Hq, int Hkv, int Sq, int Skv, int D,
@@ -395,34 +455,21 @@ attn_status_t attn_fwd_splitkv(const void* Q, const void* K, const void* V,
                                int num_splits, void* workspace,
                                size_t workspace_bytes, attn_stream_t stream) {
   const Shape s{B, Hq, Hkv, Sq, Skv, D, causal != 0, input_pos};
-  attn_status_t st = check_scalars(s, scale, dtype);
-  if (st != ATTN_OK) return st;
-  if (B == 0 || Sq == 0) return ATTN_OK;
-  if (num_splits < 1 || num_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
-  int dev = 0, sms = 0;
-  unsigned int* status = nullptr;
-  st = check_call(s, scale, dtype, Q, K, V, O, LSE, &dev, &status, &sms);
-  if (st != ATTN_OK) return st;
-  int splits = 0, tiles = 0;
-  splitkv_shape(s, num_splits, sms, &splits, &tiles);
-  if (splits != num_splits) return ATTN_ERR_INVALID_ARG;  // not a planned count
-  if (workspace == nullptr ||
-      reinterpret_cast<uintptr_t>(workspace) % kWorkspaceAlign != 0)
-    return ATTN_ERR_ALIGNMENT;
-  if (workspace_bytes < splitkv_bytes(s, splits)) return ATTN_ERR_INVALID_ARG;
-  if (!is_device_ptr(workspace, dev)) return ATTN_ERR_INVALID_ARG;
-  const size_t rows = static_cast<size_t>(B) * Hq * Sq;
-  const size_t o_bytes =
-      round_up(static_cast<size_t>(splits) * rows * D * 4, kWorkspaceAlign);
-  const size_t lse_bytes =
-      round_up(static_cast<size_t>(splits) * rows * 4, kWorkspaceAlign);
-  char* ws = static_cast<char*>(workspace);
-  // One launch: the forward kernel also merges the key ranges.
-  return launch_forward(
-      s, Q, K, V, O, LSE, scale, dtype, status, sms, splits, tiles,
-      reinterpret_cast<float*>(ws), reinterpret_cast<float*>(ws + o_bytes),
-      reinterpret_cast<unsigned long long*>(ws + o_bytes + lse_bytes),
-      reinterpret_cast<cudaStream_t>(stream));
+  return splitkv_impl(s, Q, K, V, O, LSE, scale, dtype, num_splits,
+                      workspace, workspace_bytes, stream);
+}
+
+attn_status_t attn_fwd_splitkv_window(const void* Q, const void* K,
+                                      const void* V, void* O, float* LSE,
+                                      int B, int Hq, int Hkv, int Sq, int Skv,
+                                      int D, float scale, int causal,
+                                      int input_pos, int window,
+                                      attn_dtype_t dtype, int num_splits,
+                                      void* workspace, size_t workspace_bytes,
+                                      attn_stream_t stream) {
+  const Shape s{B, Hq, Hkv, Sq, Skv, D, causal != 0, input_pos, window};
+  return splitkv_impl(s, Q, K, V, O, LSE, scale, dtype, num_splits,
+                      workspace, workspace_bytes, stream);
 }
 
 const char* attn_status_string(attn_status_t status) {

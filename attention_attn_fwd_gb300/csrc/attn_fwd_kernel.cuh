@@ -43,6 +43,7 @@ struct FwdParams {
   int B, Hq, Hkv, Sq, Skv;
   int causal;
   int input_pos;
+  int window;              // sliding window in keys (causal only), 0: none
   int num_m_blocks;        // m-blocks per head (of 128 or 256 rows)
   int pair_heads;          // a unit = 2 heads x 128 rows (else 1 head x 256)
   // GQA packing (few query rows): one Q tile holds the Sq rows of all
@@ -113,21 +114,31 @@ struct Layout {
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 };
 
-// K/V tiles [kt0, kt0 + n) of the key range [kt0, kt1) are visited by the
-// 128-row Q tile starting at m0; tiles with index >= ms need the mask.
-__device__ __forceinline__ void tile_extent(const FwdParams& p, int m0,
-                                            int kt0, int kt1, int& n,
-                                            int& ms) {
-  n = 0;
-  ms = 0;
-  if (m0 >= p.Sq) return;
-  const int rows_end = min(m0 + cfg::kTM, p.Sq);
-  const int kend = p.causal ? min(p.input_pos + rows_end, p.Skv) : p.Skv;
-  const int t_end = min((kend + cfg::kTN - 1) / cfg::kTN, kt1);
-  n = max(0, t_end - kt0);
+// Key tiles of the Q tile whose first row is m0 (packed: the tile holding
+// the Sq rows of every head of a GQA group, m0 = 0): tiles [lo, hi) hold
+// every key its rows can see; tiles >= ms need the causal / key-tail mask
+// and tiles < wl the sliding-window mask.  hi == 0: the tile has no rows.
+struct TileKeys {
+  int lo, hi, ms, wl;
+};
+
+template <bool kWindow>
+__device__ __forceinline__ TileKeys tile_keys(const FwdParams& p, int m0) {
+  TileKeys k{0, 0, 0, 0};
+  if (m0 >= p.Sq) return k;
+  // Absolute positions of the tile's first and last valid rows.
+  const int pos_first = p.input_pos + m0;
+  const int pos_last = p.input_pos + min(m0 + cfg::kTM, p.Sq) - 1;
+  const int kend = p.causal ? min(pos_last + 1, p.Skv) : p.Skv;
+  k.hi = (kend + cfg::kTN - 1) / cfg::kTN;
   const int full_tiles = p.Skv / cfg::kTN;
-  ms = p.causal ? min((p.input_pos + m0 + 1) / cfg::kTN, full_tiles)
-                : full_tiles;
+  k.ms = p.causal ? min((pos_first + 1) / cfg::kTN, full_tiles) : full_tiles;
+  if constexpr (kWindow) {
+    // Row at position r sees keys r - window + 1 .. r.
+    k.lo = max(0, pos_first - p.window + 1) / cfg::kTN;
+    k.wl = (max(0, pos_last - p.window + 1) + cfg::kTN - 1) / cfg::kTN;
+  }
+  return k;
 }
 
 // Bounded wait.  Returns false if the CTA is aborting or the wait ran out.
@@ -167,23 +178,28 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity,
 // block order); consecutive units are consecutive heads, so the heads of a
 // K/V group run together and find K/V in L2.
 struct Unit {
-  int kt0;       // first K/V tile of the unit's key range
+  int kb;        // first K/V tile the unit streams (tile j of the unit is
+                 // key tile kb + j)
+  int lo;        // first K/V tile any row of the unit can see (window)
   int split;     // key-range index (0 without split-KV)
   int plane[2];  // [B*Hq] plane of each Q tile
   int m0[2];     // first row of each Q tile
-  int n[2];      // K/V tiles each Q tile visits
-  int ms[2];     // first K/V tile that needs the mask
+  int n[2];      // K/V tiles each Q tile visits (from kb)
+  int hi[2];     // end of the key tiles each Q tile can see
+  int ms[2];     // first K/V tile that needs the causal / tail mask
+  int wl[2];     // K/V tiles below wl need the window mask
   int kv_plane;  // [B*Hkv] plane of the shared K/V head
   int n_kv;      // K/V tiles the unit streams
 };
 
-template <bool kPack>
+template <bool kPack, bool kWindow>
 __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   Unit w;
   w.split = u % p.num_splits;
   u /= p.num_splits;
-  w.kt0 = w.split * p.split_tiles;
-  const int kt1 = w.kt0 + p.split_tiles;
+  const int kt0 = w.split * p.split_tiles;  // key range of the unit
+  const int kt1 = kt0 + p.split_tiles;
+  TileKeys tk[2];
   if constexpr (kPack) {
     // Unit = one (batch, K/V head): tile 0 holds all its query rows.
     const int b = u / p.Hkv;
@@ -192,34 +208,46 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
     w.plane[0] = b * p.Hq + kvh * p.group;  // first head of the group
     w.plane[1] = w.plane[0];
     w.m0[0] = w.m0[1] = 0;
-    tile_extent(p, 0, w.kt0, kt1, w.n[0], w.ms[0]);
-    w.n[1] = 0;
-    w.ms[1] = 0;
-    w.n_kv = w.n[0];
-    return w;
+    tk[0] = tile_keys<kWindow>(p, 0);
+    tk[1] = TileKeys{0, 0, 0, 0};
+  } else {
+    const int per_m = p.pair_heads ? p.B * (p.Hq / 2) : p.B * p.Hq;
+    const int mb = p.num_m_blocks - 1 - u / per_m;
+    const int ub = u % per_m;
+    const int b = p.pair_heads ? ub / (p.Hq / 2) : ub / p.Hq;
+    const int h0 = p.pair_heads ? 2 * (ub % (p.Hq / 2)) : ub % p.Hq;
+    w.kv_plane = b * p.Hkv + h0 / (p.Hq / p.Hkv);
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      w.plane[t] = b * p.Hq + h0 + (p.pair_heads ? t : 0);
+      w.m0[t] = p.pair_heads ? mb * cfg::kTM : mb * cfg::kBlockM + t * cfg::kTM;
+      tk[t] = tile_keys<kWindow>(p, w.m0[t]);
+    }
   }
-  const int per_m = p.pair_heads ? p.B * (p.Hq / 2) : p.B * p.Hq;
-  const int mb = p.num_m_blocks - 1 - u / per_m;
-  const int ub = u % per_m;
-  const int b = p.pair_heads ? ub / (p.Hq / 2) : ub / p.Hq;
-  const int h0 = p.pair_heads ? 2 * (ub % (p.Hq / 2)) : ub % p.Hq;
-  w.kv_plane = b * p.Hkv + h0 / (p.Hq / p.Hkv);
+  // Both tiles share one K/V stream, from the first tile any of the unit's
+  // rows can see (tile 0 holds the earliest rows); with a window, tile 1's
+  // first tiles may then be fully masked for it.
+  w.lo = tk[0].lo;
+  w.kb = max(kt0, w.lo);
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
-    w.plane[t] = b * p.Hq + h0 + (p.pair_heads ? t : 0);
-    w.m0[t] = p.pair_heads ? mb * cfg::kTM : mb * cfg::kBlockM + t * cfg::kTM;
-    tile_extent(p, w.m0[t], w.kt0, kt1, w.n[t], w.ms[t]);
+    w.hi[t] = tk[t].hi;
+    w.ms[t] = tk[t].ms;
+    w.wl[t] = tk[t].wl;
+    w.n[t] = max(0, min(tk[t].hi, kt1) - w.kb);
   }
   w.n_kv = max(w.n[0], w.n[1]);
   return w;
 }
 
-// Number of key ranges (split-KV) that reach the 128-row Q tile at m0:
-// ranges starting past the tile's causal horizon are never visited.
-__device__ __forceinline__ int ranges_visited(const FwdParams& p, int m0) {
-  int n, ms;
-  tile_extent(p, m0, 0, 1 << 30, n, ms);
-  return min(p.num_splits, (n + p.split_tiles - 1) / p.split_tiles);
+// Number of key ranges (split-KV) that reach Q tile t of unit w: ranges
+// before the unit's window or past the tile's causal horizon are never
+// visited.
+__device__ __forceinline__ int ranges_visited(const FwdParams& p,
+                                              const Unit& w, int t) {
+  const int hi = t ? w.hi[1] : w.hi[0];
+  return min(p.num_splits, (hi + p.split_tiles - 1) / p.split_tiles) -
+         w.lo / p.split_tiles;
 }
 
 // Counts this unit's arrival on a tile's merge counter; true for the
@@ -257,10 +285,10 @@ __device__ __forceinline__ bool merge_arrive(unsigned long long* ctr,
 // output O_c and log-sum-exp lse_c; with M = max_c lse_c and
 // w_c = e^(lse_c - M),  O = sum_c w_c O_c / sum_c w_c  and
 // LSE = M + ln(sum_c w_c) -- the online-softmax rescale applied once more,
-// across ranges.  Ranges past a row's causal horizon hold nothing for it
-// and are not read.  Thread tid takes 4 columns of one row, so the 32 (or
+// across ranges.  Ranges past a row's causal horizon or before its window
+// hold nothing for it and are not read.  Thread tid takes 4 columns of one row, so the 32 (or
 // 16) threads of a row read its partials as contiguous 512 (256) bytes.
-template <int D, bool kBF16, bool kPack>
+template <int D, bool kBF16, bool kPack, bool kWindow>
 __device__ __forceinline__ void merge_tile(const FwdParams& p, int plane0,
                                            int m0, int tid) {
   constexpr float kLog2e = 1.4426950408889634f;
@@ -278,16 +306,18 @@ __device__ __forceinline__ void merge_tile(const FwdParams& p, int plane0,
       q_row = r % p.Sq;
     }
     const long long row = static_cast<long long>(q_plane) * p.Sq + q_row;
-    const int vis_end =
-        p.causal ? min(p.Skv, p.input_pos + q_row + 1) : p.Skv;
+    const int row_pos = p.input_pos + q_row;
+    const int vis_end = p.causal ? min(p.Skv, row_pos + 1) : p.Skv;
     const int ns = min(p.num_splits, (vis_end + split_keys - 1) / split_keys);
+    const int c0 =
+        kWindow ? max(0, row_pos - p.window + 1) / split_keys : 0;
     float mx = -INFINITY;
-    for (int c = 0; c < ns; ++c)
+    for (int c = c0; c < ns; ++c)
       mx = fmaxf(mx, __ldcg(p.lse_part + c * rows + row));
     float wsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-    for (int c = 0; c < ns; ++c) {
+    for (int c = c0; c < ns; ++c) {
       const float wc =
           ptx::ex2((__ldcg(p.lse_part + c * rows + row) - mx) * kLog2e);
       const float4 x = __ldcg(
@@ -325,7 +355,11 @@ __device__ __forceinline__ int unit_index(int k, int cta, int ctas) {
 // kSplit: split-KV launch (o_part set) -- compiles the in-kernel merge of
 // the per-range partial results; the partial writes themselves follow
 // o_part at run time.
-template <int D, bool kBF16, bool kPack, bool kSplit>
+// kWindow: causal sliding window (window > 0) -- compiles the lower mask.
+// The variants keep each launch's softmax loop free of the others' code:
+// in one kernel with run-time switches the two-tile loop ran out of
+// registers and lost 5-11 %.
+template <int D, bool kBF16, bool kPack, bool kSplit, bool kWindow>
 __global__ void __launch_bounds__(cfg::kThreads, 1)
     attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
@@ -397,7 +431,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
     for (int k = 0; k * u_step < p.num_units && ok; ++k) {
       const int u = unit_index(k, u_first, u_step);
       if (u >= p.num_units) continue;
-      const Unit w = decode_unit<kPack>(p, u);
+      const Unit w = decode_unit<kPack, kWindow>(p, u);
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (w.n[t] == 0 || !ok) continue;
@@ -430,7 +464,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
           for (int c = 0; c < L::kChunks; ++c)
             ptx::tma_load_3d_elect(dst + c * L::kBoxBytes, kv ? &tm_v : &tm_k,
                                    bar_full + 8 * slot, c * 64,
-                                   (w.kt0 + j) * kTN, w.kv_plane);
+                                   (w.kb + j) * kTN, w.kv_plane);
           ++it;
         }
       }
@@ -494,7 +528,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
     for (int k = 0; k * u_step < p.num_units && ok; ++k) {
       const int u = unit_index(k, u_first, u_step);
       if (u >= p.num_units) continue;
-      const Unit w = decode_unit<kPack>(p, u);
+      const Unit w = decode_unit<kPack, kWindow>(p, u);
       // A key range wholly past the causal horizon of both tiles has no
       // work (split-KV only); the producer and softmax warps skip it too.
       if (w.n_kv == 0) continue;
@@ -652,10 +686,11 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
     for (int k = 0; k * u_step < p.num_units && ok; ++k) {
       const int u = unit_index(k, u_first, u_step);
       if (u >= p.num_units) continue;
-      const Unit w = decode_unit<kPack>(p, u);
+      const Unit w = decode_unit<kPack, kWindow>(p, u);
       const int n = t ? w.n[1] : w.n[0];
       if (n == 0) continue;
       const int ms = t ? w.ms[1] : w.ms[0];
+      const int wl = kWindow ? (t ? w.wl[1] : w.wl[0]) : 0;
       const int m0 = t ? w.m0[1] : w.m0[0];
       // This thread's query row: head plane and row index within the head.
       int q_plane = t ? w.plane[1] : w.plane[0];
@@ -689,15 +724,30 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
         }
 
         // Pass 1: row maximum of the scaled scores over the visible keys.
-        // Visible keys of this row in the tile are the columns < lim: key <
-        // Skv, and key <= row_pos when causal (only tiles >= ms can cut).
-        const bool masked = w.kt0 + j >= ms;
-        int lim = kTN;
+        // Visible keys of this row in the tile are the columns c with
+        // lo <= c < lim: key < Skv, key <= row_pos when causal (only tiles
+        // >= ms can cut), key > row_pos - window with a window (only tiles
+        // < wl can cut; lo stays 0 without one).
+        const int kt = w.kb + j;  // key tile index
+        const bool masked = kt >= ms || (kWindow && kt < wl);
+        int lim = kTN, lo = 0, span = kTN;
         if (masked) {
-          const int kbase = (w.kt0 + j) * kTN;
+          const int kbase = kt * kTN;
           lim = min(kTN, p.Skv - kbase);
           if (p.causal) lim = min(lim, row_pos - kbase + 1);
+          if constexpr (kWindow) {
+            lo = row_pos - p.window + 1 - kbase;
+            span = max(lim - lo, 0);
+          }
         }
+        // One unsigned compare tests both ends of [lo, lo + span); in a
+        // same-box A/B it ran the window workload 11 % faster than two
+        // signed compares.
+        auto hidden = [&](int c) {
+          if constexpr (kWindow)
+            return static_cast<unsigned>(c - lo) >= static_cast<unsigned>(span);
+          return c >= lim;
+        };
         float mx;
         {
           uint32_t sr[kTN];
@@ -708,7 +758,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
           if (masked) {
 #pragma unroll
             for (int q = 0; q < kTN; ++q)
-              if (q >= lim) sr[q] = __float_as_uint(-INFINITY);
+              if (hidden(q)) sr[q] = __float_as_uint(-INFINITY);
           }
           // Four independent chains of 3-input max.
           float mc[4];
@@ -765,8 +815,8 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
               ptx::ffma2(x0, x1, __uint_as_float(cur[2 * e]),
                          __uint_as_float(cur[2 * e + 1]), c, neg_m);
               if (masked) {
-                if (32 * q + 2 * e >= lim) x0 = -INFINITY;
-                if (32 * q + 2 * e + 1 >= lim) x1 = -INFINITY;
+                if (hidden(32 * q + 2 * e)) x0 = -INFINITY;
+                if (hidden(32 * q + 2 * e + 1)) x1 = -INFINITY;
               }
               const float p0 = ptx::ex2(x0);
               const float p1 = ptx::ex2(x1);
@@ -892,10 +942,11 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
         if (r == 0)
           *merge_flag = merge_arrive(
               p.merge_ctr + 2 * (u / p.num_splits) + t, p.merge_seq,
-              ranges_visited(p, m0), p);
+              ranges_visited(p, w, t), p);
         ptx::named_barrier_sync(1 + t, kTM);
         if (*merge_flag) {
-          merge_tile<D, kBF16, kPack>(p, t ? w.plane[1] : w.plane[0], m0, r);
+          merge_tile<D, kBF16, kPack, kWindow>(p, t ? w.plane[1] : w.plane[0],
+                                               m0, r);
         }
       }
       ptx::tc_fence_before();

@@ -9,11 +9,11 @@ namespace attn {
 // library) keeps its own "attribute set" flag per kernel.
 namespace {
 
-template <int D, bool kBF16, bool kPack, bool kSplit>
+template <int D, bool kBF16, bool kPack, bool kSplit, bool kWindow>
 cudaError_t launch_variant(const CUtensorMap& q, const CUtensorMap& k,
                            const CUtensorMap& v, const FwdParams& p, int grid,
                            cudaStream_t stream) {
-  auto kernel = attn_fwd_sm103_kernel<D, kBF16, kPack, kSplit>;
+  auto kernel = attn_fwd_sm103_kernel<D, kBF16, kPack, kSplit, kWindow>;
   const int smem = Layout<D, kPack>::kSmemBytes;
   // The attribute is per device; setting it again is cheap and idempotent.
   static thread_local int configured_device = -1;
@@ -35,17 +35,34 @@ cudaError_t launch_variant(const CUtensorMap& q, const CUtensorMap& k,
   return cudaLaunchKernelEx(&cfg, kernel, q, k, v, p);
 }
 
-// Dtype and split-KV dispatch of one (D, tile mode) variant; split-KV when
-// the parameters carry partial-result buffers.
+// Dtype, split-KV and window dispatch of one (D, tile mode) variant:
+// split-KV when the parameters carry partial-result buffers, the window
+// variant when a window is set.
+template <int D, bool kPack, bool kSplit, bool kWindow>
+cudaError_t launch_dtype(bool bf16, const CUtensorMap& q, const CUtensorMap& k,
+                         const CUtensorMap& v, const FwdParams& p, int grid,
+                         cudaStream_t stream) {
+  return bf16 ? launch_variant<D, true, kPack, kSplit, kWindow>(q, k, v, p,
+                                                                grid, stream)
+              : launch_variant<D, false, kPack, kSplit, kWindow>(q, k, v, p,
+                                                                 grid, stream);
+}
+
 template <int D, bool kPack>
 cudaError_t launch_mode(bool bf16, const CUtensorMap& q, const CUtensorMap& k,
                         const CUtensorMap& v, const FwdParams& p, int grid,
                         cudaStream_t stream) {
-  if (p.o_part != nullptr)
-    return bf16 ? launch_variant<D, true, kPack, true>(q, k, v, p, grid, stream)
-                : launch_variant<D, false, kPack, true>(q, k, v, p, grid, stream);
-  return bf16 ? launch_variant<D, true, kPack, false>(q, k, v, p, grid, stream)
-              : launch_variant<D, false, kPack, false>(q, k, v, p, grid, stream);
+  const bool split = p.o_part != nullptr;
+  const bool window = p.window > 0;
+  if (split)
+    return window ? launch_dtype<D, kPack, true, true>(bf16, q, k, v, p, grid,
+                                                       stream)
+                  : launch_dtype<D, kPack, true, false>(bf16, q, k, v, p, grid,
+                                                        stream);
+  return window ? launch_dtype<D, kPack, false, true>(bf16, q, k, v, p, grid,
+                                                      stream)
+                : launch_dtype<D, kPack, false, false>(bf16, q, k, v, p, grid,
+                                                       stream);
 }
 
 }  // namespace

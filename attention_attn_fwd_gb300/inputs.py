@@ -23,6 +23,7 @@ class Workload:
     dtype: str          # "f16" or "bf16"
     causal: bool
     input_pos: int = 0
+    window: int = 0     # sliding window in keys (causal only), 0: none
 
     @property
     def scale(self) -> float:
@@ -43,7 +44,9 @@ class Workload:
             return self.B * self.Hq * self.Sq * self.Skv
         total = 0
         for i in range(self.Sq):
-            total += min(self.Skv, self.input_pos + i + 1)
+            pos = self.input_pos + i
+            lo = max(0, pos - self.window + 1) if self.window else 0
+            total += max(0, min(self.Skv, pos + 1) - lo)
         return self.B * self.Hq * total
 
     def exact_flops(self) -> float:
@@ -70,6 +73,11 @@ GQA_8K = Workload("gqa_B1_Hq32_Hkv4_S8192_D128_bf16_causal", 1, 32, 4, 8192,
 PREFILL_CHUNK = Workload("prefill_B8_Hq32_Hkv8_Sq512_pos3584_Skv4096_D128_bf16",
                          8, 32, 8, 512, 4096, 128, "bf16", True, 3584)
 
+
+# GQA 32k causal prefill with a 4096-key sliding window (each query sees its
+# last 4096 positions).
+WINDOW_32K = Workload("window_B1_Hq32_Hkv4_S32768_W4096_D128_bf16", 1, 32, 4,
+                      32768, 32768, 128, "bf16", True, 0, 4096)
 
 # One new token per sequence against a full 4096-key cache (the decode step
 # after the prefill chunk above); the split-KV path's workload.

@@ -475,6 +475,81 @@ def run_decode(args):
         print(json.dumps(out), flush=True)
 
 
+# ------------------------------------------------------- sliding window
+def run_window(args):
+    """Causal GQA 32k prefill with a 4096-key sliding window: tensor-bound,
+    reported in TFLOPS of the exactly visible query-key pairs (4*D FLOPs
+    each; the causal-halved formula does not describe a window) against the
+    measured dense bf16 peak.  L2 flushed between timed steps."""
+    import torch
+
+    import attention_attn_fwd_gb300 as attn
+    from attention_attn_fwd_gb300.inputs import WINDOW_32K, make_qkv
+
+    ws, rank, local = dist_info()
+    if ws > 1:
+        torch.cuda.set_device(local)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = WINDOW_32K
+    q, k, v = (t.to(dev) for t in make_qkv(w, seed=0))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    dt = attn.ATTN_BF16
+
+    def step():
+        st = attn.attn_fwd_window(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+            lse.data_ptr(), w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.scale, 1,
+            w.input_pos, w.window, dt, stream.cuda_stream)
+        if st != attn.ATTN_OK:
+            raise RuntimeError("attn_fwd_window: " +
+                               attn.attn_status_string(st))
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(dev.index) as clocks:
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    st, code = attn.attn_device_status()
+    if st != attn.ATTN_OK:
+        raise RuntimeError("device status %d code %#x" % (st, code))
+    ms = sum(s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)) / args.steps
+    flops = w.exact_flops()
+    tflops = flops / (ms * 1e-3) / 1e12
+    peak, _, src = peaks()
+    out = {
+        "metric": "attention fwd TFLOPS, causal sliding window (exact "
+                  "visible FLOPs)",
+        "value": round(tflops, 1), "unit": "TFLOPS", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic: Q/K/V ~ N(0,1) from a seeded CPU generator",
+        "config": config_dict(w, {
+            "window": w.window,
+            "l2": "flushed between timed steps (256 MiB write, untimed)"}),
+        "roofline": {"bound": "tensor", "achieved": round(tflops, 1),
+                     "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(tflops / peak, 4),
+                     "peak_source": "%s bf16 dense burst (cuBLAS)" % src,
+                     "traffic": None},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -484,10 +559,11 @@ def main():
     ap.add_argument("--cpu-s", type=float, default=15.0,
                     help="CPU-oracle baseline budget in seconds")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["gqa8k", "decode"],
+    ap.add_argument("--workload", choices=["gqa8k", "decode", "window"],
                     default="gqa8k",
                     help="gqa8k: the headline causal GQA forward (default); "
-                         "decode: the split-KV decode step")
+                         "decode: the split-KV decode step; window: causal "
+                         "GQA 32k with a 4096-key sliding window")
     ap.add_argument("--splits", type=int, default=0,
                     help="split count for --workload decode (0: automatic)")
     args = ap.parse_args()
@@ -497,6 +573,8 @@ def main():
         run_reference(args)
     elif args.workload == "decode":
         run_decode(args)
+    elif args.workload == "window":
+        run_window(args)
     else:
         run_ours(args)
 

@@ -81,6 +81,28 @@ attn_status_t attn_fwd(const void* Q, const void* K, const void* V, void* O,
                        attn_dtype_t dtype, attn_stream_t stream);
 
 /*
+ * attn_fwd_window — attn_fwd with a causal sliding window: the query at
+ * absolute position p = input_pos + i sees the keys j with
+ * p - window < j <= p (its last `window` positions, itself included).
+ * "Flash Attention from Scratch", section "What's Next", names sliding
+ * window attention for ultra-long sequences as future work without
+ * defining it; this is the plain reading consistent with the causal offset
+ * rule above.  Key tiles wholly before a query tile's window are skipped
+ * like those past its causal horizon.
+ *
+ * Arguments as attn_fwd, plus:
+ * window   >= 0 keys; 0 means no window (the result of attn_fwd).  A
+ *          window needs causal != 0, and every query must see a key
+ *          (input_pos + Sq - window < Skv); otherwise
+ *          ATTN_ERR_INVALID_ARG.
+ */
+attn_status_t attn_fwd_window(const void* Q, const void* K, const void* V,
+                              void* O, float* LSE, int B, int Hq, int Hkv,
+                              int Sq, int Skv, int D, float scale, int causal,
+                              int input_pos, int window, attn_dtype_t dtype,
+                              attn_stream_t stream);
+
+/*
  * attn_fwd_splitkv — the same operation as attn_fwd, with the key range cut
  * into num_splits pieces of equal length (multiples of 128 keys) that are
  * processed in parallel, then merged by their log-sum-exps: for a row with
@@ -112,6 +134,21 @@ attn_status_t attn_fwd_splitkv(const void* Q, const void* K, const void* V,
                                int input_pos, attn_dtype_t dtype,
                                int num_splits, void* workspace,
                                size_t workspace_bytes, attn_stream_t stream);
+
+/*
+ * attn_fwd_splitkv_window — attn_fwd_splitkv with the sliding window of
+ * attn_fwd_window (same `window` rule).  Plan with attn_splitkv_plan (the
+ * plan does not depend on the window); ranges wholly outside a row
+ * block's window are skipped.
+ */
+attn_status_t attn_fwd_splitkv_window(const void* Q, const void* K,
+                                      const void* V, void* O, float* LSE,
+                                      int B, int Hq, int Hkv, int Sq, int Skv,
+                                      int D, float scale, int causal,
+                                      int input_pos, int window,
+                                      attn_dtype_t dtype, int num_splits,
+                                      void* workspace, size_t workspace_bytes,
+                                      attn_stream_t stream);
 
 /*
  * attn_splitkv_plan — split count and workspace size for attn_fwd_splitkv.

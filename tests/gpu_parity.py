@@ -15,7 +15,7 @@ TOL_LSE = 1e-3
 def run_gpu(w, q, k, v, scale=None):
     scale = w.scale if scale is None else scale
     o, lse = attn.fwd(q.cuda(), k.cuda(), v.cuda(), scale=scale,
-                      causal=w.causal, input_pos=w.input_pos)
+                      causal=w.causal, input_pos=w.input_pos, window=w.window)
     torch.cuda.synchronize()
     st, code = attn.attn_device_status()
     assert st == 0, "device status %d code %#x" % (st, code)
@@ -28,7 +28,8 @@ def check_full(w, seed=0, scale=None, q=None, k=None, v=None):
         q, k, v = make_qkv(w, seed)
     scale = w.scale if scale is None else scale
     o, lse = run_gpu(w, q, k, v, scale)
-    o_ref, lse_ref = oracle.attention(q, k, v, scale, w.causal, w.input_pos)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale, w.causal, w.input_pos,
+                                      w.window)
     o_gpu = o.double().cpu().numpy()
     lse_gpu = lse.double().cpu().numpy()
     assert np.all(np.isfinite(o_gpu)) and np.all(np.isfinite(lse_gpu))
@@ -62,7 +63,7 @@ def check_sampled(w, seed=0, n_rows=192):
     o, lse = run_gpu(w, q, k, v)
     rows = sample_rows(w, n_rows, seed)
     o_ref, lse_ref = oracle.attention_rows(q, k, v, w.scale, w.causal,
-                                           w.input_pos, rows)
+                                           w.input_pos, rows, w.window)
     b, h, i = rows[:, 0], rows[:, 1], rows[:, 2]
     idx = torch.from_numpy(rows).cuda()
     o_rows = o[idx[:, 0], idx[:, 1], idx[:, 2]].double().cpu().numpy()
