@@ -54,6 +54,10 @@ class Oracle:
                                              ctypes.c_double, ctypes.c_int, L,
                                              L, L, L, L, dp]
         lib.attn_oracle_prob_row.restype = ctypes.c_int
+        lib.attn_oracle_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, L, L, L,
+                                        L, L, L, ctypes.c_double,
+                                        ctypes.c_int, L, L]
+        lib.attn_oracle_bwd.restype = ctypes.c_int
         lib.attn_oracle_threads.argtypes = []
         lib.attn_oracle_threads.restype = ctypes.c_int
         self._lib = lib
@@ -106,6 +110,25 @@ class Oracle:
             raise ValueError("oracle rejected the arguments (code %d)" % rc)
         return p
 
+    def backward(self, q, k, v, do, scale, causal=False, input_pos=0,
+                 window=0):
+        """Gradients (dQ, dK, dV) in float64 for upstream gradient ``do``
+        (same shape as the output)."""
+        q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+        B, Hq, Hkv, Sq, Skv, D = _shapes(q, k, v)
+        if do.shape != q.shape:
+            raise ValueError("do must have the shape of q")
+        dq = np.zeros(q.shape, np.float64)
+        dk = np.zeros(k.shape, np.float64)
+        dv = np.zeros(v.shape, np.float64)
+        rc = self._lib.attn_oracle_bwd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
+            B, Hq, Hkv, Sq, Skv, D, float(scale), int(bool(causal)),
+            int(input_pos), int(window))
+        if rc != 0:
+            raise ValueError("oracle rejected the arguments (code %d)" % rc)
+        return dq, dk, dv
+
     def threads(self) -> int:
         """Number of OpenMP threads the oracle's loops use."""
         return int(self._lib.attn_oracle_threads())
@@ -133,6 +156,10 @@ def attention_rows(q, k, v, scale, causal, input_pos, rows, window=0):
 def prob_row(q, k, v, scale, causal, input_pos, b, h, i, window=0):
     return default().prob_row(q, k, v, scale, causal, input_pos, b, h, i,
                               window)
+
+
+def backward(q, k, v, do, scale, causal=False, input_pos=0, window=0):
+    return default().backward(q, k, v, do, scale, causal, input_pos, window)
 
 
 def threads() -> int:

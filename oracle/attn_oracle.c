@@ -230,6 +230,93 @@ int attn_oracle_prob_row(const double* Q, const double* K, const double* V,
   return ORACLE_OK;
 }
 
+/*
+ * Backward pass: gradients of the forward output O with respect to Q, K
+ * and V for an upstream gradient dO ("Flash Attention from Scratch",
+ * section "What's Next", lists the backward pass as future work; no page
+ * gives its formulas, so this is the chain rule applied to the definition
+ * above, in the order the definition computes):
+ *
+ *   O_i   = sum_j P_ij V_j                      =>  dV_j += P_ij dO_i
+ *   dP_ij = dO_i . V_j
+ *   P_ij  = softmax_j(s_ij), s_ij = scale q_i.k_j
+ *                     =>  ds_ij = P_ij (dP_ij - sum_k P_ik dP_ik)
+ *   dQ_i  = scale sum_j ds_ij K_j,   dK_j += scale ds_ij Q_i
+ *
+ * Masked keys have P_ij = 0 and get no gradient.  With grouped K/V heads
+ * the query heads of a group add into the same dK, dV.  Rows are handled
+ * one at a time in double; the parallel loop runs over (b, K/V head) so
+ * that every dK / dV row has one writer.  dQ, dK, dV: same layouts as Q,
+ * K, V.
+ */
+int attn_oracle_bwd(const double* Q, const double* K, const double* V,
+                    const double* dO, double* dQ, double* dK, double* dV,
+                    long B, long Hq, long Hkv, long Sq, long Skv, long D,
+                    double scale, int causal, long input_pos, long window) {
+  if (!check_shape(B, Hq, Hkv, Sq, Skv, D, causal, input_pos, window))
+    return ORACLE_BAD_ARG;
+  const long group = Hq / Hkv;
+  for (long x = 0; x < B * Hkv * Skv * D; ++x) {
+    dK[x] = 0.0;
+    dV[x] = 0.0;
+  }
+  int failed = 0;
+#pragma omp parallel
+  {
+    double* score = (double*)malloc(sizeof(double) * (size_t)Skv);
+    double* prob = (double*)malloc(sizeof(double) * (size_t)Skv);
+    double* dprob = (double*)malloc(sizeof(double) * (size_t)Skv);
+    double* out = (double*)malloc(sizeof(double) * (size_t)D);
+    if (!score || !prob || !dprob || !out) {
+#pragma omp atomic write
+      failed = 1;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (long bk = 0; bk < B * Hkv; ++bk) {
+        const long b = bk / Hkv, kvh = bk % Hkv;
+        const double* k = K + bk * Skv * D;
+        const double* v = V + bk * Skv * D;
+        double* dk = dK + bk * Skv * D;
+        double* dv = dV + bk * Skv * D;
+        for (long h = kvh * group; h < (kvh + 1) * group; ++h) {
+          for (long i = 0; i < Sq; ++i) {
+            const long r = (b * Hq + h) * Sq + i;
+            const double* q = Q + r * D;
+            const double* dout = dO + r * D;
+            double lse;
+            oracle_row(Q, K, V, Hq, Hkv, Sq, Skv, D, scale, causal,
+                       input_pos, window, b, h, i, score, prob, out, &lse);
+            /* dP_ij = dO_i . V_j and the row sum of P_ij dP_ij. */
+            double pdp = 0.0;
+            for (long j = 0; j < Skv; ++j) {
+              double dot = 0.0;
+              for (long d = 0; d < D; ++d) dot += dout[d] * v[j * D + d];
+              dprob[j] = dot;
+              pdp += prob[j] * dot;
+            }
+            double* dq = dQ + r * D;
+            for (long d = 0; d < D; ++d) dq[d] = 0.0;
+            for (long j = 0; j < Skv; ++j) {
+              if (prob[j] == 0.0) continue;
+              const double ds = prob[j] * (dprob[j] - pdp);
+              for (long d = 0; d < D; ++d) {
+                dq[d] += scale * ds * k[j * D + d];
+                dk[j * D + d] += scale * ds * q[d];
+                dv[j * D + d] += prob[j] * dout[d];
+              }
+            }
+          }
+        }
+      }
+    }
+    free(score);
+    free(prob);
+    free(dprob);
+    free(out);
+  }
+  return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
+}
+
 /* Threads the parallel loops will use. */
 int attn_oracle_threads(void) {
 #ifdef _OPENMP

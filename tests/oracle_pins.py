@@ -319,10 +319,90 @@ def pin_window_decode_slice(orc):
                                    rtol=0, atol=1e-12)
 
 
+def _sdpa_grads(q, k, v, do, scale, causal, pos, window):
+    """torch float64 autograd through scaled_dot_product_attention with the
+    visibility written as an explicit boolean mask."""
+    F = torch.nn.functional
+    g = q.shape[1] // k.shape[1]
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    Sq, Skv = q.shape[2], k.shape[2]
+    rows = torch.arange(Sq)[:, None] + pos
+    cols = torch.arange(Skv)[None, :]
+    mask = torch.ones(Sq, Skv, dtype=torch.bool)
+    if causal:
+        mask = cols <= rows
+        if window:
+            mask = mask & (cols > rows - window)
+    o = F.scaled_dot_product_attention(tq, tk.repeat_interleave(g, dim=1),
+                                       tv.repeat_interleave(g, dim=1),
+                                       attn_mask=mask, scale=scale)
+    o.backward(torch.from_numpy(do))
+    return tq.grad.numpy(), tk.grad.numpy(), tv.grad.numpy()
+
+
+def pin_bwd_torch_autograd(orc):
+    """Library pin of the backward: torch autograd in float64 (GQA heads
+    expanded by repeat_interleave, whose gradient sums the group)."""
+    rng = np.random.default_rng(31)
+    for (B, Hq, Hkv, Sq, Skv, D, causal, pos, W) in (
+            (2, 4, 2, 6, 9, 8, False, 0, 0),
+            (1, 2, 2, 7, 7, 4, True, 0, 0),
+            (1, 4, 1, 5, 12, 8, True, 6, 0),
+            (2, 2, 1, 6, 14, 8, True, 5, 4)):
+        q = _rand((B, Hq, Sq, D), rng)
+        k = _rand((B, Hkv, Skv, D), rng)
+        v = _rand((B, Hkv, Skv, D), rng)
+        do = _rand((B, Hq, Sq, D), rng)
+        got = orc.backward(q, k, v, do, 0.45, causal, pos, W)
+        ref = _sdpa_grads(q, k, v, do, 0.45, causal, pos, W)
+        for name, a_, b_ in zip(("dQ", "dK", "dV"), got, ref):
+            np.testing.assert_allclose(a_, b_, rtol=0, atol=1e-12,
+                                       err_msg=name)
+
+
+def pin_bwd_finite_differences(orc):
+    """The backward is the derivative of the forward: central differences
+    of L = sum(O * dO) through the oracle's forward pass, every input
+    element of a tiny causal GQA case with an offset and a window."""
+    rng = np.random.default_rng(32)
+    B, Hq, Hkv, Sq, Skv, D, pos, W = 1, 2, 1, 3, 5, 3, 2, 3
+    q = _rand((B, Hq, Sq, D), rng)
+    k = _rand((B, Hkv, Skv, D), rng)
+    v = _rand((B, Hkv, Skv, D), rng)
+    do = _rand((B, Hq, Sq, D), rng)
+    grads = orc.backward(q, k, v, do, 0.7, True, pos, W)
+    h = 1e-5
+    for x, gx in zip((q, k, v), grads):
+        for idx in np.ndindex(x.shape):
+            old = x[idx]
+            x[idx] = old + h
+            lp = float(np.sum(orc.attention(q, k, v, 0.7, True, pos, W)[0] * do))
+            x[idx] = old - h
+            lm = float(np.sum(orc.attention(q, k, v, 0.7, True, pos, W)[0] * do))
+            x[idx] = old
+            assert abs((lp - lm) / (2 * h) - gx[idx]) < 1e-7, idx
+
+
+def pin_bwd_single_key(orc):
+    """Skv = 1: O = V_0 whatever Q and K are, so dQ = dK = 0 and dV_0 is
+    the sum of dO over the group's query heads and rows."""
+    rng = np.random.default_rng(33)
+    B, Hq, Hkv, Sq, D = 2, 4, 2, 3, 5
+    q = _rand((B, Hq, Sq, D), rng)
+    k = _rand((B, Hkv, 1, D), rng)
+    v = _rand((B, Hkv, 1, D), rng)
+    do = _rand((B, Hq, Sq, D), rng)
+    dq, dk, dv = orc.backward(q, k, v, do, 0.9, True, 0)
+    assert np.all(dq == 0.0) and np.all(dk == 0.0)
+    want = do.reshape(B, Hkv, Hq // Hkv, Sq, D).sum(axis=(2, 3))
+    np.testing.assert_allclose(dv[:, :, 0], want, rtol=0, atol=1e-12)
+
+
 ALL_PINS = [
     pin_hand_cases, pin_single_key, pin_uniform_scores, pin_prob_rows,
     pin_gqa_equivalence, pin_causal_first_row, pin_permutation_invariance,
     pin_causal_prefix, pin_shift_invariance, pin_negated_scale,
     pin_torch_sdpa, pin_window_single_key, pin_window_uniform_scores,
     pin_window_wide_is_causal, pin_window_decode_slice,
+    pin_bwd_torch_autograd, pin_bwd_finite_differences, pin_bwd_single_key,
 ]

@@ -39,6 +39,16 @@ MUTANTS = {
                        "return 1;"),
     "window_without_offset": ("j > input_pos + i - window",
                               "j > i - window"),
+    "bwd_rowsum_dropped": ("const double ds = prob[j] * (dprob[j] - pdp);",
+                           "const double ds = prob[j] * dprob[j];"),
+    "bwd_dq_scale_dropped": ("dq[d] += scale * ds * k[j * D + d];",
+                             "dq[d] += ds * k[j * D + d];"),
+    "bwd_dk_uses_k": ("dk[j * D + d] += scale * ds * q[d];",
+                      "dk[j * D + d] += scale * ds * k[j * D + d];"),
+    "bwd_dv_uses_ds": ("dv[j * D + d] += prob[j] * dout[d];",
+                       "dv[j * D + d] += ds * dout[d];"),
+    "bwd_dp_uses_k": ("dot += dout[d] * v[j * D + d];",
+                      "dot += dout[d] * k[j * D + d];"),
 }
 
 
