@@ -19,7 +19,8 @@ __all__ = [
     "attn_fwd_splitkv", "attn_fwd_splitkv_window",
     "attn_splitkv_plan", "attn_fwd_splitkv_noalloc",
     "attn_noalloc_scratch_bytes", "attn_status_string", "attn_device_status",
-    "attn_tile_config", "attn_version", "fwd", "fwd_splitkv",
+    "attn_tile_config", "attn_version", "attn_bwd", "attn_bwd_workspace_bytes",
+    "fwd", "fwd_splitkv", "bwd",
     "library_path", "load_library",
 ]
 
@@ -95,6 +96,12 @@ def load_library():
                                                  i, i, i, ctypes.c_float, i,
                                                  i, i, i, vp]
         lib.attn_fwd_splitkv_noalloc.restype = i
+        lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i,
+                                 i, i, i, ctypes.c_float, i, i, i, i, vp, sz,
+                                 vp]
+        lib.attn_bwd.restype = i
+        lib.attn_bwd_workspace_bytes.argtypes = [i, i, i]
+        lib.attn_bwd_workspace_bytes.restype = sz
         lib.attn_noalloc_scratch_bytes.argtypes = []
         lib.attn_noalloc_scratch_bytes.restype = sz
         _lib = lib
@@ -151,6 +158,21 @@ def attn_fwd_splitkv_noalloc(Q, K, V, O, LSE, B, Hq, Hkv, Sq, Skv, D, scale,
         Q or None, K or None, V or None, O or None, LSE or None, B, Hq, Hkv,
         Sq, Skv, D, float(scale), int(causal), int(input_pos), int(dtype),
         int(num_splits), stream or None))
+
+
+def attn_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, B, Hq, Hkv, Sq, Skv, D, scale,
+             causal, input_pos, window, dtype, workspace, workspace_bytes,
+             stream) -> int:
+    """Raw C-ABI call of the backward pass; pointers are integers."""
+    return int(load_library().attn_bwd(
+        Q or None, K or None, V or None, O or None, LSE or None, dO or None,
+        dQ or None, dK or None, dV or None, B, Hq, Hkv, Sq, Skv, D,
+        float(scale), int(causal), int(input_pos), int(window), int(dtype),
+        workspace or None, int(workspace_bytes), stream or None))
+
+
+def attn_bwd_workspace_bytes(B, Hq, Sq) -> int:
+    return int(load_library().attn_bwd_workspace_bytes(B, Hq, Sq))
 
 
 def attn_noalloc_scratch_bytes() -> int:
@@ -312,3 +334,42 @@ def fwd_splitkv(q, k, v, scale=None, causal=True, input_pos=0, num_splits=0,
     if st != ATTN_OK:
         raise AttnError("attn_fwd_splitkv: " + attn_status_string(st), st)
     return out, (lse if need_lse else None)
+
+
+def bwd(q, k, v, o, lse, do, scale=None, causal=True, input_pos=0, window=0,
+        dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward pass on CUDA tensors: (dQ, dK, dV) for upstream gradient
+    ``do``, given the forward's ``o`` and ``lse`` for the same arguments."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do),
+                    ("lse", lse)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise AttnError("%s must be a contiguous CUDA tensor" % name,
+                            ATTN_ERR_INVALID_ARG)
+    dt = _dtype_code(q)
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Skv, _ = k.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(q.device):
+        if dq is None:
+            dq = torch.empty_like(q)
+        if dk is None:
+            dk = torch.empty_like(k)
+        if dv is None:
+            dv = torch.empty_like(v)
+        if workspace is None:
+            workspace = torch.empty(max(attn_bwd_workspace_bytes(B, Hq, Sq), 1),
+                                    dtype=torch.uint8, device=q.device)
+        if stream is None:
+            stream = torch.cuda.current_stream(q.device)
+        st = attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                      lse.data_ptr(), do.data_ptr(), dq.data_ptr(),
+                      dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Sq, Skv, D,
+                      scale, causal, input_pos, window, dt,
+                      workspace.data_ptr(),
+                      workspace.numel() * workspace.element_size(),
+                      stream.cuda_stream)
+    if st != ATTN_OK:
+        raise AttnError("attn_bwd: " + attn_status_string(st), st)
+    return dq, dk, dv

@@ -18,9 +18,10 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libattn_fwd_gb300.so")
 SOURCES = ["attn_api.cu", "attn_fwd_d64.cu", "attn_fwd_d128.cu",
            "attn_fwd_d64_packed.cu", "attn_fwd_d128_packed.cu",
-           "attn_noalloc.cu"]
-HEADERS = ["attn_fwd_kernel.cuh", "attn_fwd_launch.cuh", "sm103_ptx.cuh",
-           "attn_launch.h"]
+           "attn_noalloc.cu", "attn_bwd.cu"]
+HEADERS = ["attn_fwd_kernel.cuh", "attn_fwd_launch.cuh", "attn_sync.cuh",
+           "attn_bwd_kernel.cuh",
+           "sm103_ptx.cuh", "attn_launch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

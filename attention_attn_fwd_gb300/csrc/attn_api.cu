@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/attn.h"
+#include "attn_bwd_kernel.cuh"
 #include "attn_launch.h"
 
 // Device status word: bit 0 = a pipeline wait ran out, bits 8-15 = role.
@@ -406,6 +407,126 @@ attn_status_t splitkv_impl(const Shape& s, const void* Q, const void* K,
       reinterpret_cast<cudaStream_t>(stream));
 }
 
+// Rows per (batch, query head) plane of the backward's per-row arrays:
+// Sq padded to whole 128-row tiles.
+size_t bwd_sq_pad(const Shape& s) {
+  return (static_cast<size_t>(s.Sq) + attn::bwd::kT - 1) / attn::bwd::kT *
+         attn::bwd::kT;
+}
+
+// Bytes of the backward workspace: lse2 and D, fp32 per padded query row.
+size_t bwd_workspace_bytes(const Shape& s) {
+  const size_t rows = static_cast<size_t>(s.B) * s.Hq * bwd_sq_pad(s);
+  return 2 * round_up(rows * 4, kWorkspaceAlign);
+}
+
+attn_status_t bwd_impl(const Shape& s, const void* Q, const void* K,
+                       const void* V, const void* O, const float* LSE,
+                       const void* dO, void* dQ, void* dK, void* dV,
+                       float scale, attn_dtype_t dtype, void* workspace,
+                       size_t workspace_bytes, attn_stream_t stream) {
+  attn_status_t st = check_scalars(s, scale, dtype);
+  if (st != ATTN_OK) return st;
+  if (s.B == 0) return ATTN_OK;
+  const void* in16[] = {Q, K, V, O, dO};
+  void* out16[] = {dQ, dK, dV};
+  for (const void* ptr : in16)
+    if (ptr == nullptr) return ATTN_ERR_INVALID_ARG;
+  for (void* ptr : out16)
+    if (ptr == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (LSE == nullptr) return ATTN_ERR_INVALID_ARG;
+  auto misaligned = [](const void* ptr, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(ptr) % a) != 0;
+  };
+  for (const void* ptr : in16)
+    if (misaligned(ptr, 16)) return ATTN_ERR_ALIGNMENT;
+  for (void* ptr : out16)
+    if (misaligned(ptr, 16)) return ATTN_ERR_ALIGNMENT;
+  if (misaligned(LSE, 4)) return ATTN_ERR_ALIGNMENT;
+  const size_t q_bytes = static_cast<size_t>(s.B) * s.Hq * s.Sq * s.D * 2;
+  const size_t kv_bytes = static_cast<size_t>(s.B) * s.Hkv * s.Skv * s.D * 2;
+  const size_t lse_bytes = static_cast<size_t>(s.B) * s.Hq * s.Sq * 4;
+  // Outputs must not overlap any input or each other.
+  const void* ins[] = {Q, K, V, O, dO, LSE};
+  const size_t in_bytes[] = {q_bytes, kv_bytes, kv_bytes, q_bytes, q_bytes,
+                             lse_bytes};
+  const size_t out_bytes[] = {q_bytes, kv_bytes, kv_bytes};
+  for (int o = 0; o < 3; ++o) {
+    for (int i = 0; i < 6; ++i)
+      if (overlaps(out16[o], out_bytes[o], ins[i], in_bytes[i]))
+        return ATTN_ERR_INVALID_ARG;
+    for (int o2 = o + 1; o2 < 3; ++o2)
+      if (overlaps(out16[o], out_bytes[o], out16[o2], out_bytes[o2]))
+        return ATTN_ERR_INVALID_ARG;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  for (const void* ptr : ins)
+    if (!is_device_ptr(ptr, dev)) return ATTN_ERR_INVALID_ARG;
+  for (void* ptr : out16)
+    if (!is_device_ptr(ptr, dev)) return ATTN_ERR_INVALID_ARG;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (s.Sq == 0) {
+    // No query: the gradients of K and V are zero.
+    if (cudaMemsetAsync(dK, 0, kv_bytes, cs) != cudaSuccess ||
+        cudaMemsetAsync(dV, 0, kv_bytes, cs) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    return ATTN_OK;
+  }
+  if (workspace == nullptr ||
+      reinterpret_cast<uintptr_t>(workspace) % kWorkspaceAlign != 0)
+    return ATTN_ERR_ALIGNMENT;
+  if (workspace_bytes < bwd_workspace_bytes(s)) return ATTN_ERR_INVALID_ARG;
+  if (!is_device_ptr(workspace, dev)) return ATTN_ERR_INVALID_ARG;
+  for (int i = 0; i < 6; ++i)
+    if (overlaps(workspace, workspace_bytes, ins[i], in_bytes[i]))
+      return ATTN_ERR_INVALID_ARG;
+  for (int o = 0; o < 3; ++o)
+    if (overlaps(workspace, workspace_bytes, out16[o], out_bytes[o]))
+      return ATTN_ERR_INVALID_ARG;
+  unsigned int* status = status_ptr(dev);
+  if (status == nullptr) return ATTN_ERR_CUDA;
+
+  const long long q_planes = static_cast<long long>(s.B) * s.Hq;
+  const long long kv_planes = static_cast<long long>(s.B) * s.Hkv;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_map(&tq, Q, dtype, s.D, s.Sq, q_planes) ||
+      !make_map(&tk, K, dtype, s.D, s.Skv, kv_planes) ||
+      !make_map(&tv, V, dtype, s.D, s.Skv, kv_planes) ||
+      !make_map(&tdo, dO, dtype, s.D, s.Sq, q_planes))
+    return ATTN_ERR_CUDA;
+  const size_t rows = static_cast<size_t>(s.B) * s.Hq * bwd_sq_pad(s);
+  float* lse2 = static_cast<float*>(workspace);
+  float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                          round_up(rows * 4, kWorkspaceAlign));
+  attn::BwdParams p{};
+  p.B = s.B;
+  p.Hq = s.Hq;
+  p.Hkv = s.Hkv;
+  p.Sq = s.Sq;
+  p.Skv = s.Skv;
+  p.causal = s.causal != 0;
+  p.input_pos = s.causal != 0 ? s.input_pos : 0;
+  p.window = s.causal != 0 ? s.window : 0;
+  p.group = s.Hq / s.Hkv;
+  p.q_tiles = (s.Sq + attn::bwd::kT - 1) / attn::bwd::kT;
+  p.k_tiles = (s.Skv + attn::bwd::kT - 1) / attn::bwd::kT;
+  p.sq_pad = static_cast<int>(bwd_sq_pad(s));
+  p.scale_log2 = std::fabs(scale) * 1.4426950408889634f;
+  p.negate_scores = scale < 0.f;
+  p.scale = scale;
+  p.lse2 = lse2;
+  p.delta = delta;
+  p.dq = dQ;
+  p.dk = dK;
+  p.dv = dV;
+  p.status = status;
+  p.timeout_ns = timeout_ns();
+  const cudaError_t err = attn::launch_bwd(s.D, dtype == ATTN_BF16, tq, tk,
+                                           tv, tdo, O, dO, LSE, p, cs);
+  return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -470,6 +591,24 @@ attn_status_t attn_fwd_splitkv_window(const void* Q, const void* K,
   const Shape s{B, Hq, Hkv, Sq, Skv, D, causal != 0, input_pos, window};
   return splitkv_impl(s, Q, K, V, O, LSE, scale, dtype, num_splits,
                       workspace, workspace_bytes, stream);
+}
+
+size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq) {
+  if (B < 0 || Hq < 0 || Sq < 0) return 0;
+  const Shape s{B, Hq, 1, Sq, 1, 64, 0, 0};
+  return bwd_workspace_bytes(s);
+}
+
+attn_status_t attn_bwd(const void* Q, const void* K, const void* V,
+                       const void* O, const float* LSE, const void* dO,
+                       void* dQ, void* dK, void* dV, int B, int Hq, int Hkv,
+                       int Sq, int Skv, int D, float scale, int causal,
+                       int input_pos, int window, attn_dtype_t dtype,
+                       void* workspace, size_t workspace_bytes,
+                       attn_stream_t stream) {
+  const Shape s{B, Hq, Hkv, Sq, Skv, D, causal != 0, input_pos, window};
+  return bwd_impl(s, Q, K, V, O, LSE, dO, dQ, dK, dV, scale, dtype,
+                  workspace, workspace_bytes, stream);
 }
 
 const char* attn_status_string(attn_status_t status) {

@@ -1,0 +1,82 @@
+// Launches of the backward kernels (row pass, dK/dV, dQ) for D = 64 / 128
+// and fp16 / bf16.
+#include "attn_bwd_kernel.cuh"
+#include "attn_launch.h"
+
+namespace attn {
+namespace {
+
+template <class Kernel>
+cudaError_t set_smem(Kernel kernel, int smem, int* configured) {
+  // The attribute is per device; set it once per device and kernel.
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (*configured != dev) {
+    err = cudaFuncSetAttribute(kernel,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               smem);
+    if (err != cudaSuccess) return err;
+    *configured = dev;
+  }
+  return cudaSuccess;
+}
+
+template <class Kernel>
+cudaError_t launch(Kernel kernel, int smem, int grid, cudaStream_t stream,
+                   const CUtensorMap& q, const CUtensorMap& k,
+                   const CUtensorMap& v, const CUtensorMap& d,
+                   const BwdParams& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(bwd::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, kernel, q, k, v, d, p);
+}
+
+template <int D, bool kBF16>
+cudaError_t run(const CUtensorMap& q, const CUtensorMap& k,
+                const CUtensorMap& v, const CUtensorMap& d, const void* O,
+                const void* dO, const float* LSE, const BwdParams& p,
+                cudaStream_t stream) {
+  static thread_local int cfg_dkdv = -1, cfg_dq = -1;
+  const long long rows = static_cast<long long>(p.B) * p.Hq * p.sq_pad;
+  float* lse2 = const_cast<float*>(p.lse2);
+  float* delta = const_cast<float*>(p.delta);
+  const long long blocks = (rows * 32 + 255) / 256;
+  attn_bwd_prep_kernel<D, kBF16><<<static_cast<unsigned>(blocks), 256, 0,
+                                   stream>>>(O, dO, LSE, lse2, delta, rows,
+                                             p.Sq, p.sq_pad);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+
+  auto dkdv = attn_bwd_dkdv_kernel<D, kBF16>;
+  const int smem_kv = DkdvLayout<D>::kSmemBytes;
+  err = set_smem(dkdv, smem_kv, &cfg_dkdv);
+  if (err != cudaSuccess) return err;
+  err = launch(dkdv, smem_kv, p.B * p.Hkv * p.k_tiles, stream, q, k, v, d, p);
+  if (err != cudaSuccess) return err;
+
+  auto dq = attn_bwd_dq_kernel<D, kBF16>;
+  const int smem_q = DqLayout<D>::kSmemBytes;
+  err = set_smem(dq, smem_q, &cfg_dq);
+  if (err != cudaSuccess) return err;
+  return launch(dq, smem_q, p.B * p.Hq * p.q_tiles, stream, q, k, v, d, p);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(int D, bool bf16, const CUtensorMap& q,
+                       const CUtensorMap& k, const CUtensorMap& v,
+                       const CUtensorMap& d, const void* O, const void* dO,
+                       const float* LSE, const BwdParams& p,
+                       cudaStream_t stream) {
+  if (D == 64)
+    return bf16 ? run<64, true>(q, k, v, d, O, dO, LSE, p, stream)
+                : run<64, false>(q, k, v, d, O, dO, LSE, p, stream);
+  return bf16 ? run<128, true>(q, k, v, d, O, dO, LSE, p, stream)
+              : run<128, false>(q, k, v, d, O, dO, LSE, p, stream);
+}
+
+}  // namespace attn

@@ -1,0 +1,917 @@
+// Backward pass of the attention forward on sm_103a: dQ, dK, dV for an
+// upstream gradient dO.
+//
+// "Flash Attention from Scratch" lists the backward pass as future work
+// (section "What's Next") and gives no design; this is the recomputation
+// scheme of the flash method -- nothing of size Sq x Skv is stored, P is
+// rebuilt tile by tile from the forward's log-sum-exp -- built from the
+// forward kernel's tcgen05 / TMA pieces.  With lse2_i = LSE_i log2(e),
+// c = |scale| log2(e) and D_i = sum_d dO_id O_id:
+//   P_ij  = 2^(s_ij c - lse2_i)          (s_ij = +-q_i.k_j, sign of scale)
+//   dV_j  = sum_i P_ij dO_i
+//   dP_ij = dO_i . V_j,   dS_ij = P_ij (dP_ij - D_i)
+//   dQ_i  = scale sum_j dS_ij K_j,       dK_j = scale sum_i dS_ij Q_i
+// Three launches: a row pass computing D and lse2; the dK/dV kernel (one
+// CTA per (batch, K/V head, 128-key tile), looping over the group's query
+// heads and the query tiles that see those keys, dK and dV accumulating in
+// TMEM); the dQ kernel (one CTA per (batch, query head, 128-row tile),
+// looping over the key tiles it sees, dQ accumulating in TMEM).  S and dP
+// are computed in both kernels (7 tile products where one pass with dQ
+// atomics would need 5), so every output has a single writer and the result
+// is deterministic.
+//
+// Roles (256 threads): warp 0 TMEM allocator and tcgen05.mma issuer, warp 1
+// TMA producer, warps 4-7 the element-wise work (one TMEM lane = one row
+// per thread) and the epilogue; warps 2-3 idle.  Every mbarrier wait is
+// bounded as in the forward kernel.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "attn_sync.cuh"
+#include "sm103_ptx.cuh"
+
+namespace attn {
+
+struct BwdParams {
+  int B, Hq, Hkv, Sq, Skv;
+  int causal;
+  int input_pos;
+  int window;              // sliding window in keys (causal only), 0: none
+  int group;               // Hq / Hkv
+  int q_tiles, k_tiles;    // 128-row query / key tiles per head
+  int sq_pad;              // q_tiles * 128: rows per plane of lse2 / delta
+  float scale_log2;        // |scale| * log2(e)
+  int negate_scores;       // scale < 0: S is computed as -(Q K^T)
+  float scale;             // signed; dQ and dK carry this factor
+  const float* lse2;       // [B*Hq, sq_pad] LSE * log2(e), +inf past Sq
+  const float* delta;      // [B*Hq, sq_pad] rowsum(dO * O), 0 past Sq
+  void* dq;                // [B, Hq, Sq, D]
+  void* dk;                // [B, Hkv, Skv, D]
+  void* dv;                // [B, Hkv, Skv, D]
+  unsigned int* status;
+  unsigned long long timeout_ns;
+};
+
+namespace bwd {
+constexpr int kT = 128;        // rows per query / key tile
+constexpr int kThreads = 256;
+constexpr int kMmaWarp = 0;
+constexpr int kLoadWarp = 1;
+constexpr int kWorkWarp0 = 4;  // warps 4-7
+constexpr int kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+}  // namespace bwd
+
+// Any valid query row of tile m sees a key of tile n.
+__device__ __forceinline__ bool pair_visible(const BwdParams& p, int m,
+                                             int n) {
+  if (!p.causal) return true;
+  const int pos_first = p.input_pos + m * bwd::kT;
+  const int pos_last = p.input_pos + min(m * bwd::kT + bwd::kT, p.Sq) - 1;
+  const int key_first = n * bwd::kT;
+  const int key_last = min(n * bwd::kT + bwd::kT, p.Skv) - 1;
+  if (key_first > pos_last) return false;
+  if (p.window > 0 && key_last <= pos_first - p.window) return false;
+  return true;
+}
+
+// Every valid query row of tile m sees every valid key of tile n.
+__device__ __forceinline__ bool pair_full(const BwdParams& p, int m, int n) {
+  if (!p.causal) return true;
+  const int pos_first = p.input_pos + m * bwd::kT;
+  const int pos_last = p.input_pos + min(m * bwd::kT + bwd::kT, p.Sq) - 1;
+  const int key_first = n * bwd::kT;
+  const int key_last = min(n * bwd::kT + bwd::kT, p.Skv) - 1;
+  if (key_last > pos_first) return false;
+  if (p.window > 0 && key_first <= pos_last - p.window) return false;
+  return true;
+}
+
+// (y0, y1) = (x0, x1) * m + (a0, a1) as one packed f32x2 FMA.
+__device__ __forceinline__ void ffma2v(float& y0, float& y1, float x0,
+                                       float x1, float m, float a0, float a1) {
+  asm("{\n\t.reg .b64 x, mm, aa, y;\n\t"
+      "mov.b64 x, {%2, %3};\n\tmov.b64 mm, {%4, %4};\n\t"
+      "mov.b64 aa, {%5, %6};\n\t"
+      "fma.rn.ftz.f32x2 y, x, mm, aa;\n\t"
+      "mov.b64 {%0, %1}, y;\n\t}"
+      : "=f"(y0), "=f"(y1)
+      : "f"(x0), "f"(x1), "f"(m), "f"(a0), "f"(a1));
+}
+
+// 16-bit pair (as packed by ptx::pack2) back to two floats.
+template <bool kBF16>
+__device__ __forceinline__ float2 unpack2(uint32_t v) {
+  if constexpr (kBF16) {
+    return make_float2(__uint_as_float(v << 16),
+                       __uint_as_float(v & 0xffff0000u));
+  } else {
+    return __half22float2(*reinterpret_cast<const __half2*>(&v));
+  }
+}
+
+// First (query head, query tile) index hm >= from whose tile sees key tile
+// n (dK/dV steps), or `end`.
+__device__ __forceinline__ int next_pair_hm(const BwdParams& p, int n,
+                                            int from, int end) {
+  int hm = from;
+  while (hm < end && !pair_visible(p, hm % p.q_tiles, n)) ++hm;
+  return hm;
+}
+
+// First key tile index >= from that query tile m sees (dQ steps), or
+// k_tiles.
+__device__ __forceinline__ int next_key_tile(const BwdParams& p, int m,
+                                             int from) {
+  int n = from;
+  while (n < p.k_tiles && !pair_visible(p, m, n)) ++n;
+  return n;
+}
+
+// ------------------------------------------------------------- row pass
+// D_i = sum_d dO_id O_id and lse2_i = LSE_i log2(e), one warp per row of
+// the padded [planes, sq_pad] arrays; rows past Sq get lse2 = +inf (so
+// P = 0 there) and D = 0, and the tile loops read whole tiles unchecked.
+template <int D, bool kBF16>
+__global__ void __launch_bounds__(256)
+    attn_bwd_prep_kernel(const void* __restrict__ O,
+                         const void* __restrict__ dO,
+                         const float* __restrict__ LSE,
+                         float* __restrict__ lse2, float* __restrict__ delta,
+                         long long padded_rows, int Sq, int sq_pad) {
+  constexpr int kPer = D / 32;  // elements per lane (2 or 4)
+  const long long prow =
+      (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  if (prow >= padded_rows) return;
+  const long long plane = prow / sq_pad;
+  const int r = static_cast<int>(prow % sq_pad);
+  if (r >= Sq) {
+    if (lane == 0) {
+      delta[prow] = 0.f;
+      lse2[prow] = INFINITY;
+    }
+    return;
+  }
+  const long long row = plane * Sq + r;
+  const uint16_t* o = static_cast<const uint16_t*>(O) + row * D + lane * kPer;
+  const uint16_t* g = static_cast<const uint16_t*>(dO) + row * D + lane * kPer;
+  float acc = 0.f;
+#pragma unroll
+  for (int e = 0; e < kPer; e += 2) {
+    const uint32_t ov = *reinterpret_cast<const uint32_t*>(o + e);
+    const uint32_t gv = *reinterpret_cast<const uint32_t*>(g + e);
+    float2 of, gf;
+    if constexpr (kBF16) {
+      of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov));
+      gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gv));
+    } else {
+      of = __half22float2(*reinterpret_cast<const __half2*>(&ov));
+      gf = __half22float2(*reinterpret_cast<const __half2*>(&gv));
+    }
+    acc = fmaf(of.x, gf.x, acc);
+    acc = fmaf(of.y, gf.y, acc);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+    acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) {
+    delta[prow] = acc;
+    lse2[prow] = LSE[row] * bwd::kLog2e;
+  }
+}
+
+// ------------------------------------------------------ shared layouts
+template <int D>
+struct BwdTiles {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kBoxBytes = 128 * 128;            // 128 rows x 128 B
+  static constexpr int kTileBytes = kChunks * kBoxBytes; // one 128 x D tile
+};
+
+// dK/dV kernel: K and V tiles resident, separate rings of Q and dO tiles
+// (Q is held until dK(s), dO only until dV(s), so the Q ring is the deeper
+// one; 3 + 2 slots fill the 227 KB at D=128).
+template <int D>
+struct DkdvLayout : BwdTiles<D> {
+  using T = BwdTiles<D>;
+  static constexpr int kQSlots = (D == 128) ? 3 : 4;
+  static constexpr int kDoSlots = (D == 128) ? 2 : 4;
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = T::kTileBytes;
+  static constexpr int kQOff = 2 * T::kTileBytes;
+  static constexpr int kDoOff = kQOff + kQSlots * T::kTileBytes;
+  static constexpr int kBarOff = kDoOff + kDoSlots * T::kTileBytes;
+  // kv_full, q_full[QS], q_empty[QS], do_full[DS], do_empty[DS], s_ready,
+  // dp_ready, p_ready, ds_ready, acc_done, drain
+  static constexpr int kNumBars = 1 + 2 * kQSlots + 2 * kDoSlots + 6;
+  static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+};
+
+// dQ kernel: Q and dO resident, a ring of K / V tiles.
+template <int D>
+struct DqLayout : BwdTiles<D> {
+  using T = BwdTiles<D>;
+  static constexpr int kSlots = (D == 128) ? 4 : 8;
+  static constexpr int kQOff = 0;
+  static constexpr int kDoOff = T::kTileBytes;
+  static constexpr int kRingOff = 2 * T::kTileBytes;
+  static constexpr int kBarOff = kRingOff + kSlots * T::kTileBytes;
+  // q_full, full[S], empty[S], s_ready[2], dp_ready, ds_ready, acc_done,
+  // drain
+  static constexpr int kNumBars = 1 + 2 * kSlots + 6;
+  static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+};
+
+// Stores one 16-bit output row (D values, fp32 in TMEM at t_acc, times
+// `mul`) from registers; `store` false reads TMEM only (every lane of the
+// warp takes part in tcgen05.ld).
+template <int D, bool kBF16>
+__device__ __forceinline__ void store_row(uint32_t t_acc, float mul,
+                                          uint16_t* dst, bool store) {
+  uint4* out = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < D / 32; ++q) {
+    uint32_t a[32];
+    ptx::tmem_ld32(t_acc + 32 * q, a);
+    ptx::tmem_wait_ld();
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        w[e] = ptx::pack2<kBF16>(__uint_as_float(a[8 * v + 2 * e]) * mul,
+                                 __uint_as_float(a[8 * v + 2 * e + 1]) * mul);
+      if (store) out[4 * q + v] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+// ------------------------------------------------------- dK / dV kernel
+// Unit u: key tile n = u / (B*Hkv) (under a causal mask the first key tiles
+// see the most queries, so they start first), (b, K/V head) = u % (B*Hkv).
+// Steps: the (query head of the group, query tile m) pairs that see tile
+// n, in order.  TMEM: S^T [0,128), dP^T [128,256), dV [256,256+D),
+// dK [256+D, 256+2D); P^T and dS^T (16-bit) overwrite the first 64 columns
+// of S^T and dP^T and are the A operands of dV += P^T dO and dK += dS^T Q.
+// Software pipeline: the element-wise pass is split at "P ready" and "dS
+// ready" (P stays in registers, 16-bit, for the dS half), so the tensor
+// pipe runs dV(s) and S^T(s+1) while dS(s) is computed, and dK(s) and
+// dP^T(s+1) while P(s+1) is.
+template <int D, bool kBF16>
+__global__ void __launch_bounds__(bwd::kThreads, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v,
+                         const __grid_constant__ CUtensorMap tm_do,
+                         const BwdParams p) {
+  using L = DkdvLayout<D>;
+  using namespace bwd;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s_base = ptx::smem_u32(smem);
+  const uint32_t s_k = s_base + L::kKOff;
+  const uint32_t s_v = s_base + L::kVOff;
+  const uint32_t s_qr = s_base + L::kQOff;   // Q ring
+  const uint32_t s_dor = s_base + L::kDoOff; // dO ring
+  const uint32_t bar0 = s_base + L::kBarOff;
+  const uint32_t bar_kv = bar0;
+  const uint32_t bar_qf = bar0 + 8;                      // [kQSlots]
+  const uint32_t bar_qe = bar_qf + 8 * L::kQSlots;       // [kQSlots]
+  const uint32_t bar_df = bar_qe + 8 * L::kQSlots;       // [kDoSlots]
+  const uint32_t bar_de = bar_df + 8 * L::kDoSlots;      // [kDoSlots]
+  const uint32_t bar_s = bar_de + 8 * L::kDoSlots;
+  const uint32_t bar_dp = bar_s + 8;
+  const uint32_t bar_p = bar_dp + 8;
+  const uint32_t bar_ds = bar_p + 8;
+  const uint32_t bar_acc = bar_ds + 8;
+  const uint32_t bar_drain = bar_acc + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<int*>(smem + L::kMiscOff + 4);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int bkv = p.B * p.Hkv;
+  const int n = static_cast<int>(blockIdx.x) / bkv;
+  const int bk = static_cast<int>(blockIdx.x) % bkv;  // b * Hkv + kvh
+  const int b = bk / p.Hkv;
+  const int qplane0 = b * p.Hq + (bk % p.Hkv) * p.group;
+  const int steps_all = p.group * p.q_tiles;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < L::kNumBars; ++i) {
+      const uint32_t bar = bar0 + 8 * i;
+      ptx::mbar_init(bar, (bar == bar_p || bar == bar_ds) ? kT : 1);
+    }
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kLoadWarp) {
+    // -------------------------------------------------------- producer
+    if (lane == 0) {
+      ptx::prefetch_tensormap(&tm_q);
+      ptx::prefetch_tensormap(&tm_k);
+      ptx::prefetch_tensormap(&tm_v);
+      ptx::prefetch_tensormap(&tm_do);
+    }
+    ptx::mbar_arrive_expect_tx_elect(bar_kv, 2 * L::kTileBytes);
+    for (int c = 0; c < L::kChunks; ++c) {
+      ptx::tma_load_3d_elect(s_k + c * L::kBoxBytes, &tm_k, bar_kv, c * 64,
+                             n * kT, bk);
+      ptx::tma_load_3d_elect(s_v + c * L::kBoxBytes, &tm_v, bar_kv, c * 64,
+                             n * kT, bk);
+    }
+    bool ok = true;
+    int s = 0;
+    int nq = 0, nd = 0;  // Q / dO copies issued
+    for (int hm = 0; hm < steps_all && ok; ++hm) {
+      const int m = hm % p.q_tiles;
+      if (!pair_visible(p, m, n)) continue;
+      const int qplane = qplane0 + hm / p.q_tiles;
+      const int qs = s % L::kQSlots, ds = s % L::kDoSlots;
+      if (s >= L::kQSlots) {
+        ok = __all_sync(0xffffffffu,
+                        wait_bounded(bar_qe + 8 * qs,
+                                     ((s / L::kQSlots) - 1) & 1, abort_flag,
+                                     p, 1));
+        if (!ok) break;
+      }
+      ptx::mbar_arrive_expect_tx_elect(bar_qf + 8 * qs, L::kTileBytes);
+      for (int c = 0; c < L::kChunks; ++c)
+        ptx::tma_load_3d_elect(s_qr + qs * L::kTileBytes + c * L::kBoxBytes,
+                               &tm_q, bar_qf + 8 * qs, c * 64, m * kT, qplane);
+      ++nq;
+      if (s >= L::kDoSlots) {
+        ok = __all_sync(0xffffffffu,
+                        wait_bounded(bar_de + 8 * ds,
+                                     ((s / L::kDoSlots) - 1) & 1, abort_flag,
+                                     p, 1));
+        if (!ok) break;
+      }
+      ptx::mbar_arrive_expect_tx_elect(bar_df + 8 * ds, L::kTileBytes);
+      for (int c = 0; c < L::kChunks; ++c)
+        ptx::tma_load_3d_elect(s_dor + ds * L::kTileBytes + c * L::kBoxBytes,
+                               &tm_do, bar_df + 8 * ds, c * 64, m * kT,
+                               qplane);
+      ++nd;
+      ++s;
+    }
+    if (!ok) {
+      // Let every copy still in flight land before the CTA goes away.
+      drain_wait(bar_kv, 0, p);
+      for (int i = max(0, nq - L::kQSlots); i < nq; ++i)
+        drain_wait(bar_qf + 8 * (i % L::kQSlots), (i / L::kQSlots) & 1, p);
+      for (int i = max(0, nd - L::kDoSlots); i < nd; ++i)
+        drain_wait(bar_df + 8 * (i % L::kDoSlots), (i / L::kDoSlots) & 1, p);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------ MMA issuer
+    constexpr uint32_t kHi = ptx::sdesc_hi_sw128(1024);
+    const uint32_t idesc_s =
+        ptx::idesc_f16(kBF16, kT, kT, false, p.negate_scores != 0);
+    const uint32_t idesc_dp = ptx::idesc_f16(kBF16, kT, kT, false, false);
+    const uint32_t idesc_acc = ptx::idesc_f16(kBF16, kT, D, true, false);
+    const uint32_t t_st = tmem, t_dpt = tmem + kT;
+    const uint32_t t_dv = tmem + 2 * kT, t_dk = tmem + 2 * kT + D;
+    const uint32_t k_lo = ptx::sdesc_lo(s_k, 16);
+    const uint32_t v_lo = ptx::sdesc_lo(s_v, 16);
+    // Q / dO tiles of step s: K-major descriptors for S^T and dP^T,
+    // MN-major ones for the B operands of dK and dV.
+    auto q_tile = [&](int s) { return s_qr + (s % L::kQSlots) * L::kTileBytes; };
+    auto do_tile = [&](int s) {
+      return s_dor + (s % L::kDoSlots) * L::kTileBytes;
+    };
+    auto wait_q = [&](int s) {
+      return __all_sync(0xffffffffu,
+                        wait_bounded(bar_qf + 8 * (s % L::kQSlots),
+                                     (s / L::kQSlots) & 1, abort_flag, p, 2));
+    };
+    auto wait_do = [&](int s) {
+      return __all_sync(0xffffffffu,
+                        wait_bounded(bar_df + 8 * (s % L::kDoSlots),
+                                     (s / L::kDoSlots) & 1, abort_flag, p, 2));
+    };
+    // S^T = K Q^T or dP^T = V dO^T (M = keys, N = queries, K = D).
+    auto issue_kq = [&](uint32_t d, uint32_t a_lo, uint32_t b_lo,
+                        uint32_t idesc) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk / 4) * L::kBoxBytes + (kk % 4) * 32) >> 4;
+        ptx::mma_ss_elect(d, a_lo + off, b_lo + off, kHi, idesc,
+                          kk > 0 ? 1u : 0u);
+      }
+    };
+    // dV += P^T dO or dK += dS^T Q (M = keys, N = D, K = queries).
+    auto issue_acc = [&](uint32_t d, uint32_t a_tmem, uint32_t b_mn,
+                         bool acc) {
+#pragma unroll
+      for (int kk = 0; kk < kT / 16; ++kk)
+        ptx::mma_ts_elect(d, a_tmem + kk * 8, b_mn + ((kk * 16 * 128) >> 4),
+                          kHi, idesc_acc, (acc || kk > 0) ? 1u : 0u);
+    };
+    bool ok = __all_sync(0xffffffffu,
+                         wait_bounded(bar_kv, 0, abort_flag, p, 2));
+    bool issued = false;
+    int s = 0;
+    int hm = next_pair_hm(p, n, 0, steps_all);
+    if (ok && hm < steps_all) {
+      ok = wait_q(0);
+      if (ok) {
+        ptx::tc_fence_after();
+        issue_kq(t_st, k_lo, ptx::sdesc_lo(q_tile(0), 16), idesc_s);
+        ptx::tc_commit_elect(bar_s);
+        issued = true;
+        ok = wait_do(0);
+      }
+      if (ok) {
+        ptx::tc_fence_after();
+        issue_kq(t_dpt, v_lo, ptx::sdesc_lo(do_tile(0), 16), idesc_dp);
+        ptx::tc_commit_elect(bar_dp);
+      }
+    }
+    while (ok && hm < steps_all) {
+      const int hm_next = next_pair_hm(p, n, hm + 1, steps_all);
+      const bool more = hm_next < steps_all;
+      // dV(s) once P^T(s) is in TMEM (dO(s) free after it), then S^T(s+1)
+      // (after dV in issue order, so P^T is read before it is overwritten).
+      ok = __all_sync(0xffffffffu,
+                      wait_bounded(bar_p, s & 1, abort_flag, p, 2));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      issue_acc(t_dv, t_st, ptx::sdesc_lo(do_tile(s), L::kBoxBytes), s > 0);
+      ptx::tc_commit_elect(bar_de + 8 * (s % L::kDoSlots));
+      if (more) {
+        ok = wait_q(s + 1);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_kq(t_st, k_lo, ptx::sdesc_lo(q_tile(s + 1), 16), idesc_s);
+        ptx::tc_commit_elect(bar_s);
+      }
+      // dK(s) once dS^T(s) is in TMEM (Q(s) free after it), then dP^T(s+1).
+      ok = __all_sync(0xffffffffu,
+                      wait_bounded(bar_ds, s & 1, abort_flag, p, 2));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      issue_acc(t_dk, t_dpt, ptx::sdesc_lo(q_tile(s), L::kBoxBytes), s > 0);
+      ptx::tc_commit_elect(bar_qe + 8 * (s % L::kQSlots));
+      if (more) {
+        ok = wait_do(s + 1);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_kq(t_dpt, v_lo, ptx::sdesc_lo(do_tile(s + 1), 16), idesc_dp);
+        ptx::tc_commit_elect(bar_dp);
+      }
+      ++s;
+      hm = hm_next;
+    }
+    if (ok && s > 0) ptx::tc_commit_elect(bar_acc);
+    if (!ok && issued) {
+      ptx::tc_commit_elect(bar_drain);
+      drain_wait(bar_drain, 0, p);
+    }
+    __syncwarp();
+  } else if (warp >= kWorkWarp0) {
+    // ----------------------------------------- P^T, dS^T and epilogue
+    const int r = threadIdx.x - kWorkWarp0 * 32;  // key row in the tile
+    const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    const uint32_t t_st = tmem + lane_off;
+    const uint32_t t_dpt = tmem + lane_off + kT;
+    const int key = n * kT + r;
+    const float c = p.scale_log2;
+    bool ok = true;
+    int s = 0;
+    for (int hm = 0; hm < steps_all && ok; ++hm) {
+      const int m = hm % p.q_tiles;
+      if (!pair_visible(p, m, n)) continue;
+      // lse2 / D of the tile's 128 query rows (padded arrays: no checks).
+      const long long vbase =
+          static_cast<long long>(qplane0 + hm / p.q_tiles) * p.sq_pad + m * kT;
+      const float4* v_l = reinterpret_cast<const float4*>(p.lse2 + vbase);
+      const float4* v_d = reinterpret_cast<const float4*>(p.delta + vbase);
+      // Query column j (position input_pos + m*128 + j) sees this key iff
+      // j >= jlo and, with a window, j < jlo + window.
+      const bool full = pair_full(p, m, n);
+      const int jlo = key - (p.input_pos + m * kT);
+      const unsigned span =
+          p.window > 0 ? static_cast<unsigned>(p.window) : 0x40000000u;
+      // P^T = 2^(S^T c - lse2), kept in registers (16-bit) for dS.
+      ok = __all_sync(0xffffffffu,
+                      wait_bounded(bar_s, s & 1, abort_flag, p, 3));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      uint32_t pk[kT / 32][16];
+#pragma unroll
+      for (int q = 0; q < kT / 32; ++q) {
+        uint32_t sv[32];
+        ptx::tmem_ld32(t_st + 32 * q, sv);
+        float lv[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 t4 = __ldg(v_l + 8 * q + i);
+          lv[4 * i] = t4.x;
+          lv[4 * i + 1] = t4.y;
+          lv[4 * i + 2] = t4.z;
+          lv[4 * i + 3] = t4.w;
+        }
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int j = 32 * q + 2 * e;
+          float x0, x1;
+          ffma2v(x0, x1, __uint_as_float(sv[2 * e]),
+                 __uint_as_float(sv[2 * e + 1]), c, -lv[2 * e], -lv[2 * e + 1]);
+          if (!full) {
+            if (static_cast<unsigned>(j - jlo) >= span) x0 = -INFINITY;
+            if (static_cast<unsigned>(j + 1 - jlo) >= span) x1 = -INFINITY;
+          }
+          pk[q][e] = ptx::pack2<kBF16>(ptx::ex2(x0), ptx::ex2(x1));
+        }
+        // 16-bit P^T over fp32 columns already consumed.
+        ptx::tmem_st16(t_st + 16 * q, pk[q]);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar_p);
+      // dS^T = P^T (dP^T - D).
+      ok = __all_sync(0xffffffffu,
+                      wait_bounded(bar_dp, s & 1, abort_flag, p, 3));
+      if (!ok) break;
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int q = 0; q < kT / 32; ++q) {
+        uint32_t dv[32];
+        ptx::tmem_ld32(t_dpt + 32 * q, dv);
+        float dl[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 t4 = __ldg(v_d + 8 * q + i);
+          dl[4 * i] = t4.x;
+          dl[4 * i + 1] = t4.y;
+          dl[4 * i + 2] = t4.z;
+          dl[4 * i + 3] = t4.w;
+        }
+        ptx::tmem_wait_ld();
+        uint32_t dk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float2 pp = unpack2<kBF16>(pk[q][e]);
+          dk[e] = ptx::pack2<kBF16>(
+              pp.x * (__uint_as_float(dv[2 * e]) - dl[2 * e]),
+              pp.y * (__uint_as_float(dv[2 * e + 1]) - dl[2 * e + 1]));
+        }
+        ptx::tmem_st16(t_dpt + 16 * q, dk);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar_ds);
+      ++s;
+    }
+    if (ok) {
+      // Epilogue: dV and scale * dK rows (keys past Skv are not stored; a
+      // key tile no query sees gets zeros).
+      const long long row = static_cast<long long>(bk) * p.Skv + key;
+      const bool in = key < p.Skv;
+      uint16_t* dvr = static_cast<uint16_t*>(p.dv) + row * D;
+      uint16_t* dkr = static_cast<uint16_t*>(p.dk) + row * D;
+      if (s > 0) {
+        ok = __all_sync(0xffffffffu,
+                        wait_bounded(bar_acc, 0, abort_flag, p, 4));
+        if (ok) {
+          ptx::tc_fence_after();
+          store_row<D, kBF16>(tmem + lane_off + 2 * kT, 1.f, dvr, in);
+          store_row<D, kBF16>(tmem + lane_off + 2 * kT + D, p.scale, dkr, in);
+        }
+      } else if (in) {
+        uint4* a = reinterpret_cast<uint4*>(dvr);
+        uint4* k4 = reinterpret_cast<uint4*>(dkr);
+        for (int i = 0; i < D / 8; ++i) {
+          a[i] = make_uint4(0u, 0u, 0u, 0u);
+          k4[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------ dQ kernel
+// Unit u: query tile m = q_tiles - 1 - u / (B*Hq) (under a causal mask the
+// last rows see the most keys), plane (b, query head) = u % (B*Hq).  Steps:
+// the key tiles n that tile m sees, in order.  TMEM: S double-buffered in
+// [0,128) and [128,256), dP [256,384), dQ [384,384+D); dS (16-bit)
+// overwrites the first 64 columns of dP and is the A operand of
+// dQ += dS K.  Software pipeline: S(s+2) is issued as soon as step s's
+// element-wise pass is done, so P(s+1) can be computed while the tensor
+// pipe runs dQ(s) and dP(s+1).
+template <int D, bool kBF16>
+__global__ void __launch_bounds__(bwd::kThreads, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_do,
+                       const BwdParams p) {
+  using L = DqLayout<D>;
+  using namespace bwd;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s_base = ptx::smem_u32(smem);
+  const uint32_t s_q = s_base + L::kQOff;
+  const uint32_t s_do = s_base + L::kDoOff;
+  const uint32_t s_ring = s_base + L::kRingOff;
+  const uint32_t bar0 = s_base + L::kBarOff;
+  const uint32_t bar_q = bar0;
+  const uint32_t bar_full = bar0 + 8;
+  const uint32_t bar_empty = bar_full + 8 * L::kSlots;
+  const uint32_t bar_s = bar_empty + 8 * L::kSlots;  // [2], per S buffer
+  const uint32_t bar_dp = bar_s + 16;
+  const uint32_t bar_ds = bar_dp + 8;
+  const uint32_t bar_acc = bar_ds + 8;
+  const uint32_t bar_drain = bar_acc + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<int*>(smem + L::kMiscOff + 4);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int bhq = p.B * p.Hq;
+  const int m = p.q_tiles - 1 - static_cast<int>(blockIdx.x) / bhq;
+  const int qplane = static_cast<int>(blockIdx.x) % bhq;  // b * Hq + h
+  const int kvplane = (qplane / p.Hq) * p.Hkv + (qplane % p.Hq) / p.group;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < L::kNumBars; ++i) {
+      const uint32_t bar = bar0 + 8 * i;
+      ptx::mbar_init(bar, bar == bar_ds ? kT : 1);
+    }
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kLoadWarp) {
+    // -------------------------------------------------------- producer
+    if (lane == 0) {
+      ptx::prefetch_tensormap(&tm_q);
+      ptx::prefetch_tensormap(&tm_k);
+      ptx::prefetch_tensormap(&tm_v);
+      ptx::prefetch_tensormap(&tm_do);
+    }
+    ptx::mbar_arrive_expect_tx_elect(bar_q, 2 * L::kTileBytes);
+    for (int c = 0; c < L::kChunks; ++c) {
+      ptx::tma_load_3d_elect(s_q + c * L::kBoxBytes, &tm_q, bar_q, c * 64,
+                             m * kT, qplane);
+      ptx::tma_load_3d_elect(s_do + c * L::kBoxBytes, &tm_do, bar_q, c * 64,
+                             m * kT, qplane);
+    }
+    bool ok = true;
+    int it = 0;  // ring items K_0, V_0, K_1, ... issued
+    for (int n = 0; n < p.k_tiles && ok; ++n) {
+      if (!pair_visible(p, m, n)) continue;
+      for (int kv = 0; kv < 2; ++kv) {
+        const int slot = it % L::kSlots;
+        if (it >= L::kSlots) {
+          ok = __all_sync(0xffffffffu,
+                          wait_bounded(bar_empty + 8 * slot,
+                                       ((it / L::kSlots) - 1) & 1, abort_flag,
+                                       p, 1));
+          if (!ok) break;
+        }
+        const uint32_t dst = s_ring + slot * L::kTileBytes;
+        ptx::mbar_arrive_expect_tx_elect(bar_full + 8 * slot, L::kTileBytes);
+        for (int c = 0; c < L::kChunks; ++c)
+          ptx::tma_load_3d_elect(dst + c * L::kBoxBytes, kv ? &tm_v : &tm_k,
+                                 bar_full + 8 * slot, c * 64, n * kT, kvplane);
+        ++it;
+      }
+    }
+    if (!ok) {
+      drain_wait(bar_q, 0, p);
+      for (int i = max(0, it - L::kSlots); i < it; ++i)
+        drain_wait(bar_full + 8 * (i % L::kSlots), (i / L::kSlots) & 1, p);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------ MMA issuer
+    constexpr uint32_t kHi = ptx::sdesc_hi_sw128(1024);
+    const uint32_t idesc_s =
+        ptx::idesc_f16(kBF16, kT, kT, false, p.negate_scores != 0);
+    const uint32_t idesc_dp = ptx::idesc_f16(kBF16, kT, kT, false, false);
+    const uint32_t idesc_acc = ptx::idesc_f16(kBF16, kT, D, true, false);
+    const uint32_t t_dp = tmem + 2 * kT, t_dq = tmem + 3 * kT;
+    const uint32_t q_lo = ptx::sdesc_lo(s_q, 16);
+    const uint32_t do_lo = ptx::sdesc_lo(s_do, 16);
+    // Ring item `it` (K_s = 2s, V_s = 2s+1) landed.
+    auto wait_item = [&](int it) {
+      return __all_sync(0xffffffffu,
+                        wait_bounded(bar_full + 8 * (it % L::kSlots),
+                                     (it / L::kSlots) & 1, abort_flag, p, 2));
+    };
+    auto tile = [&](int it) { return s_ring + (it % L::kSlots) * L::kTileBytes; };
+    // d = A B^T with A, B K-major 128 x D tiles (S = Q K^T, dP = dO V^T).
+    auto issue_nt = [&](uint32_t d, uint32_t a_lo, uint32_t b_lo,
+                        uint32_t idesc) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk / 4) * L::kBoxBytes + (kk % 4) * 32) >> 4;
+        ptx::mma_ss_elect(d, a_lo + off, b_lo + off, kHi, idesc,
+                          kk > 0 ? 1u : 0u);
+      }
+    };
+    bool ok = __all_sync(0xffffffffu,
+                         wait_bounded(bar_q, 0, abort_flag, p, 2));
+    bool issued = false;
+    const int n0 = next_key_tile(p, m, 0);
+    const int n1 = n0 < p.k_tiles ? next_key_tile(p, m, n0 + 1) : p.k_tiles;
+    // Prologue: S(0), dP(0), S(1).
+    if (ok && n0 < p.k_tiles) {
+      ok = wait_item(0) && wait_item(1);
+      if (ok) {
+        ptx::tc_fence_after();
+        issue_nt(tmem, q_lo, ptx::sdesc_lo(tile(0), 16), idesc_s);
+        ptx::tc_commit_elect(bar_s);
+        issue_nt(t_dp, do_lo, ptx::sdesc_lo(tile(1), 16), idesc_dp);
+        ptx::tc_commit_elect(bar_dp);
+        ptx::tc_commit_elect(bar_empty + 8 * (1 % L::kSlots));
+        issued = true;
+      }
+      if (ok && n1 < p.k_tiles) {
+        ok = wait_item(2);
+        if (ok) {
+          ptx::tc_fence_after();
+          issue_nt(tmem + kT, q_lo, ptx::sdesc_lo(tile(2), 16), idesc_s);
+          ptx::tc_commit_elect(bar_s + 8);
+        }
+      }
+    }
+    int s = 0;
+    int n_cur = n0, n_next = n1;
+    while (ok && n_cur < p.k_tiles) {
+      const int n_after =
+          n_next < p.k_tiles ? next_key_tile(p, m, n_next + 1) : p.k_tiles;
+      // dQ(s) += dS(s) K(s) once dS(s) is in TMEM.
+      ok = __all_sync(0xffffffffu,
+                      wait_bounded(bar_ds, s & 1, abort_flag, p, 2));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t k_mn = ptx::sdesc_lo(tile(2 * s), L::kBoxBytes);
+#pragma unroll
+      for (int kk = 0; kk < kT / 16; ++kk)
+        ptx::mma_ts_elect(t_dq, t_dp + kk * 8, k_mn + ((kk * 16 * 128) >> 4),
+                          kHi, idesc_acc, (s > 0 || kk > 0) ? 1u : 0u);
+      ptx::tc_commit_elect(bar_empty + 8 * ((2 * s) % L::kSlots));
+      // dP(s+1) into the dP region (after dQ(s) in issue order).
+      if (n_next < p.k_tiles) {
+        ok = wait_item(2 * s + 3);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_nt(t_dp, do_lo, ptx::sdesc_lo(tile(2 * s + 3), 16), idesc_dp);
+        ptx::tc_commit_elect(bar_dp);
+        ptx::tc_commit_elect(bar_empty + 8 * ((2 * s + 3) % L::kSlots));
+      }
+      // S(s+2) into S buffer s % 2, free since step s's pass is done.
+      if (n_after < p.k_tiles) {
+        ok = wait_item(2 * s + 4);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_nt(tmem + (s & 1) * kT, q_lo, ptx::sdesc_lo(tile(2 * s + 4), 16),
+                 idesc_s);
+        ptx::tc_commit_elect(bar_s + 8 * (s & 1));
+      }
+      ++s;
+      n_cur = n_next;
+      n_next = n_after;
+    }
+    if (ok && s > 0) ptx::tc_commit_elect(bar_acc);
+    if (!ok && issued) {
+      ptx::tc_commit_elect(bar_drain);
+      drain_wait(bar_drain, 0, p);
+    }
+    __syncwarp();
+  } else if (warp >= kWorkWarp0) {
+    // -------------------------------------------- dS and the epilogue
+    const int r = threadIdx.x - kWorkWarp0 * 32;  // query row in the tile
+    const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    const uint32_t t_dp = tmem + lane_off + 2 * kT;
+    const int q_row = m * kT + r;
+    const bool row_ok = q_row < p.Sq;
+    const long long grow = static_cast<long long>(qplane) * p.Sq + q_row;
+    const long long vrow = static_cast<long long>(qplane) * p.sq_pad + q_row;
+    const float lse2 = p.lse2[vrow];  // +inf past Sq: P = 0
+    const float dlt = p.delta[vrow];
+    const int pos = p.input_pos + q_row;
+    const float c = p.scale_log2;
+    const float neg_l = -lse2;
+    bool ok = true;
+    int s = 0;
+    for (int n = 0; n < p.k_tiles && ok; ++n) {
+      if (!pair_visible(p, m, n)) continue;
+      // Key column k (key n*128 + k) is visible iff lo <= k < lo + span.
+      const bool full = pair_full(p, m, n);
+      const int kbase = n * kT;
+      int lo = 0, lim = kT;
+      if (!full) {
+        lim = pos - kbase + 1;
+        if (p.window > 0) lo = pos - p.window + 1 - kbase;
+      }
+      const unsigned span = static_cast<unsigned>(max(lim - lo, 0));
+      // P = 2^(S c - lse2), kept in registers (16-bit) for dS.
+      ok = __all_sync(0xffffffffu, wait_bounded(bar_s + 8 * (s & 1),
+                                                (s >> 1) & 1, abort_flag, p,
+                                                3));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t t_s = tmem + lane_off + (s & 1) * kT;
+      uint32_t pk[kT / 32][16];
+#pragma unroll
+      for (int q = 0; q < kT / 32; ++q) {
+        uint32_t sv[32];
+        ptx::tmem_ld32(t_s + 32 * q, sv);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int k = 32 * q + 2 * e;
+          float x0, x1;
+          ptx::ffma2(x0, x1, __uint_as_float(sv[2 * e]),
+                     __uint_as_float(sv[2 * e + 1]), c, neg_l);
+          if (!full) {
+            if (static_cast<unsigned>(k - lo) >= span) x0 = -INFINITY;
+            if (static_cast<unsigned>(k + 1 - lo) >= span) x1 = -INFINITY;
+          }
+          pk[q][e] = ptx::pack2<kBF16>(ptx::ex2(x0), ptx::ex2(x1));
+        }
+      }
+      // dS = P (dP - D), 16-bit, over dP.
+      ok = __all_sync(0xffffffffu,
+                      wait_bounded(bar_dp, s & 1, abort_flag, p, 3));
+      if (!ok) break;
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int q = 0; q < kT / 32; ++q) {
+        uint32_t dv[32];
+        ptx::tmem_ld32(t_dp + 32 * q, dv);
+        ptx::tmem_wait_ld();
+        uint32_t dk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float2 pp = unpack2<kBF16>(pk[q][e]);
+          dk[e] = ptx::pack2<kBF16>(pp.x * (__uint_as_float(dv[2 * e]) - dlt),
+                                    pp.y * (__uint_as_float(dv[2 * e + 1]) - dlt));
+        }
+        ptx::tmem_st16(t_dp + 16 * q, dk);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar_ds);
+      ++s;
+    }
+    if (ok && s > 0) {
+      ok = __all_sync(0xffffffffu, wait_bounded(bar_acc, 0, abort_flag, p, 4));
+      if (ok) {
+        ptx::tc_fence_after();
+        store_row<D, kBF16>(tmem + lane_off + 3 * kT, p.scale,
+                            static_cast<uint16_t*>(p.dq) + grow * D, row_ok);
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace attn

@@ -35,6 +35,7 @@
 #include <cstdint>
 #include <cuda.h>
 
+#include "attn_sync.cuh"
 #include "sm103_ptx.cuh"
 
 namespace attn {
@@ -139,36 +140,6 @@ __device__ __forceinline__ TileKeys tile_keys(const FwdParams& p, int m0) {
     k.wl = (max(0, pos_last - p.window + 1) + cfg::kTN - 1) / cfg::kTN;
   }
   return k;
-}
-
-// Bounded wait.  Returns false if the CTA is aborting or the wait ran out.
-// After one immediate test the thread sleeps in try_wait (woken when the
-// phase completes, or after at most 20 us), so waiting warps do not take
-// issue slots from the working ones; abort flag and clock are checked
-// between sleeps.
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
-                                             volatile int* abort_flag,
-                                             const FwdParams& p, int role) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = ptx::globaltimer_ns();
-  while (true) {
-    if (ptx::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-    if (*abort_flag) return false;
-    if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
-      *abort_flag = 1;
-      atomicOr(p.status, 1u | (static_cast<unsigned>(role) << 8));
-      return false;
-    }
-  }
-}
-
-// Wait used while tearing down after an abort: ignores the abort flag.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity,
-                                           const FwdParams& p) {
-  const uint64_t t0 = ptx::globaltimer_ns();
-  while (!ptx::mbar_try_wait(bar, parity)) {
-    if (ptx::globaltimer_ns() - t0 > p.timeout_ns) return;
-  }
 }
 
 // One work unit: two 128-row Q tiles.  With an even GQA group the tiles

@@ -114,3 +114,14 @@ def make_qkv(w: Workload, seed: int = 0, device="cpu"):
     if device != "cpu":
         q, k, v = q.to(device), k.to(device), v.to(device)
     return q, k, v
+
+
+def make_do(w: Workload, seed: int = 0, device="cpu"):
+    """Upstream gradient dO [B, Hq, Sq, D] for the backward pass: float32
+    N(0, 1) from its own seeded CPU generator (seed + 1000003, so it never
+    repeats Q), rounded to the workload's dtype."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed) + 1000003)
+    do = torch.randn((w.B, w.Hq, w.Sq, w.D), generator=g,
+                     dtype=torch.float32).to(w.torch_dtype)
+    return do.to(device) if device != "cpu" else do

@@ -550,6 +550,87 @@ def run_window(args):
         print(json.dumps(out), flush=True)
 
 
+# -------------------------------------------------------------- backward
+def run_bwd(args):
+    """Backward pass (dQ, dK, dV) of the GQA 8k causal workload: the row
+    pass, the dK/dV kernel and the dQ kernel of one attn_bwd call per step,
+    inputs (Q, K, V, O, LSE, dO) resident, L2 flushed between steps.
+    FLOPs: 2.5x the forward's causal-halved count (five tile products per
+    visible score where the forward has two; this implementation computes
+    seven, recomputing S and dP in both kernels, which is not counted)."""
+    import torch
+
+    import attention_attn_fwd_gb300 as attn
+    from attention_attn_fwd_gb300.inputs import GQA_8K, make_do, make_qkv
+
+    ws, rank, local = dist_info()
+    if ws > 1:
+        torch.cuda.set_device(local)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = GQA_8K
+    q, k, v = (t.to(dev) for t in make_qkv(w, seed=0))
+    do = make_do(w, seed=0).to(dev)
+    o, lse = attn.fwd(q, k, v, scale=w.scale, causal=True)
+    dq, dk, dv = (torch.empty_like(t) for t in (q, k, v))
+    ws_bytes = attn.attn_bwd_workspace_bytes(w.B, w.Hq, w.Sq)
+    work = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    dt = attn.ATTN_BF16
+
+    def step():
+        st = attn.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                           o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                           dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B,
+                           w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.scale, 1, 0, 0,
+                           dt, work.data_ptr(), ws_bytes, stream.cuda_stream)
+        if st != attn.ATTN_OK:
+            raise RuntimeError("attn_bwd: " + attn.attn_status_string(st))
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(dev.index) as clocks:
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    st, code = attn.attn_device_status()
+    if st != attn.ATTN_OK:
+        raise RuntimeError("device status %d code %#x" % (st, code))
+    ms = sum(s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)) / args.steps
+    flops = 2.5 * w.flops()
+    tflops = flops / (ms * 1e-3) / 1e12
+    peak, _, src = peaks()
+    out = {
+        "metric": "attention bwd TFLOPS (2.5x forward causal-halved FLOPs)",
+        "value": round(tflops, 1), "unit": "TFLOPS", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic: Q/K/V/dO ~ N(0,1) from seeded CPU generators",
+        "config": config_dict(w, {
+            "pass": "backward (dQ, dK, dV)",
+            "bwd_flops_per_step": flops,
+            "kernels_per_step": 3,
+            "l2": "flushed between timed steps (256 MiB write, untimed)"}),
+        "roofline": {"bound": "tensor", "achieved": round(tflops, 1),
+                     "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(tflops / peak, 4),
+                     "peak_source": "%s bf16 dense burst (cuBLAS)" % src,
+                     "traffic": None},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -559,11 +640,13 @@ def main():
     ap.add_argument("--cpu-s", type=float, default=15.0,
                     help="CPU-oracle baseline budget in seconds")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["gqa8k", "decode", "window"],
+    ap.add_argument("--workload",
+                    choices=["gqa8k", "decode", "window", "bwd"],
                     default="gqa8k",
                     help="gqa8k: the headline causal GQA forward (default); "
                          "decode: the split-KV decode step; window: causal "
-                         "GQA 32k with a 4096-key sliding window")
+                         "GQA 32k with a 4096-key sliding window; bwd: the "
+                         "backward pass of gqa8k")
     ap.add_argument("--splits", type=int, default=0,
                     help="split count for --workload decode (0: automatic)")
     args = ap.parse_args()
@@ -575,6 +658,8 @@ def main():
         run_decode(args)
     elif args.workload == "window":
         run_window(args)
+    elif args.workload == "bwd":
+        run_bwd(args)
     else:
         run_ours(args)
 

@@ -191,6 +191,45 @@ attn_status_t attn_fwd_splitkv_noalloc(const void* Q, const void* K,
 /* Bytes of the fixed scratch array attn_fwd_splitkv_noalloc uses. */
 size_t attn_noalloc_scratch_bytes(void);
 
+/*
+ * attn_bwd — backward pass: gradients dQ, dK, dV of the forward output O
+ * for an upstream gradient dO.  "Flash Attention from Scratch", section
+ * "What's Next", lists the backward pass as future work without formulas;
+ * this is the chain rule on the forward's definition, recomputing P tile
+ * by tile from the forward's LSE instead of storing it:
+ *   P_ij = exp(scale q_i.k_j - LSE_i) on visible keys (0 elsewhere),
+ *   D_i = sum_d dO_id O_id,  dV_j = sum_i P_ij dO_i,
+ *   dS_ij = P_ij (dO_i.v_j - D_i),
+ *   dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i,
+ * with the query heads of a GQA group adding into the same dK, dV.
+ *
+ * Q, K, V, O, dO   device, same dtype and layouts as attn_fwd (O and LSE
+ *                  are the forward's outputs for these Q, K, V and scale,
+ *                  causal, input_pos, window);
+ * LSE              device fp32 [B, Hq, Sq] (required);
+ * dQ               device [B, Hq, Sq, D]; dK, dV device [B, Hkv, Skv, D];
+ *                  outputs, same dtype, 16-byte aligned, overlapping no
+ *                  input, each other or the workspace;
+ * window           as attn_fwd_window (0: none);
+ * workspace        device, 256-byte aligned, at least
+ *                  attn_bwd_workspace_bytes(B, Hq, Sq) bytes (per-row
+ *                  lse2 and D); contents need no initialisation;
+ * Three kernels are enqueued on `stream` (row pass, dK/dV, dQ); every
+ * output element has one writer, so results are deterministic.  Sq = 0
+ * writes zero dK, dV.  Errors as attn_fwd.
+ */
+attn_status_t attn_bwd(const void* Q, const void* K, const void* V,
+                       const void* O, const float* LSE, const void* dO,
+                       void* dQ, void* dK, void* dV, int B, int Hq, int Hkv,
+                       int Sq, int Skv, int D, float scale, int causal,
+                       int input_pos, int window, attn_dtype_t dtype,
+                       void* workspace, size_t workspace_bytes,
+                       attn_stream_t stream);
+
+/* Workspace bytes attn_bwd needs for B x Hq x Sq query rows: two fp32
+ * values per row, Sq padded to a multiple of 128 (0 on negative sizes). */
+size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq);
+
 /* Short English description of a status code (static storage). */
 const char* attn_status_string(attn_status_t status);
 

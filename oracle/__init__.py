@@ -58,6 +58,10 @@ class Oracle:
                                         L, L, L, ctypes.c_double,
                                         ctypes.c_int, L, L]
         lib.attn_oracle_bwd.restype = ctypes.c_int
+        lib.attn_oracle_bwd_dq_rows.argtypes = [
+            dp, dp, dp, dp, L, L, L, L, L, L, ctypes.c_double, ctypes.c_int,
+            L, L, ctypes.POINTER(ctypes.c_int64), L, dp]
+        lib.attn_oracle_bwd_dq_rows.restype = ctypes.c_int
         lib.attn_oracle_threads.argtypes = []
         lib.attn_oracle_threads.restype = ctypes.c_int
         self._lib = lib
@@ -129,6 +133,23 @@ class Oracle:
             raise ValueError("oracle rejected the arguments (code %d)" % rc)
         return dq, dk, dv
 
+    def backward_dq_rows(self, q, k, v, do, scale, causal, input_pos, rows,
+                         window=0):
+        """dQ of rows (b, h, i) given as an (n, 3) int array: [n, D]."""
+        q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+        B, Hq, Hkv, Sq, Skv, D = _shapes(q, k, v)
+        rows = np.ascontiguousarray(
+            np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+        n = rows.shape[0]
+        dq = np.zeros((n, D), np.float64)
+        rc = self._lib.attn_oracle_bwd_dq_rows(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(do), B, Hq, Hkv, Sq, Skv, D,
+            float(scale), int(bool(causal)), int(input_pos), int(window),
+            rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n, _ptr(dq))
+        if rc != 0:
+            raise ValueError("oracle rejected the arguments (code %d)" % rc)
+        return dq
+
     def threads(self) -> int:
         """Number of OpenMP threads the oracle's loops use."""
         return int(self._lib.attn_oracle_threads())
@@ -160,6 +181,11 @@ def prob_row(q, k, v, scale, causal, input_pos, b, h, i, window=0):
 
 def backward(q, k, v, do, scale, causal=False, input_pos=0, window=0):
     return default().backward(q, k, v, do, scale, causal, input_pos, window)
+
+
+def backward_dq_rows(q, k, v, do, scale, causal, input_pos, rows, window=0):
+    return default().backward_dq_rows(q, k, v, do, scale, causal, input_pos,
+                                      rows, window)
 
 
 def threads() -> int:

@@ -317,6 +317,69 @@ int attn_oracle_bwd(const double* Q, const double* K, const double* V,
   return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
 }
 
+/*
+ * dQ of selected query rows only (the same chain rule as attn_oracle_bwd,
+ * which needs every row for dK and dV; a query row's dQ needs only its own
+ * P and dP rows).  rows_bhi holds n triplets (b, h, i); dQ_rows[r*D ..).
+ */
+int attn_oracle_bwd_dq_rows(const double* Q, const double* K, const double* V,
+                            const double* dO, long B, long Hq, long Hkv,
+                            long Sq, long Skv, long D, double scale, int causal,
+                            long input_pos, long window,
+                            const int64_t* rows_bhi, long n, double* dQ_rows) {
+  if (!check_shape(B, Hq, Hkv, Sq, Skv, D, causal, input_pos, window))
+    return ORACLE_BAD_ARG;
+  for (long r = 0; r < n; ++r) {
+    const int64_t b = rows_bhi[3 * r], h = rows_bhi[3 * r + 1],
+                  i = rows_bhi[3 * r + 2];
+    if (b < 0 || b >= B || h < 0 || h >= Hq || i < 0 || i >= Sq)
+      return ORACLE_BAD_ARG;
+  }
+  const long group = Hq / Hkv;
+  int failed = 0;
+#pragma omp parallel
+  {
+    double* score = (double*)malloc(sizeof(double) * (size_t)Skv);
+    double* prob = (double*)malloc(sizeof(double) * (size_t)Skv);
+    double* out = (double*)malloc(sizeof(double) * (size_t)D);
+    if (!score || !prob || !out) {
+#pragma omp atomic write
+      failed = 1;
+    } else {
+#pragma omp for schedule(dynamic, 4)
+      for (long r = 0; r < n; ++r) {
+        const long b = rows_bhi[3 * r], h = rows_bhi[3 * r + 1],
+                   i = rows_bhi[3 * r + 2];
+        const double* k = K + (b * Hkv + h / group) * Skv * D;
+        const double* v = V + (b * Hkv + h / group) * Skv * D;
+        const double* dout = dO + ((b * Hq + h) * Sq + i) * D;
+        double lse;
+        oracle_row(Q, K, V, Hq, Hkv, Sq, Skv, D, scale, causal, input_pos,
+                   window, b, h, i, score, prob, out, &lse);
+        /* score[] is free now: reuse it for dP_ij = dO_i . V_j. */
+        double pdp = 0.0;
+        for (long j = 0; j < Skv; ++j) {
+          double dot = 0.0;
+          for (long d = 0; d < D; ++d) dot += dout[d] * v[j * D + d];
+          score[j] = dot;
+          pdp += prob[j] * dot;
+        }
+        double* dq = dQ_rows + r * D;
+        for (long d = 0; d < D; ++d) dq[d] = 0.0;
+        for (long j = 0; j < Skv; ++j) {
+          if (prob[j] == 0.0) continue;
+          const double ds = prob[j] * (score[j] - pdp);
+          for (long d = 0; d < D; ++d) dq[d] += scale * ds * k[j * D + d];
+        }
+      }
+    }
+    free(score);
+    free(prob);
+    free(out);
+  }
+  return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
+}
+
 /* Threads the parallel loops will use. */
 int attn_oracle_threads(void) {
 #ifdef _OPENMP

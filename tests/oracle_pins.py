@@ -358,6 +358,13 @@ def pin_bwd_torch_autograd(orc):
         for name, a_, b_ in zip(("dQ", "dK", "dV"), got, ref):
             np.testing.assert_allclose(a_, b_, rtol=0, atol=1e-12,
                                        err_msg=name)
+        # The row-sampled dQ against the same library gradient.
+        rows = np.array([(bb, h, i) for bb in range(B) for h in range(Hq)
+                         for i in range(0, Sq, 2)])
+        dq_rows = orc.backward_dq_rows(q, k, v, do, 0.45, causal, pos, rows, W)
+        np.testing.assert_allclose(dq_rows, ref[0][rows[:, 0], rows[:, 1],
+                                                   rows[:, 2]],
+                                   rtol=0, atol=1e-12, err_msg="dQ rows")
 
 
 def pin_bwd_finite_differences(orc):

@@ -49,6 +49,9 @@ MUTANTS = {
                        "dv[j * D + d] += ds * dout[d];"),
     "bwd_dp_uses_k": ("dot += dout[d] * v[j * D + d];",
                       "dot += dout[d] * k[j * D + d];"),
+    "bwd_rows_rowsum_dropped": (
+        "const double ds = prob[j] * (score[j] - pdp);",
+        "const double ds = prob[j] * score[j];"),
 }
 
 
