@@ -20,10 +20,12 @@
 // atomics would need 5), so every output has a single writer and the result
 // is deterministic.
 //
-// Roles (256 threads): warp 0 TMEM allocator and tcgen05.mma issuer, warp 1
-// TMA producer, warps 4-7 the element-wise work (one TMEM lane = one row
-// per thread) and the epilogue; warps 2-3 idle.  Every mbarrier wait is
-// bounded as in the forward kernel.
+// Roles (384 threads): warp 0 TMEM allocator and tcgen05.mma issuer, warp 1
+// TMA producer, warps 4-11 the element-wise work and the epilogue -- two
+// warpgroups on the same TMEM rows (one row per thread), each taking 64 of
+// a tile's 128 columns, so that two warps per scheduler hide each other's
+// latencies; warps 2-3 idle.  Every mbarrier wait is bounded as in the
+// forward kernel.
 #pragma once
 
 #include <cstdint>
@@ -58,10 +60,11 @@ struct BwdParams {
 
 namespace bwd {
 constexpr int kT = 128;        // rows per query / key tile
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr int kMmaWarp = 0;
 constexpr int kLoadWarp = 1;
-constexpr int kWorkWarp0 = 4;  // warps 4-7
+constexpr int kWorkWarp0 = 4;  // warps 4-11: two warpgroups
+constexpr int kWork = 256;     // element-wise threads
 constexpr int kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 }  // namespace bwd
@@ -207,8 +210,8 @@ struct DkdvLayout : BwdTiles<D> {
   static constexpr int kDoOff = kQOff + kQSlots * T::kTileBytes;
   static constexpr int kBarOff = kDoOff + kDoSlots * T::kTileBytes;
   // kv_full, q_full[QS], q_empty[QS], do_full[DS], do_empty[DS], s_ready,
-  // dp_ready, p_ready, ds_ready, acc_done, drain
-  static constexpr int kNumBars = 1 + 2 * kQSlots + 2 * kDoSlots + 6;
+  // dp_ready, p_ready, ds_ready, acc_done, drain, xa, xb
+  static constexpr int kNumBars = 1 + 2 * kQSlots + 2 * kDoSlots + 8;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -224,8 +227,8 @@ struct DqLayout : BwdTiles<D> {
   static constexpr int kRingOff = 2 * T::kTileBytes;
   static constexpr int kBarOff = kRingOff + kSlots * T::kTileBytes;
   // q_full, full[S], empty[S], s_ready[2], dp_ready, ds_ready, acc_done,
-  // drain
-  static constexpr int kNumBars = 1 + 2 * kSlots + 6;
+  // drain, x
+  static constexpr int kNumBars = 1 + 2 * kSlots + 7;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -240,6 +243,30 @@ __device__ __forceinline__ void store_row(uint32_t t_acc, float mul,
   uint4* out = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int q = 0; q < D / 32; ++q) {
+    uint32_t a[32];
+    ptx::tmem_ld32(t_acc + 32 * q, a);
+    ptx::tmem_wait_ld();
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        w[e] = ptx::pack2<kBF16>(__uint_as_float(a[8 * v + 2 * e]) * mul,
+                                 __uint_as_float(a[8 * v + 2 * e + 1]) * mul);
+      if (store) out[4 * q + v] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+// Stores kCols columns (fp32 in TMEM at t_acc, times `mul`) of a 16-bit
+// output row at dst; `store` false reads TMEM only (every lane of the warp
+// takes part in tcgen05.ld).
+template <int kCols, bool kBF16>
+__device__ __forceinline__ void store_cols(uint32_t t_acc, float mul,
+                                           uint16_t* dst, bool store) {
+  uint4* out = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < kCols / 32; ++q) {
     uint32_t a[32];
     ptx::tmem_ld32(t_acc + 32 * q, a);
     ptx::tmem_wait_ld();
@@ -295,6 +322,8 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
   const uint32_t bar_ds = bar_p + 8;
   const uint32_t bar_acc = bar_ds + 8;
   const uint32_t bar_drain = bar_acc + 8;
+  const uint32_t bar_xa = bar_drain + 8;  // both halves loaded S^T
+  const uint32_t bar_xb = bar_xa + 8;     // both halves loaded dP^T
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<int*>(smem + L::kMiscOff + 4);
 
@@ -310,7 +339,9 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumBars; ++i) {
       const uint32_t bar = bar0 + 8 * i;
-      ptx::mbar_init(bar, (bar == bar_p || bar == bar_ds) ? kT : 1);
+      const bool work = bar == bar_p || bar == bar_ds || bar == bar_xa ||
+                        bar == bar_xb;
+      ptx::mbar_init(bar, work ? kWork : 1);
     }
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -491,7 +522,11 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     __syncwarp();
   } else if (warp >= kWorkWarp0) {
     // ----------------------------------------- P^T, dS^T and epilogue
-    const int r = threadIdx.x - kWorkWarp0 * 32;  // key row in the tile
+    // Half h takes query columns [64h, 64h+64) of its key row.  A half's
+    // 16-bit stores land on fp32 columns the other half reads, so each pass
+    // loads all it needs, the halves meet on an mbarrier, then store.
+    const int h = (warp - kWorkWarp0) / 4;
+    const int r = (warp % 4) * 32 + lane;  // key row in the tile
     const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const uint32_t t_st = tmem + lane_off;
     const uint32_t t_dpt = tmem + lane_off + kT;
@@ -518,9 +553,10 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
                       wait_bounded(bar_s, s & 1, abort_flag, p, 3));
       if (!ok) break;
       ptx::tc_fence_after();
-      uint32_t pk[kT / 32][16];
+      uint32_t pk[32];
 #pragma unroll
-      for (int q = 0; q < kT / 32; ++q) {
+      for (int k = 0; k < 2; ++k) {
+        const int q = 2 * h + k;
         uint32_t sv[32];
         ptx::tmem_ld32(t_st + 32 * q, sv);
         float lv[32];
@@ -543,11 +579,16 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
             if (static_cast<unsigned>(j - jlo) >= span) x0 = -INFINITY;
             if (static_cast<unsigned>(j + 1 - jlo) >= span) x1 = -INFINITY;
           }
-          pk[q][e] = ptx::pack2<kBF16>(ptx::ex2(x0), ptx::ex2(x1));
+          pk[16 * k + e] = ptx::pack2<kBF16>(ptx::ex2(x0), ptx::ex2(x1));
         }
-        // 16-bit P^T over fp32 columns already consumed.
-        ptx::tmem_st16(t_st + 16 * q, pk[q]);
       }
+      ptx::mbar_arrive(bar_xa);
+      ok = __all_sync(0xffffffffu,
+                      wait_bounded(bar_xa, s & 1, abort_flag, p, 3));
+      if (!ok) break;
+      // 16-bit P^T of query columns 64h.. into TMEM columns 32h..
+      ptx::tmem_st16(t_st + 32 * h, pk);
+      ptx::tmem_st16(t_st + 32 * h + 16, pk + 16);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar_p);
@@ -556,8 +597,10 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
                       wait_bounded(bar_dp, s & 1, abort_flag, p, 3));
       if (!ok) break;
       ptx::tc_fence_after();
+      uint32_t dk[32];
 #pragma unroll
-      for (int q = 0; q < kT / 32; ++q) {
+      for (int k = 0; k < 2; ++k) {
+        const int q = 2 * h + k;
         uint32_t dv[32];
         ptx::tmem_ld32(t_dpt + 32 * q, dv);
         float dl[32];
@@ -570,43 +613,42 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
           dl[4 * i + 3] = t4.w;
         }
         ptx::tmem_wait_ld();
-        uint32_t dk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float2 pp = unpack2<kBF16>(pk[q][e]);
-          dk[e] = ptx::pack2<kBF16>(
+          const float2 pp = unpack2<kBF16>(pk[16 * k + e]);
+          dk[16 * k + e] = ptx::pack2<kBF16>(
               pp.x * (__uint_as_float(dv[2 * e]) - dl[2 * e]),
               pp.y * (__uint_as_float(dv[2 * e + 1]) - dl[2 * e + 1]));
         }
-        ptx::tmem_st16(t_dpt + 16 * q, dk);
       }
+      ptx::mbar_arrive(bar_xb);
+      ok = __all_sync(0xffffffffu,
+                      wait_bounded(bar_xb, s & 1, abort_flag, p, 3));
+      if (!ok) break;
+      ptx::tmem_st16(t_dpt + 32 * h, dk);
+      ptx::tmem_st16(t_dpt + 32 * h + 16, dk + 16);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar_ds);
       ++s;
     }
     if (ok) {
-      // Epilogue: dV and scale * dK rows (keys past Skv are not stored; a
-      // key tile no query sees gets zeros).
+      // Epilogue: half 0 writes the dV row, half 1 the scale * dK row
+      // (keys past Skv are not stored; a key tile no query sees gets zeros).
       const long long row = static_cast<long long>(bk) * p.Skv + key;
       const bool in = key < p.Skv;
-      uint16_t* dvr = static_cast<uint16_t*>(p.dv) + row * D;
-      uint16_t* dkr = static_cast<uint16_t*>(p.dk) + row * D;
+      uint16_t* dst = static_cast<uint16_t*>(h ? p.dk : p.dv) + row * D;
       if (s > 0) {
         ok = __all_sync(0xffffffffu,
                         wait_bounded(bar_acc, 0, abort_flag, p, 4));
         if (ok) {
           ptx::tc_fence_after();
-          store_row<D, kBF16>(tmem + lane_off + 2 * kT, 1.f, dvr, in);
-          store_row<D, kBF16>(tmem + lane_off + 2 * kT + D, p.scale, dkr, in);
+          store_cols<D, kBF16>(tmem + lane_off + 2 * kT + h * D,
+                               h ? p.scale : 1.f, dst, in);
         }
       } else if (in) {
-        uint4* a = reinterpret_cast<uint4*>(dvr);
-        uint4* k4 = reinterpret_cast<uint4*>(dkr);
-        for (int i = 0; i < D / 8; ++i) {
-          a[i] = make_uint4(0u, 0u, 0u, 0u);
-          k4[i] = make_uint4(0u, 0u, 0u, 0u);
-        }
+        uint4* z = reinterpret_cast<uint4*>(dst);
+        for (int i = 0; i < D / 8; ++i) z[i] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
   }
@@ -653,6 +695,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
   const uint32_t bar_ds = bar_dp + 8;
   const uint32_t bar_acc = bar_ds + 8;
   const uint32_t bar_drain = bar_acc + 8;
+  const uint32_t bar_x = bar_drain + 8;  // both halves loaded dP
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<int*>(smem + L::kMiscOff + 4);
 
@@ -666,7 +709,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumBars; ++i) {
       const uint32_t bar = bar0 + 8 * i;
-      ptx::mbar_init(bar, bar == bar_ds ? kT : 1);
+      ptx::mbar_init(bar, (bar == bar_ds || bar == bar_x) ? kWork : 1);
     }
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -821,7 +864,11 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     __syncwarp();
   } else if (warp >= kWorkWarp0) {
     // -------------------------------------------- dS and the epilogue
-    const int r = threadIdx.x - kWorkWarp0 * 32;  // query row in the tile
+    // Half h takes key columns [64h, 64h+64) of its query row; the 16-bit
+    // dS stores land on fp32 dP columns the other half reads, so the halves
+    // meet on an mbarrier between loading dP and storing dS.
+    const int h = (warp - kWorkWarp0) / 4;
+    const int r = (warp % 4) * 32 + lane;  // query row in the tile
     const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const uint32_t t_dp = tmem + lane_off + 2 * kT;
     const int q_row = m * kT + r;
@@ -853,9 +900,10 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       if (!ok) break;
       ptx::tc_fence_after();
       const uint32_t t_s = tmem + lane_off + (s & 1) * kT;
-      uint32_t pk[kT / 32][16];
+      uint32_t pk[32];
 #pragma unroll
-      for (int q = 0; q < kT / 32; ++q) {
+      for (int kh = 0; kh < 2; ++kh) {
+        const int q = 2 * h + kh;
         uint32_t sv[32];
         ptx::tmem_ld32(t_s + 32 * q, sv);
         ptx::tmem_wait_ld();
@@ -869,7 +917,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
             if (static_cast<unsigned>(k - lo) >= span) x0 = -INFINITY;
             if (static_cast<unsigned>(k + 1 - lo) >= span) x1 = -INFINITY;
           }
-          pk[q][e] = ptx::pack2<kBF16>(ptx::ex2(x0), ptx::ex2(x1));
+          pk[16 * kh + e] = ptx::pack2<kBF16>(ptx::ex2(x0), ptx::ex2(x1));
         }
       }
       // dS = P (dP - D), 16-bit, over dP.
@@ -877,20 +925,27 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
                       wait_bounded(bar_dp, s & 1, abort_flag, p, 3));
       if (!ok) break;
       ptx::tc_fence_after();
+      uint32_t dk[32];
 #pragma unroll
-      for (int q = 0; q < kT / 32; ++q) {
+      for (int kh = 0; kh < 2; ++kh) {
+        const int q = 2 * h + kh;
         uint32_t dv[32];
         ptx::tmem_ld32(t_dp + 32 * q, dv);
         ptx::tmem_wait_ld();
-        uint32_t dk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float2 pp = unpack2<kBF16>(pk[q][e]);
-          dk[e] = ptx::pack2<kBF16>(pp.x * (__uint_as_float(dv[2 * e]) - dlt),
-                                    pp.y * (__uint_as_float(dv[2 * e + 1]) - dlt));
+          const float2 pp = unpack2<kBF16>(pk[16 * kh + e]);
+          dk[16 * kh + e] =
+              ptx::pack2<kBF16>(pp.x * (__uint_as_float(dv[2 * e]) - dlt),
+                                pp.y * (__uint_as_float(dv[2 * e + 1]) - dlt));
         }
-        ptx::tmem_st16(t_dp + 16 * q, dk);
       }
+      ptx::mbar_arrive(bar_x);
+      ok = __all_sync(0xffffffffu,
+                      wait_bounded(bar_x, s & 1, abort_flag, p, 3));
+      if (!ok) break;
+      ptx::tmem_st16(t_dp + 32 * h, dk);
+      ptx::tmem_st16(t_dp + 32 * h + 16, dk + 16);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar_ds);
@@ -899,9 +954,11 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     if (ok && s > 0) {
       ok = __all_sync(0xffffffffu, wait_bounded(bar_acc, 0, abort_flag, p, 4));
       if (ok) {
+        // Half h writes columns [h*D/2, (h+1)*D/2) of the scale * dQ row.
         ptx::tc_fence_after();
-        store_row<D, kBF16>(tmem + lane_off + 3 * kT, p.scale,
-                            static_cast<uint16_t*>(p.dq) + grow * D, row_ok);
+        store_cols<D / 2, kBF16>(
+            tmem + lane_off + 3 * kT + h * (D / 2), p.scale,
+            static_cast<uint16_t*>(p.dq) + grow * D + h * (D / 2), row_ok);
       }
     }
   }
