@@ -217,11 +217,13 @@ struct DkdvLayout : BwdTiles<D> {
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 };
 
-// dQ kernel: Q and dO resident, a ring of K / V tiles.
+// dQ kernel: Q and dO resident, a ring of K / V tiles.  At step s the MMA
+// issuer wants V(s+1) and K(s+2); with 5 slots (D=128) both copies can
+// start a full step earlier than that (with 4, K(s+2) waited for dQ(s)).
 template <int D>
 struct DqLayout : BwdTiles<D> {
   using T = BwdTiles<D>;
-  static constexpr int kSlots = (D == 128) ? 4 : 8;
+  static constexpr int kSlots = (D == 128) ? 5 : 8;
   static constexpr int kQOff = 0;
   static constexpr int kDoOff = T::kTileBytes;
   static constexpr int kRingOff = 2 * T::kTileBytes;
