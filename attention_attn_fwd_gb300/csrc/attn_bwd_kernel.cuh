@@ -63,6 +63,7 @@ constexpr int kT = 128;        // rows per query / key tile
 constexpr int kThreads = 384;
 constexpr int kMmaWarp = 0;
 constexpr int kLoadWarp = 1;
+constexpr int kVecWarp = 2;    // dK/dV kernel: stages the per-step vectors
 constexpr int kWorkWarp0 = 4;  // warps 4-11: two warpgroups
 constexpr int kWork = 256;     // element-wise threads
 constexpr int kTmemCols = 512;
@@ -208,10 +209,14 @@ struct DkdvLayout : BwdTiles<D> {
   static constexpr int kVOff = T::kTileBytes;
   static constexpr int kQOff = 2 * T::kTileBytes;
   static constexpr int kDoOff = kQOff + kQSlots * T::kTileBytes;
-  static constexpr int kBarOff = kDoOff + kDoSlots * T::kTileBytes;
+  // lse2 and D of the current step's 128 query rows (1 KB, staged one step
+  // ahead by its own warp: read from L2 inside the element-wise passes their
+  // latency sat on the critical path).
+  static constexpr int kVecOff = kDoOff + kDoSlots * T::kTileBytes;
+  static constexpr int kBarOff = kVecOff + 2 * bwd::kT * 4;
   // kv_full, q_full[QS], q_empty[QS], do_full[DS], do_empty[DS], s_ready,
-  // dp_ready, p_ready, ds_ready, acc_done, drain, xa, xb
-  static constexpr int kNumBars = 1 + 2 * kQSlots + 2 * kDoSlots + 8;
+  // dp_ready, p_ready, ds_ready, acc_done, drain, xa, xb, vec_full, vec_free
+  static constexpr int kNumBars = 1 + 2 * kQSlots + 2 * kDoSlots + 10;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -326,6 +331,9 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
   const uint32_t bar_drain = bar_acc + 8;
   const uint32_t bar_xa = bar_drain + 8;  // both halves loaded S^T
   const uint32_t bar_xb = bar_xa + 8;     // both halves loaded dP^T
+  const uint32_t bar_vf = bar_xb + 8;     // step vectors staged
+  const uint32_t bar_ve = bar_vf + 8;     // step vectors consumed
+  float* vec = reinterpret_cast<float*>(smem + L::kVecOff);  // lse2, D
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<int*>(smem + L::kMiscOff + 4);
 
@@ -342,7 +350,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     for (int i = 0; i < L::kNumBars; ++i) {
       const uint32_t bar = bar0 + 8 * i;
       const bool work = bar == bar_p || bar == bar_ds || bar == bar_xa ||
-                        bar == bar_xb;
+                        bar == bar_xb || bar == bar_ve;
       ptx::mbar_init(bar, work ? kWork : 1);
     }
     *abort_flag = 0;
@@ -416,6 +424,31 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
         drain_wait(bar_df + 8 * (i % L::kDoSlots), (i / L::kDoSlots) & 1, p);
     }
     __syncwarp();
+  } else if (warp == kVecWarp) {
+    // ------------------------------------------- per-step vector staging
+    // lse2 and D of step s's 128 query rows into shared memory, once the
+    // element-wise warps are done with step s-1's (padded arrays: no
+    // bounds checks).
+    bool ok = true;
+    int s = 0;
+    for (int hm = 0; hm < steps_all && ok; ++hm) {
+      const int m = hm % p.q_tiles;
+      if (!pair_visible(p, m, n)) continue;
+      if (s > 0) {
+        ok = __all_sync(0xffffffffu,
+                        wait_bounded(bar_ve, (s - 1) & 1, abort_flag, p, 5));
+        if (!ok) break;
+      }
+      const long long vbase =
+          static_cast<long long>(qplane0 + hm / p.q_tiles) * p.sq_pad + m * kT;
+      const float4 l4 = reinterpret_cast<const float4*>(p.lse2 + vbase)[lane];
+      const float4 d4 = reinterpret_cast<const float4*>(p.delta + vbase)[lane];
+      reinterpret_cast<float4*>(vec)[lane] = l4;
+      reinterpret_cast<float4*>(vec + kT)[lane] = d4;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar_vf);
+      ++s;
+    }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------ MMA issuer
     constexpr uint32_t kHi = ptx::sdesc_hi_sw128(1024);
@@ -539,11 +572,9 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     for (int hm = 0; hm < steps_all && ok; ++hm) {
       const int m = hm % p.q_tiles;
       if (!pair_visible(p, m, n)) continue;
-      // lse2 / D of the tile's 128 query rows (padded arrays: no checks).
-      const long long vbase =
-          static_cast<long long>(qplane0 + hm / p.q_tiles) * p.sq_pad + m * kT;
-      const float4* v_l = reinterpret_cast<const float4*>(p.lse2 + vbase);
-      const float4* v_d = reinterpret_cast<const float4*>(p.delta + vbase);
+      // lse2 / D of the tile's 128 query rows, staged in shared memory.
+      const float4* v_l = reinterpret_cast<const float4*>(vec);
+      const float4* v_d = reinterpret_cast<const float4*>(vec + kT);
       // Query column j (position input_pos + m*128 + j) sees this key iff
       // j >= jlo and, with a window, j < jlo + window.
       const bool full = pair_full(p, m, n);
@@ -553,6 +584,9 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       // P^T = 2^(S^T c - lse2), kept in registers (16-bit) for dS.
       ok = __all_sync(0xffffffffu,
                       wait_bounded(bar_s, s & 1, abort_flag, p, 3));
+      if (ok)
+        ok = __all_sync(0xffffffffu,
+                        wait_bounded(bar_vf, s & 1, abort_flag, p, 3));
       if (!ok) break;
       ptx::tc_fence_after();
       uint32_t pk[32];
@@ -564,7 +598,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
         float lv[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float4 t4 = __ldg(v_l + 8 * q + i);
+          const float4 t4 = v_l[8 * q + i];
           lv[4 * i] = t4.x;
           lv[4 * i + 1] = t4.y;
           lv[4 * i + 2] = t4.z;
@@ -608,7 +642,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
         float dl[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float4 t4 = __ldg(v_d + 8 * q + i);
+          const float4 t4 = v_d[8 * q + i];
           dl[4 * i] = t4.x;
           dl[4 * i + 1] = t4.y;
           dl[4 * i + 2] = t4.z;
@@ -623,6 +657,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
               pp.y * (__uint_as_float(dv[2 * e + 1]) - dl[2 * e + 1]));
         }
       }
+      ptx::mbar_arrive(bar_ve);  // done with this step's vectors
       ptx::mbar_arrive(bar_xb);
       ok = __all_sync(0xffffffffu,
                       wait_bounded(bar_xb, s & 1, abort_flag, p, 3));
