@@ -142,6 +142,28 @@ def workload():
     return GQA_8K
 
 
+def max_over_ranks(values, device="cpu"):
+    """Element-wise max of a list of floats over all ranks of the default
+    process group (the values unchanged without one or with one rank).  The
+    path shards into independent replicas, so timing is the slowest rank's
+    and this is the only collective."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or \
+            dist.get_world_size() == 1:
+        return [float(x) for x in values]
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64,
+                     device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def whole_job_rate(units_per_rank, ms, world):
+    """Units per second of the whole job: `world` replicas each process
+    `units_per_rank` units in `ms` milliseconds (the max over ranks)."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def config_dict(w, extra=None):
     d = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq,
          "Skv": w.Skv, "D": w.D, "causal": w.causal,
@@ -271,14 +293,11 @@ def run_ours(args):
     e2e_launches = args.steps
 
     # Max over ranks.
-    if ws > 1:
-        t = torch.tensor([kernel_ms, e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        kernel_ms, e2e_ms = float(t[0]), float(t[1])
+    kernel_ms, e2e_ms = max_over_ranks([kernel_ms, e2e_ms], dev)
 
     flops = w.flops()
-    value = ws * flops / (kernel_ms * 1e-3) / 1e12
-    e2e_value = ws * flops / (e2e_ms * 1e-3) / 1e12
+    value = whole_job_rate(flops, kernel_ms, ws) / 1e12
+    e2e_value = whole_job_rate(flops, e2e_ms, ws) / 1e12
     peak_tf, _, peak_src = peaks()
     achieved = flops / (kernel_ms * 1e-3) / 1e12  # one launch, one GPU
     out = {
