@@ -32,7 +32,7 @@ def _rank(rank, world, port, out):
 def test_max_over_ranks_two_gloo_ranks():
     world = 2
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.start_processes(_rank, args=(world, port, out), nprocs=world,
                            start_method="spawn", join=True)
