@@ -222,20 +222,24 @@ struct DkdvLayout : BwdTiles<D> {
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 };
 
-// dQ kernel: Q and dO resident, a ring of K / V tiles.  At step s the MMA
-// issuer wants V(s+1) and K(s+2); with 5 slots (D=128) both copies can
-// start a full step earlier than that (with 4, K(s+2) waited for dQ(s)).
+// dQ kernel: Q and dO resident, separate rings of K and V tiles.  K(s) is
+// held from S(s) (issued two steps ahead) until dQ(s), V(s) only for dP(s);
+// in one shared ring the late release of K(s-1) held back the copy of
+// V(s+1).  At step s the MMA issuer wants V(s+1) and K(s+2): 3 K + 2 V
+// slots (D=128) give both copies a step or more of lead.
 template <int D>
 struct DqLayout : BwdTiles<D> {
   using T = BwdTiles<D>;
-  static constexpr int kSlots = (D == 128) ? 5 : 8;
+  static constexpr int kKSlots = (D == 128) ? 3 : 4;
+  static constexpr int kVSlots = (D == 128) ? 2 : 4;
   static constexpr int kQOff = 0;
   static constexpr int kDoOff = T::kTileBytes;
-  static constexpr int kRingOff = 2 * T::kTileBytes;
-  static constexpr int kBarOff = kRingOff + kSlots * T::kTileBytes;
-  // q_full, full[S], empty[S], s_ready[2], dp_ready, ds_ready, acc_done,
-  // drain, x
-  static constexpr int kNumBars = 1 + 2 * kSlots + 7;
+  static constexpr int kKOff = 2 * T::kTileBytes;
+  static constexpr int kVOff = kKOff + kKSlots * T::kTileBytes;
+  static constexpr int kBarOff = kVOff + kVSlots * T::kTileBytes;
+  // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_ready[2],
+  // dp_ready, ds_ready, acc_done, drain, x
+  static constexpr int kNumBars = 1 + 2 * kKSlots + 2 * kVSlots + 7;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -722,12 +726,15 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
   const uint32_t s_base = ptx::smem_u32(smem);
   const uint32_t s_q = s_base + L::kQOff;
   const uint32_t s_do = s_base + L::kDoOff;
-  const uint32_t s_ring = s_base + L::kRingOff;
+  const uint32_t s_kr = s_base + L::kKOff;  // K ring
+  const uint32_t s_vr = s_base + L::kVOff;  // V ring
   const uint32_t bar0 = s_base + L::kBarOff;
   const uint32_t bar_q = bar0;
-  const uint32_t bar_full = bar0 + 8;
-  const uint32_t bar_empty = bar_full + 8 * L::kSlots;
-  const uint32_t bar_s = bar_empty + 8 * L::kSlots;  // [2], per S buffer
+  const uint32_t bar_kf = bar0 + 8;                    // [kKSlots]
+  const uint32_t bar_ke = bar_kf + 8 * L::kKSlots;     // [kKSlots]
+  const uint32_t bar_vf = bar_ke + 8 * L::kKSlots;     // [kVSlots]
+  const uint32_t bar_ve = bar_vf + 8 * L::kVSlots;     // [kVSlots]
+  const uint32_t bar_s = bar_ve + 8 * L::kVSlots;  // [2], per S buffer
   const uint32_t bar_dp = bar_s + 16;
   const uint32_t bar_ds = bar_dp + 8;
   const uint32_t bar_acc = bar_ds + 8;
@@ -776,30 +783,45 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
                              m * kT, qplane);
     }
     bool ok = true;
-    int it = 0;  // ring items K_0, V_0, K_1, ... issued
+    int nk = 0, nv = 0;  // K / V copies issued (step index of the next)
     for (int n = 0; n < p.k_tiles && ok; ++n) {
       if (!pair_visible(p, m, n)) continue;
-      for (int kv = 0; kv < 2; ++kv) {
-        const int slot = it % L::kSlots;
-        if (it >= L::kSlots) {
-          ok = __all_sync(0xffffffffu,
-                          wait_bounded(bar_empty + 8 * slot,
-                                       ((it / L::kSlots) - 1) & 1, abort_flag,
-                                       p, 1));
-          if (!ok) break;
-        }
-        const uint32_t dst = s_ring + slot * L::kTileBytes;
-        ptx::mbar_arrive_expect_tx_elect(bar_full + 8 * slot, L::kTileBytes);
-        for (int c = 0; c < L::kChunks; ++c)
-          ptx::tma_load_3d_elect(dst + c * L::kBoxBytes, kv ? &tm_v : &tm_k,
-                                 bar_full + 8 * slot, c * 64, n * kT, kvplane);
-        ++it;
+      const int ks = nk % L::kKSlots;
+      if (nk >= L::kKSlots) {
+        ok = __all_sync(0xffffffffu,
+                        wait_bounded(bar_ke + 8 * ks,
+                                     ((nk / L::kKSlots) - 1) & 1, abort_flag,
+                                     p, 1));
+        if (!ok) break;
       }
+      ptx::mbar_arrive_expect_tx_elect(bar_kf + 8 * ks, L::kTileBytes);
+      for (int c = 0; c < L::kChunks; ++c)
+        ptx::tma_load_3d_elect(s_kr + ks * L::kTileBytes + c * L::kBoxBytes,
+                               &tm_k, bar_kf + 8 * ks, c * 64, n * kT,
+                               kvplane);
+      ++nk;
+      const int vs = nv % L::kVSlots;
+      if (nv >= L::kVSlots) {
+        ok = __all_sync(0xffffffffu,
+                        wait_bounded(bar_ve + 8 * vs,
+                                     ((nv / L::kVSlots) - 1) & 1, abort_flag,
+                                     p, 1));
+        if (!ok) break;
+      }
+      ptx::mbar_arrive_expect_tx_elect(bar_vf + 8 * vs, L::kTileBytes);
+      for (int c = 0; c < L::kChunks; ++c)
+        ptx::tma_load_3d_elect(s_vr + vs * L::kTileBytes + c * L::kBoxBytes,
+                               &tm_v, bar_vf + 8 * vs, c * 64, n * kT,
+                               kvplane);
+      ++nv;
     }
     if (!ok) {
+      // Let every copy still in flight land before the CTA goes away.
       drain_wait(bar_q, 0, p);
-      for (int i = max(0, it - L::kSlots); i < it; ++i)
-        drain_wait(bar_full + 8 * (i % L::kSlots), (i / L::kSlots) & 1, p);
+      for (int i = max(0, nk - L::kKSlots); i < nk; ++i)
+        drain_wait(bar_kf + 8 * (i % L::kKSlots), (i / L::kKSlots) & 1, p);
+      for (int i = max(0, nv - L::kVSlots); i < nv; ++i)
+        drain_wait(bar_vf + 8 * (i % L::kVSlots), (i / L::kVSlots) & 1, p);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -812,13 +834,23 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     const uint32_t t_dp = tmem + 2 * kT, t_dq = tmem + 3 * kT;
     const uint32_t q_lo = ptx::sdesc_lo(s_q, 16);
     const uint32_t do_lo = ptx::sdesc_lo(s_do, 16);
-    // Ring item `it` (K_s = 2s, V_s = 2s+1) landed.
-    auto wait_item = [&](int it) {
+    // K(s) / V(s) landed, and their tiles.
+    auto wait_k = [&](int s) {
       return __all_sync(0xffffffffu,
-                        wait_bounded(bar_full + 8 * (it % L::kSlots),
-                                     (it / L::kSlots) & 1, abort_flag, p, 2));
+                        wait_bounded(bar_kf + 8 * (s % L::kKSlots),
+                                     (s / L::kKSlots) & 1, abort_flag, p, 2));
     };
-    auto tile = [&](int it) { return s_ring + (it % L::kSlots) * L::kTileBytes; };
+    auto wait_v = [&](int s) {
+      return __all_sync(0xffffffffu,
+                        wait_bounded(bar_vf + 8 * (s % L::kVSlots),
+                                     (s / L::kVSlots) & 1, abort_flag, p, 2));
+    };
+    auto k_tile = [&](int s) {
+      return s_kr + (s % L::kKSlots) * L::kTileBytes;
+    };
+    auto v_tile = [&](int s) {
+      return s_vr + (s % L::kVSlots) * L::kTileBytes;
+    };
     // d = A B^T with A, B K-major 128 x D tiles (S = Q K^T, dP = dO V^T).
     auto issue_nt = [&](uint32_t d, uint32_t a_lo, uint32_t b_lo,
                         uint32_t idesc) {
@@ -836,21 +868,21 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     const int n1 = n0 < p.k_tiles ? next_key_tile(p, m, n0 + 1) : p.k_tiles;
     // Prologue: S(0), dP(0), S(1).
     if (ok && n0 < p.k_tiles) {
-      ok = wait_item(0) && wait_item(1);
+      ok = wait_k(0) && wait_v(0);
       if (ok) {
         ptx::tc_fence_after();
-        issue_nt(tmem, q_lo, ptx::sdesc_lo(tile(0), 16), idesc_s);
+        issue_nt(tmem, q_lo, ptx::sdesc_lo(k_tile(0), 16), idesc_s);
         ptx::tc_commit_elect(bar_s);
-        issue_nt(t_dp, do_lo, ptx::sdesc_lo(tile(1), 16), idesc_dp);
+        issue_nt(t_dp, do_lo, ptx::sdesc_lo(v_tile(0), 16), idesc_dp);
         ptx::tc_commit_elect(bar_dp);
-        ptx::tc_commit_elect(bar_empty + 8 * (1 % L::kSlots));
+        ptx::tc_commit_elect(bar_ve);  // V(0) slot
         issued = true;
       }
       if (ok && n1 < p.k_tiles) {
-        ok = wait_item(2);
+        ok = wait_k(1);
         if (ok) {
           ptx::tc_fence_after();
-          issue_nt(tmem + kT, q_lo, ptx::sdesc_lo(tile(2), 16), idesc_s);
+          issue_nt(tmem + kT, q_lo, ptx::sdesc_lo(k_tile(1), 16), idesc_s);
           ptx::tc_commit_elect(bar_s + 8);
         }
       }
@@ -865,27 +897,27 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
                       wait_bounded(bar_ds, s & 1, abort_flag, p, 2));
       if (!ok) break;
       ptx::tc_fence_after();
-      const uint32_t k_mn = ptx::sdesc_lo(tile(2 * s), L::kBoxBytes);
+      const uint32_t k_mn = ptx::sdesc_lo(k_tile(s), L::kBoxBytes);
 #pragma unroll
       for (int kk = 0; kk < kT / 16; ++kk)
         ptx::mma_ts_elect(t_dq, t_dp + kk * 8, k_mn + ((kk * 16 * 128) >> 4),
                           kHi, idesc_acc, (s > 0 || kk > 0) ? 1u : 0u);
-      ptx::tc_commit_elect(bar_empty + 8 * ((2 * s) % L::kSlots));
+      ptx::tc_commit_elect(bar_ke + 8 * (s % L::kKSlots));
       // dP(s+1) into the dP region (after dQ(s) in issue order).
       if (n_next < p.k_tiles) {
-        ok = wait_item(2 * s + 3);
+        ok = wait_v(s + 1);
         if (!ok) break;
         ptx::tc_fence_after();
-        issue_nt(t_dp, do_lo, ptx::sdesc_lo(tile(2 * s + 3), 16), idesc_dp);
+        issue_nt(t_dp, do_lo, ptx::sdesc_lo(v_tile(s + 1), 16), idesc_dp);
         ptx::tc_commit_elect(bar_dp);
-        ptx::tc_commit_elect(bar_empty + 8 * ((2 * s + 3) % L::kSlots));
+        ptx::tc_commit_elect(bar_ve + 8 * ((s + 1) % L::kVSlots));
       }
       // S(s+2) into S buffer s % 2, free since step s's pass is done.
       if (n_after < p.k_tiles) {
-        ok = wait_item(2 * s + 4);
+        ok = wait_k(s + 2);
         if (!ok) break;
         ptx::tc_fence_after();
-        issue_nt(tmem + (s & 1) * kT, q_lo, ptx::sdesc_lo(tile(2 * s + 4), 16),
+        issue_nt(tmem + (s & 1) * kT, q_lo, ptx::sdesc_lo(k_tile(s + 2), 16),
                  idesc_s);
         ptx::tc_commit_elect(bar_s + 8 * (s & 1));
       }
