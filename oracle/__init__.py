@@ -15,10 +15,20 @@ from .build import LIB, build_oracle
 
 
 def _f64(x):
-    """Exact widening of a torch tensor / numpy array to contiguous float64."""
-    if hasattr(x, "detach"):  # torch tensor, any dtype/device
+    """Exact widening of a torch tensor / numpy array to contiguous float64.
+
+    FP8 tensors are refused: they are widened by ``decode_e4m3`` (the
+    oracle's own decoder), never by a library conversion."""
+    if hasattr(x, "detach"):  # torch tensor, any 16/32/64-bit float dtype
+        if x.element_size() == 1:
+            raise TypeError("8-bit tensor: widen it with decode_e4m3")
         x = x.detach().to("cpu").double().numpy()
     return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def torch_uint8():
+    import torch
+    return torch.uint8
 
 
 def _ptr(a):
@@ -62,6 +72,9 @@ class Oracle:
             dp, dp, dp, dp, L, L, L, L, L, L, ctypes.c_double, ctypes.c_int,
             L, L, ctypes.POINTER(ctypes.c_int64), L, dp]
         lib.attn_oracle_bwd_dq_rows.restype = ctypes.c_int
+        lib.attn_oracle_decode_e4m3.argtypes = [
+            ctypes.POINTER(ctypes.c_uint8), L, ctypes.c_double, dp]
+        lib.attn_oracle_decode_e4m3.restype = ctypes.c_int
         lib.attn_oracle_threads.argtypes = []
         lib.attn_oracle_threads.restype = ctypes.c_int
         self._lib = lib
@@ -150,6 +163,22 @@ class Oracle:
             raise ValueError("oracle rejected the arguments (code %d)" % rc)
         return dq
 
+    def decode_e4m3(self, x8, descale=1.0):
+        """E4M3 codes (a torch float8_e4m3fn / uint8 tensor or a uint8
+        array) times ``descale``, as a float64 array of the same shape."""
+        if hasattr(x8, "detach"):
+            if x8.element_size() != 1:
+                raise TypeError("expected an 8-bit tensor")
+            x8 = x8.detach().to("cpu").contiguous().view(torch_uint8()).numpy()
+        codes = np.ascontiguousarray(np.asarray(x8, dtype=np.uint8))
+        out = np.zeros(codes.shape, np.float64)
+        rc = self._lib.attn_oracle_decode_e4m3(
+            codes.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)), codes.size,
+            float(descale), _ptr(out))
+        if rc != 0:
+            raise ValueError("oracle rejected the arguments (code %d)" % rc)
+        return out
+
     def threads(self) -> int:
         """Number of OpenMP threads the oracle's loops use."""
         return int(self._lib.attn_oracle_threads())
@@ -186,6 +215,10 @@ def backward(q, k, v, do, scale, causal=False, input_pos=0, window=0):
 def backward_dq_rows(q, k, v, do, scale, causal, input_pos, rows, window=0):
     return default().backward_dq_rows(q, k, v, do, scale, causal, input_pos,
                                       rows, window)
+
+
+def decode_e4m3(x8, descale=1.0):
+    return default().decode_e4m3(x8, descale)
 
 
 def threads() -> int:

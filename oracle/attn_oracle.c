@@ -380,6 +380,43 @@ int attn_oracle_bwd_dq_rows(const double* Q, const double* K, const double* V,
   return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
 }
 
+/*
+ * FP8 inputs.  "Flash Attention from Scratch", section "What's Next", names
+ * FP8 tensor cores as future work and defines no format; the reading taken
+ * is the 8-bit E4M3 format of the OCP "8-bit Floating Point Specification"
+ * (the "e4m3fn" variant the GPU tensor cores consume), with one fp32
+ * descale factor per tensor:  Q = q_descale * decode(Q8), and so on.  The
+ * attention itself is then the definition above, in double.
+ *
+ * E4M3 bit fields: sign s (bit 7), exponent e (bits 3-6, bias 7), mantissa
+ * m (bits 0-2).
+ *   e == 0:            (-1)^s * m * 2^-9            (subnormal, incl. +-0)
+ *   e == 15, m == 7:   NaN                          (no infinities)
+ *   otherwise:         (-1)^s * (8 + m) * 2^(e-10)   (= 2^(e-7) * (1 + m/8))
+ * Every value is exact in double.
+ */
+double attn_oracle_e4m3_value(unsigned int code) {
+  const unsigned int s = (code >> 7) & 1u;
+  const unsigned int e = (code >> 3) & 15u;
+  const unsigned int m = code & 7u;
+  double v;
+  if (e == 15u && m == 7u) return NAN;
+  if (e == 0u)
+    v = ldexp((double)m, -9);
+  else
+    v = ldexp((double)(8u + m), (int)e - 10);
+  return s ? -v : v;
+}
+
+/* out[i] = scale * decode(in[i]); the product of a 4-bit significand and
+ * an fp32 descale is exact in double. */
+int attn_oracle_decode_e4m3(const uint8_t* in, long n, double scale,
+                            double* out) {
+  if (n < 0 || (n > 0 && (in == NULL || out == NULL))) return ORACLE_BAD_ARG;
+  for (long i = 0; i < n; ++i) out[i] = scale * attn_oracle_e4m3_value(in[i]);
+  return ORACLE_OK;
+}
+
 /* Threads the parallel loops will use. */
 int attn_oracle_threads(void) {
 #ifdef _OPENMP

@@ -405,6 +405,89 @@ def pin_bwd_single_key(orc):
     np.testing.assert_allclose(dv[:, :, 0], want, rtol=0, atol=1e-12)
 
 
+# FP8 (E4M3) inputs: the oracle's own decoder, then the definition above.
+
+# Codes and values fixed by the E4M3 bit layout (sign | 4-bit exponent,
+# bias 7 | 3-bit mantissa; exponent 0 subnormal; S.1111.111 NaN).
+_E4M3_HAND = {
+    0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6,
+    0x30: 0.5, 0x38: 1.0, 0x3C: 1.5, 0x40: 2.0, 0x44: 3.0, 0x77: 240.0,
+    0x78: 256.0, 0x7E: 448.0, 0x81: -(2.0 ** -9), 0xB8: -1.0, 0xFE: -448.0,
+}
+
+
+def pin_e4m3_closed_forms(orc):
+    """Values of hand-picked codes, signed zero, the two NaN codes, and
+    the ordering of the positive codes."""
+    codes = np.arange(256, dtype=np.uint8)
+    vals = orc.decode_e4m3(codes)
+    for c, want in _E4M3_HAND.items():
+        assert vals[c] == want, (hex(c), vals[c], want)
+    assert vals[0x80] == 0.0 and math.copysign(1.0, vals[0x80]) < 0
+    assert math.isnan(vals[0x7F]) and math.isnan(vals[0xFF])
+    assert int(np.isnan(vals).sum()) == 2
+    assert np.all(np.diff(vals[:0x7F]) > 0)          # 0x00 .. 0x7E ascend
+    np.testing.assert_array_equal(vals[0x80:0xFF], -vals[:0x7F])
+    half = orc.decode_e4m3(np.array([0x38, 0x40, 0x01], np.uint8), 0.375)
+    np.testing.assert_array_equal(half, [0.375, 0.75, 0.375 * 2.0 ** -9])
+
+
+def pin_e4m3_torch(orc):
+    """Every code against torch's float8_e4m3fn conversion (library)."""
+    codes = torch.arange(256, dtype=torch.uint8)
+    want = codes.view(torch.float8_e4m3fn).double().numpy()
+    got = orc.decode_e4m3(codes.numpy())
+    np.testing.assert_array_equal(got, want)
+
+
+def _e4m3(shape, rng):
+    """Random E4M3 codes of N(0, 1) draws (torch's rounding), uint8."""
+    x = torch.from_numpy(_rand(shape, rng).astype(np.float32))
+    return x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def pin_fp8_attention_sdpa(orc):
+    """Decoded E4M3 inputs with descale factors, through the oracle, against
+    torch float64 scaled_dot_product_attention on torch-decoded inputs times
+    the same factors; the V factor scales O and leaves LSE alone."""
+    rng = np.random.default_rng(41)
+    B, Hq, Hkv, Sq, Skv, D = 1, 4, 2, 9, 13, 16
+    q8, k8, v8 = (_e4m3((B, Hq, Sq, D), rng), _e4m3((B, Hkv, Skv, D), rng),
+                  _e4m3((B, Hkv, Skv, D), rng))
+    qd, kd, vd, scale = 0.75, 1.25, 0.5, 0.3
+    for causal, pos, window in ((False, 0, 0), (True, 3, 0), (True, 4, 5)):
+        o, lse = orc.attention(orc.decode_e4m3(q8, qd),
+                               orc.decode_e4m3(k8, kd),
+                               orc.decode_e4m3(v8, vd), scale, causal, pos,
+                               window)
+
+        def lib(c, f):
+            return (torch.from_numpy(c).view(torch.float8_e4m3fn).double()
+                    * f)
+        q, k, v = lib(q8, qd), lib(k8, kd), lib(v8, vd)
+        k = k.repeat_interleave(Hq // Hkv, dim=1)
+        v = v.repeat_interleave(Hq // Hkv, dim=1)
+        s = scale * q @ k.transpose(-1, -2)
+        mask = torch.ones(Sq, Skv, dtype=torch.bool)
+        if causal:
+            i = torch.arange(Sq)[:, None] + pos
+            j = torch.arange(Skv)[None, :]
+            mask = j <= i
+            if window:
+                mask &= j > i - window
+        s = s.masked_fill(~mask, float("-inf"))
+        want_o = torch.softmax(s, dim=-1) @ v
+        want_lse = torch.logsumexp(s, dim=-1)
+        np.testing.assert_allclose(o, want_o.numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse, want_lse.numpy(), rtol=0, atol=1e-12)
+        o1, lse1 = orc.attention(orc.decode_e4m3(q8, qd),
+                                 orc.decode_e4m3(k8, kd),
+                                 orc.decode_e4m3(v8, 1.0), scale, causal,
+                                 pos, window)
+        np.testing.assert_allclose(o, vd * o1, rtol=0, atol=1e-12)
+        np.testing.assert_array_equal(lse, lse1)
+
+
 ALL_PINS = [
     pin_hand_cases, pin_single_key, pin_uniform_scores, pin_prob_rows,
     pin_gqa_equivalence, pin_causal_first_row, pin_permutation_invariance,
@@ -412,4 +495,5 @@ ALL_PINS = [
     pin_torch_sdpa, pin_window_single_key, pin_window_uniform_scores,
     pin_window_wide_is_causal, pin_window_decode_slice,
     pin_bwd_torch_autograd, pin_bwd_finite_differences, pin_bwd_single_key,
+    pin_e4m3_closed_forms, pin_e4m3_torch, pin_fp8_attention_sdpa,
 ]

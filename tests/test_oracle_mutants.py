@@ -52,6 +52,18 @@ MUTANTS = {
     "bwd_rows_rowsum_dropped": (
         "const double ds = prob[j] * (score[j] - pdp);",
         "const double ds = prob[j] * score[j];"),
+    "e4m3_bias_8": ("ldexp((double)(8u + m), (int)e - 10)",
+                    "ldexp((double)(8u + m), (int)e - 11)"),
+    "e4m3_no_implicit_bit": ("ldexp((double)(8u + m), (int)e - 10)",
+                             "ldexp((double)(m), (int)e - 7)"),
+    "e4m3_subnormal_as_normal": ("if (e == 0u)\n    v = ldexp((double)m, -9);",
+                                 "if (0)\n    v = ldexp((double)m, -9);"),
+    "e4m3_sign_dropped": ("return s ? -v : v;", "return v;"),
+    "e4m3_nan_whole_binade": ("if (e == 15u && m == 7u) return NAN;",
+                              "if (e == 15u) return NAN;"),
+    "e4m3_descale_dropped": (
+        "out[i] = scale * attn_oracle_e4m3_value(in[i]);",
+        "out[i] = attn_oracle_e4m3_value(in[i]);"),
 }
 
 
