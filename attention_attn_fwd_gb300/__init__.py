@@ -15,17 +15,19 @@ import os
 import threading
 
 __all__ = [
-    "ATTN_F16", "ATTN_BF16", "AttnError", "attn_fwd", "attn_fwd_window",
+    "ATTN_F16", "ATTN_BF16", "ATTN_E4M3", "AttnError", "attn_fwd",
+    "attn_fwd_window", "attn_fwd_fp8",
     "attn_fwd_splitkv", "attn_fwd_splitkv_window",
     "attn_splitkv_plan", "attn_fwd_splitkv_noalloc",
     "attn_noalloc_scratch_bytes", "attn_status_string", "attn_device_status",
     "attn_tile_config", "attn_version", "attn_bwd", "attn_bwd_workspace_bytes",
-    "fwd", "fwd_splitkv", "bwd",
+    "fwd", "fwd_splitkv", "fwd_fp8", "bwd",
     "library_path", "load_library",
 ]
 
 ATTN_F16 = 0
 ATTN_BF16 = 1
+ATTN_E4M3 = 2
 
 ATTN_OK = 0
 ATTN_ERR_INVALID_ARG = 1
@@ -102,6 +104,10 @@ def load_library():
         lib.attn_bwd.restype = i
         lib.attn_bwd_workspace_bytes.argtypes = [i, i, i]
         lib.attn_bwd_workspace_bytes.restype = sz
+        f = ctypes.c_float
+        lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i,
+                                     f, f, f, f, i, i, i, i, vp, sz, vp]
+        lib.attn_fwd_fp8.restype = i
         lib.attn_noalloc_scratch_bytes.argtypes = []
         lib.attn_noalloc_scratch_bytes.restype = sz
         _lib = lib
@@ -124,6 +130,18 @@ def attn_fwd_window(Q, K, V, O, LSE, B, Hq, Hkv, Sq, Skv, D, scale, causal,
         Q or None, K or None, V or None, O or None, LSE or None, B, Hq, Hkv,
         Sq, Skv, D, float(scale), int(causal), int(input_pos), int(window),
         int(dtype), stream or None))
+
+
+def attn_fwd_fp8(Q, K, V, O, LSE, B, Hq, Hkv, Sq, Skv, D, scale, q_descale,
+                 k_descale, v_descale, causal, input_pos, window, num_splits,
+                 workspace, workspace_bytes, stream) -> int:
+    """Raw C-ABI call with E4M3 inputs and a bfloat16 O."""
+    return int(load_library().attn_fwd_fp8(
+        Q or None, K or None, V or None, O or None, LSE or None, B, Hq, Hkv,
+        Sq, Skv, D, float(scale), float(q_descale), float(k_descale),
+        float(v_descale), int(causal), int(input_pos), int(window),
+        int(num_splits), workspace or None, int(workspace_bytes),
+        stream or None))
 
 
 def attn_fwd_splitkv_window(Q, K, V, O, LSE, B, Hq, Hkv, Sq, Skv, D, scale,
@@ -333,6 +351,62 @@ def fwd_splitkv(q, k, v, scale=None, causal=True, input_pos=0, num_splits=0,
                 scale, causal, input_pos, dt, *ws_args)
     if st != ATTN_OK:
         raise AttnError("attn_fwd_splitkv: " + attn_status_string(st), st)
+    return out, (lse if need_lse else None)
+
+
+def fwd_fp8(q, k, v, scale=None, q_descale=1.0, k_descale=1.0,
+            v_descale=1.0, causal=True, input_pos=0, window=0, num_splits=0,
+            workspace=None, out=None, lse=None, need_lse=True, stream=None):
+    """Attention forward on E4M3 CUDA tensors (torch.float8_e4m3fn, or
+    uint8 holding the codes): q [B, Hq, Sq, 128], k and v [B, Hkv, Skv,
+    128].  The real inputs are the codes times the per-tensor descale
+    factors.  Returns (O bfloat16, LSE float32 or None).  ``num_splits``
+    0: one pass; > 0 (or -1 to let the library choose): split-KV with a
+    ``workspace`` allocated with torch when not given.
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dim() != 4 or not t.is_cuda or not t.is_contiguous():
+            raise AttnError("%s must be a contiguous 4-D CUDA tensor" % name,
+                            ATTN_ERR_INVALID_ARG)
+        if t.element_size() != 1 or t.dtype not in (
+                getattr(torch, "float8_e4m3fn", None), torch.uint8):
+            raise AttnError("%s must hold E4M3 codes (float8_e4m3fn or "
+                            "uint8), got %s" % (name, t.dtype),
+                            ATTN_ERR_INVALID_ARG)
+    B, Hq, Sq, D = q.shape
+    Bk, Hkv, Skv, Dk = k.shape
+    if (Bk, Dk) != (B, D) or tuple(v.shape) != tuple(k.shape):
+        raise AttnError("inconsistent q/k/v shapes", ATTN_ERR_INVALID_ARG)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(q.device):
+        splits, ws_bytes = 0, 0
+        if num_splits:
+            splits, ws_bytes = attn_splitkv_plan(
+                B, Hq, Hkv, Sq, Skv, D, causal, input_pos, ATTN_E4M3,
+                max(num_splits, 0))
+            if workspace is None:
+                workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8,
+                                        device=q.device)
+        if out is None:
+            out = torch.empty((B, Hq, Sq, D), dtype=torch.bfloat16,
+                              device=q.device)
+        if need_lse and lse is None:
+            lse = torch.empty((B, Hq, Sq), dtype=torch.float32,
+                              device=q.device)
+        if stream is None:
+            stream = torch.cuda.current_stream(q.device)
+        ws_ptr = workspace.data_ptr() if workspace is not None else 0
+        ws_len = (workspace.numel() * workspace.element_size()
+                  if workspace is not None else 0)
+        st = attn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                          out.data_ptr(), lse.data_ptr() if need_lse else 0,
+                          B, Hq, Hkv, Sq, Skv, D, scale, q_descale, k_descale,
+                          v_descale, causal, input_pos, window, splits,
+                          ws_ptr, ws_len, stream.cuda_stream)
+    if st != ATTN_OK:
+        raise AttnError("attn_fwd_fp8: " + attn_status_string(st), st)
     return out, (lse if need_lse else None)
 
 

@@ -18,6 +18,7 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libattn_fwd_gb300.so")
 SOURCES = ["attn_api.cu", "attn_fwd_d64.cu", "attn_fwd_d128.cu",
            "attn_fwd_d64_packed.cu", "attn_fwd_d128_packed.cu",
+           "attn_fwd_d128_fp8.cu", "attn_fwd_d128_fp8_packed.cu",
            "attn_noalloc.cu", "attn_bwd.cu"]
 HEADERS = ["attn_fwd_kernel.cuh", "attn_fwd_launch.cuh", "attn_sync.cuh",
            "attn_bwd_kernel.cuh",

@@ -117,7 +117,8 @@ attn_status_t check_scalars(const Shape& s, float scale, attn_dtype_t dtype) {
       s.D <= 0 || s.input_pos < 0)
     return ATTN_ERR_INVALID_ARG;
   if (s.Hq % s.Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16 && dtype != ATTN_E4M3)
+    return ATTN_ERR_INVALID_ARG;
   // A window is defined for causal attention only, and every query row
   // must see a key: the last row (position input_pos + Sq - 1) sees keys
   // from input_pos + Sq - window on.
@@ -133,6 +134,7 @@ attn_status_t check_scalars(const Shape& s, float scale, attn_dtype_t dtype) {
   // Planes (B*H) index a 32-bit tensor-map dimension and kernel ints.
   if (static_cast<long long>(s.B) * s.Hq > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
   if (s.D != 64 && s.D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (dtype == ATTN_E4M3 && s.D != 128) return ATTN_ERR_UNSUPPORTED;
   if (grid_size(s) > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }
@@ -144,12 +146,16 @@ struct TileChoice {
   int block_m, block_n, stages, smem_bytes;
 };
 
-TileChoice choose_tiles(const Shape& s) {
+TileChoice choose_tiles(const Shape& s, attn_dtype_t dtype) {
   const bool pack = pack_gqa(s);
+  const bool fp8 = dtype == ATTN_E4M3;
   const int block_m = pack ? (s.Hq / s.Hkv) * s.Sq : attn::cfg::kBlockM;
-  return TileChoice{block_m, attn::cfg::kTN, attn::fwd_stages(s.D, pack),
-                    attn::fwd_smem_bytes(s.D, pack)};
+  return TileChoice{block_m, attn::cfg::kTN, attn::fwd_stages(s.D, pack, fp8),
+                    attn::fwd_smem_bytes(s.D, pack, fp8)};
 }
+
+// Bytes of one element of Q, K, V (the output O is 16-bit throughout).
+size_t elem_bytes(attn_dtype_t dtype) { return dtype == ATTN_E4M3 ? 1 : 2; }
 
 bool is_device_ptr(const void* p, int dev) {
   cudaPointerAttributes a{};
@@ -162,25 +168,30 @@ bool is_device_ptr(const void* p, int dev) {
   return a.device == dev;
 }
 
-// 3-D map (D, S, planes) of a [planes, S, D] tensor; boxes of 64 x box_rows
-// x box_planes elements with 128-byte swizzle.
+// 3-D map (D, S, planes) of a [planes, S, D] tensor; boxes of one 128-byte
+// row segment (64 16-bit or 128 8-bit elements) x box_rows x box_planes
+// with 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, attn_dtype_t dtype, int D,
               int S, long long planes, int box_rows = 128,
               int box_planes = 1) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
   if (enc == nullptr) return false;
+  const cuuint64_t es = elem_bytes(dtype);
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D),
                               static_cast<cuuint64_t>(S),
                               static_cast<cuuint64_t>(planes)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
-                                 static_cast<cuuint64_t>(S) * D * 2};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows),
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * es,
+                                 static_cast<cuuint64_t>(S) * D * es};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es),
+                             static_cast<cuuint32_t>(box_rows),
                              static_cast<cuuint32_t>(box_planes)};
   const cuuint32_t estride[3] = {1, 1, 1};
+  const CUtensorMapDataType type =
+      dtype == ATTN_E4M3   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+      : dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const CUresult r = enc(
-      m, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-      3, const_cast<void*>(base), dims, strides, box, estride,
+      m, type, 3, const_cast<void*>(base), dims, strides, box, estride,
       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -195,13 +206,19 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }  // namespace
 
 namespace attn {
-int fwd_smem_bytes(int D, bool pack) {
+int fwd_smem_bytes(int D, bool pack, bool fp8) {
+  if (fp8)
+    return pack ? Layout<128, true, true>::kSmemBytes
+                : Layout<128, false, true>::kSmemBytes;
   if (pack)
     return D == 64 ? Layout<64, true>::kSmemBytes : Layout<128, true>::kSmemBytes;
   return D == 64 ? Layout<64>::kSmemBytes : Layout<128>::kSmemBytes;
 }
-int fwd_stages(int D, bool pack) {
+int fwd_stages(int D, bool pack, bool fp8) {
   // Each slot holds one K or one V tile; a stage is a K and a V tile.
+  if (fp8)
+    return (pack ? Layout<128, true, true>::kSlots
+                 : Layout<128, false, true>::kSlots) / 2;
   if (pack) return (D == 64 ? Layout<64, true>::kSlots : Layout<128, true>::kSlots) / 2;
   return (D == 64 ? Layout<64>::kSlots : Layout<128>::kSlots) / 2;
 }
@@ -278,10 +295,12 @@ attn_status_t check_call(const Shape& s, float scale, attn_dtype_t dtype,
   if (misaligned(Q, 16) || misaligned(K, 16) || misaligned(V, 16) ||
       misaligned(O, 16) || (LSE != nullptr && misaligned(LSE, 4)))
     return ATTN_ERR_ALIGNMENT;
-  const size_t q_bytes = static_cast<size_t>(s.B) * s.Hq * s.Sq * s.D * 2;
-  const size_t kv_bytes = static_cast<size_t>(s.B) * s.Hkv * s.Skv * s.D * 2;
-  if (overlaps(O, q_bytes, Q, q_bytes) || overlaps(O, q_bytes, K, kv_bytes) ||
-      overlaps(O, q_bytes, V, kv_bytes))
+  const size_t es = elem_bytes(dtype);
+  const size_t o_bytes = static_cast<size_t>(s.B) * s.Hq * s.Sq * s.D * 2;
+  const size_t q_bytes = static_cast<size_t>(s.B) * s.Hq * s.Sq * s.D * es;
+  const size_t kv_bytes = static_cast<size_t>(s.B) * s.Hkv * s.Skv * s.D * es;
+  if (overlaps(O, o_bytes, Q, q_bytes) || overlaps(O, o_bytes, K, kv_bytes) ||
+      overlaps(O, o_bytes, V, kv_bytes))
     return ATTN_ERR_INVALID_ARG;
   if (cudaGetDevice(dev) != cudaSuccess) return ATTN_ERR_CUDA;
   if (!is_device_ptr(Q, *dev) || !is_device_ptr(K, *dev) ||
@@ -296,12 +315,14 @@ attn_status_t check_call(const Shape& s, float scale, attn_dtype_t dtype,
 }
 
 // Builds the tensor maps and parameters and launches the forward kernel.
+// `scale` is the score factor (FP8: times the Q and K descales), `o_scale`
+// multiplies O (FP8: the V descale; else 1).
 attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
                              const void* V, void* O, float* LSE, float scale,
                              attn_dtype_t dtype, unsigned int* status, int sms,
                              int splits, int split_tiles, float* o_part,
                              float* lse_part, unsigned long long* merge_ctr,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, float o_scale = 1.f) {
   CUtensorMap tq, tk, tv;
   const long long q_planes = static_cast<long long>(s.B) * s.Hq;
   const long long kv_planes = static_cast<long long>(s.B) * s.Hkv;
@@ -327,10 +348,12 @@ attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
   p.pair_heads = pair_heads(s);
   p.pack_gqa = pack;
   p.group = group;
-  // 128-byte rows: 128 per tile, or group*Sq packed, per 64-column box.
-  p.q_tile_bytes = (s.D / 64) * 128 * (pack ? group * s.Sq : attn::cfg::kTM);
+  // D * element-size bytes per row: 128 rows per tile, or group*Sq packed.
+  p.q_tile_bytes = static_cast<int>(s.D * elem_bytes(dtype)) *
+                   (pack ? group * s.Sq : attn::cfg::kTM);
   p.scale_log2 = std::fabs(scale) * 1.4426950408889634f;
   p.negate_scores = scale < 0.f;
+  p.o_scale = o_scale;
   p.o = O;
   p.lse = LSE;
   p.num_splits = splits;
@@ -347,7 +370,10 @@ attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
   const int grid = static_cast<int>(std::min<long long>(p.num_units, sms));
   const bool bf16 = dtype == ATTN_BF16;
   const cudaError_t err =
-      s.D == 64
+      dtype == ATTN_E4M3
+          ? (pack ? attn::launch_fwd_d128_fp8_packed(tq, tk, tv, p, grid, stream)
+                  : attn::launch_fwd_d128_fp8(tq, tk, tv, p, grid, stream))
+      : s.D == 64
           ? (pack ? attn::launch_fwd_d64_packed(bf16, tq, tk, tv, p, grid, stream)
                   : attn::launch_fwd_d64(bf16, tq, tk, tv, p, grid, stream))
           : (pack ? attn::launch_fwd_d128_packed(bf16, tq, tk, tv, p, grid, stream)
@@ -359,6 +385,8 @@ attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
 attn_status_t fwd_impl(const Shape& s, const void* Q, const void* K,
                        const void* V, void* O, float* LSE, float scale,
                        attn_dtype_t dtype, attn_stream_t stream) {
+  // E4M3 inputs need their descale factors: attn_fwd_fp8 only.
+  if (dtype == ATTN_E4M3) return ATTN_ERR_INVALID_ARG;
   attn_status_t st = check_scalars(s, scale, dtype);
   if (st != ATTN_OK) return st;
   if (s.B == 0 || s.Sq == 0) return ATTN_OK;
@@ -376,7 +404,8 @@ attn_status_t fwd_impl(const Shape& s, const void* Q, const void* K,
 attn_status_t splitkv_impl(const Shape& s, const void* Q, const void* K,
                            const void* V, void* O, float* LSE, float scale,
                            attn_dtype_t dtype, int num_splits, void* workspace,
-                           size_t workspace_bytes, attn_stream_t stream) {
+                           size_t workspace_bytes, attn_stream_t stream,
+                           float o_scale = 1.f) {
   attn_status_t st = check_scalars(s, scale, dtype);
   if (st != ATTN_OK) return st;
   if (s.B == 0 || s.Sq == 0) return ATTN_OK;
@@ -404,7 +433,37 @@ attn_status_t splitkv_impl(const Shape& s, const void* Q, const void* K,
       s, Q, K, V, O, LSE, scale, dtype, status, sms, splits, tiles,
       reinterpret_cast<float*>(ws), reinterpret_cast<float*>(ws + o_bytes),
       reinterpret_cast<unsigned long long*>(ws + o_bytes + lse_bytes),
-      reinterpret_cast<cudaStream_t>(stream));
+      reinterpret_cast<cudaStream_t>(stream), o_scale);
+}
+
+// attn_fwd_fp8: the descales fold into the score factor (Q, K) and into
+// the output factor (V); num_splits == 0 is the single-pass forward.
+attn_status_t fp8_impl(const Shape& s, const void* Q, const void* K,
+                       const void* V, void* O, float* LSE, float scale,
+                       float q_descale, float k_descale, float v_descale,
+                       int num_splits, void* workspace,
+                       size_t workspace_bytes, attn_stream_t stream) {
+  if (!std::isfinite(scale) || !std::isfinite(q_descale) ||
+      !std::isfinite(k_descale) || !std::isfinite(v_descale))
+    return ATTN_ERR_INVALID_ARG;
+  const double eff = static_cast<double>(scale) * q_descale * k_descale;
+  if (!(std::fabs(eff) <= 3.4e38)) return ATTN_ERR_INVALID_ARG;
+  const float s_eff = static_cast<float>(eff);
+  if (num_splits < 0) return ATTN_ERR_INVALID_ARG;
+  if (num_splits > 0)
+    return splitkv_impl(s, Q, K, V, O, LSE, s_eff, ATTN_E4M3, num_splits,
+                        workspace, workspace_bytes, stream, v_descale);
+  attn_status_t st = check_scalars(s, s_eff, ATTN_E4M3);
+  if (st != ATTN_OK) return st;
+  if (s.B == 0 || s.Sq == 0) return ATTN_OK;
+  int dev = 0, sms = 0;
+  unsigned int* status = nullptr;
+  st = check_call(s, s_eff, ATTN_E4M3, Q, K, V, O, LSE, &dev, &status, &sms);
+  if (st != ATTN_OK) return st;
+  const int tiles = (s.Skv + attn::cfg::kTN - 1) / attn::cfg::kTN;
+  return launch_forward(s, Q, K, V, O, LSE, s_eff, ATTN_E4M3, status, sms, 1,
+                        tiles, nullptr, nullptr, nullptr,
+                        reinterpret_cast<cudaStream_t>(stream), v_descale);
 }
 
 // Rows per (batch, query head) plane of the backward's per-row arrays:
@@ -425,6 +484,7 @@ attn_status_t bwd_impl(const Shape& s, const void* Q, const void* K,
                        const void* dO, void* dQ, void* dK, void* dV,
                        float scale, attn_dtype_t dtype, void* workspace,
                        size_t workspace_bytes, attn_stream_t stream) {
+  if (dtype == ATTN_E4M3) return ATTN_ERR_UNSUPPORTED;  // 16-bit only
   attn_status_t st = check_scalars(s, scale, dtype);
   if (st != ATTN_OK) return st;
   if (s.B == 0) return ATTN_OK;
@@ -576,6 +636,7 @@ attn_status_t attn_fwd_splitkv(const void* Q, const void* K, const void* V,
                                int num_splits, void* workspace,
                                size_t workspace_bytes, attn_stream_t stream) {
   const Shape s{B, Hq, Hkv, Sq, Skv, D, causal != 0, input_pos};
+  if (dtype == ATTN_E4M3) return ATTN_ERR_INVALID_ARG;  // attn_fwd_fp8
   return splitkv_impl(s, Q, K, V, O, LSE, scale, dtype, num_splits,
                       workspace, workspace_bytes, stream);
 }
@@ -589,8 +650,21 @@ attn_status_t attn_fwd_splitkv_window(const void* Q, const void* K,
                                       void* workspace, size_t workspace_bytes,
                                       attn_stream_t stream) {
   const Shape s{B, Hq, Hkv, Sq, Skv, D, causal != 0, input_pos, window};
+  if (dtype == ATTN_E4M3) return ATTN_ERR_INVALID_ARG;  // attn_fwd_fp8
   return splitkv_impl(s, Q, K, V, O, LSE, scale, dtype, num_splits,
                       workspace, workspace_bytes, stream);
+}
+
+attn_status_t attn_fwd_fp8(const void* Q, const void* K, const void* V,
+                           void* O, float* LSE, int B, int Hq, int Hkv,
+                           int Sq, int Skv, int D, float scale,
+                           float q_descale, float k_descale, float v_descale,
+                           int causal, int input_pos, int window,
+                           int num_splits, void* workspace,
+                           size_t workspace_bytes, attn_stream_t stream) {
+  const Shape s{B, Hq, Hkv, Sq, Skv, D, causal != 0, input_pos, window};
+  return fp8_impl(s, Q, K, V, O, LSE, scale, q_descale, k_descale, v_descale,
+                  num_splits, workspace, workspace_bytes, stream);
 }
 
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq) {
@@ -645,7 +719,7 @@ attn_status_t attn_tile_config(int B, int Hq, int Hkv, int Sq, int Skv, int D,
   const Shape s{B, Hq, Hkv, Sq, Skv, D, causal != 0, input_pos};
   const attn_status_t st = check_scalars(s, 1.0f, dtype);
   if (st != ATTN_OK) return st;
-  const TileChoice t = choose_tiles(s);
+  const TileChoice t = choose_tiles(s, dtype);
   if (block_m) *block_m = t.block_m;
   if (block_n) *block_n = t.block_n;
   if (stages) *stages = t.stages;

@@ -1,0 +1,15 @@
+// Head-dimension-128 packed-GQA instantiations (all query heads of a K/V
+// head in one tile) of the sm_103a forward kernel for E4M3 (FP8) inputs.
+#include "attn_fwd_launch.cuh"
+
+namespace attn {
+
+cudaError_t launch_fwd_d128_fp8_packed(const CUtensorMap& q,
+                                       const CUtensorMap& k,
+                                       const CUtensorMap& v,
+                                       const FwdParams& p, int grid,
+                                       cudaStream_t stream) {
+  return launch_mode<128, true, true>(true, q, k, v, p, grid, stream);
+}
+
+}  // namespace attn

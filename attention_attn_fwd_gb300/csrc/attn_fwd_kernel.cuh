@@ -55,6 +55,7 @@ struct FwdParams {
   int q_tile_bytes;        // bytes one Q tile load brings in
   float scale_log2;        // |scale| * log2(e)
   int negate_scores;       // scale < 0: S is computed as -(Q K^T)
+  float o_scale;           // multiplies O (FP8 inputs: the V descale; else 1)
   void* o;                 // [B, Hq, Sq, D] output (16-bit elements)
   float* lse;              // [B, Hq, Sq] or nullptr
   int num_units;           // work units (pairs of 128-row Q tiles x splits)
@@ -93,15 +94,20 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 // Shared memory of one CTA: Q tiles, the K/V slot ring, mbarriers.  The
 // packed variant has one Q tile and fills the rest of the 227 KB with ring
-// slots (a decode step is bound by the K/V bytes in flight per SM).
-template <int D, bool kPack = false>
+// slots (a decode step is bound by the K/V bytes in flight per SM).  Rows
+// are cut into 128-byte boxes (64 16-bit or 128 8-bit elements): an FP8
+// tile of D = 128 has the geometry of a 16-bit tile of D = 64.
+template <int D, bool kPack = false, bool kFp8 = false>
 struct Layout {
-  static constexpr int kChunks = D / 64;                 // 128-byte boxes/row
+  static constexpr int kEs = kFp8 ? 1 : 2;               // element bytes
+  static_assert((D * kEs) % 128 == 0, "rows of whole 128-byte boxes");
+  static constexpr int kChunks = D * kEs / 128;          // 128-byte boxes/row
+  static constexpr int kBoxElems = 128 / kEs;            // elements per box row
   static constexpr int kBoxBytes = 128 * 128;            // 128 rows x 128 B
   static constexpr int kTileBytes = kChunks * kBoxBytes; // one Q/K/V tile
   static constexpr int kQTiles = kPack ? 1 : 2;
   static constexpr int kSlots =                           // K/V ring slots
-      kPack ? (D == 128 ? 6 : 13) : (D == 128 ? 4 : 8);
+      kPack ? (kChunks == 2 ? 6 : 13) : (kChunks == 2 ? 4 : 8);
   static constexpr int kQOff = 0;
   static constexpr int kRingOff = kQOff + kQTiles * kTileBytes;
   static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
@@ -330,13 +336,19 @@ __device__ __forceinline__ int unit_index(int k, int cta, int ctas) {
 // The variants keep each launch's softmax loop free of the others' code:
 // in one kernel with run-time switches the two-tile loop ran out of
 // registers and lost 5-11 %.
-template <int D, bool kBF16, bool kPack, bool kSplit, bool kWindow>
+//
+// kFp8: Q, K, V in E4M3 (O in bf16, kBF16 set): both products run as
+// kind::f8f6f4 MMAs and P is rounded to E4M3 (four keys per TMEM column);
+// p.scale_log2 carries the Q and K descales, p.o_scale the V descale.
+template <int D, bool kBF16, bool kPack, bool kSplit, bool kWindow,
+          bool kFp8 = false>
 __global__ void __launch_bounds__(cfg::kThreads, 1)
     attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v,
                           const FwdParams p) {
-  using L = Layout<D, kPack>;
+  static_assert(!kFp8 || kBF16, "FP8 inputs give a bf16 output");
+  using L = Layout<D, kPack, kFp8>;
   using namespace cfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -417,7 +429,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
         ptx::mbar_arrive_expect_tx_elect(bar_q + 8 * t, p.q_tile_bytes);
         for (int c = 0; c < L::kChunks; ++c)
           ptx::tma_load_3d_elect(dst + c * L::kBoxBytes, &tm_q, bar_q + 8 * t,
-                                 c * 64, w.m0[t], w.plane[t]);
+                                 c * L::kBoxElems, w.m0[t], w.plane[t]);
         ++q_loads[t];
       }
       for (int j = 0; j < w.n_kv && ok; ++j) {
@@ -434,7 +446,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
           ptx::mbar_arrive_expect_tx_elect(bar_full + 8 * slot, L::kTileBytes);
           for (int c = 0; c < L::kChunks; ++c)
             ptx::tma_load_3d_elect(dst + c * L::kBoxBytes, kv ? &tm_v : &tm_k,
-                                   bar_full + 8 * slot, c * 64,
+                                   bar_full + 8 * slot, c * L::kBoxElems,
                                    (w.kb + j) * kTN, w.kv_plane);
           ++it;
         }
@@ -452,15 +464,19 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
     // ------------------------------------------------------ MMA issuer
     // The whole warp runs this loop (warp-uniform); one elected lane issues.
     const uint32_t idesc_qk =
-        ptx::idesc_f16(kBF16, kTM, kTN, false, p.negate_scores != 0);
-    const uint32_t idesc_pv = ptx::idesc_f16(kBF16, kTM, D, true, false);
+        kFp8 ? ptx::idesc_e4m3(kTM, kTN, false, p.negate_scores != 0)
+             : ptx::idesc_f16(kBF16, kTM, kTN, false, p.negate_scores != 0);
+    const uint32_t idesc_pv = kFp8 ? ptx::idesc_e4m3(kTM, D, true, false)
+                                   : ptx::idesc_f16(kBF16, kTM, D, true, false);
     bool ok = true;
     bool issued_any = false;
 
     // Descriptor low words, computed once; per MMA one add of a
     // compile-time offset.  K-major tiles: LBO unused (16), SBO = 1024
-    // (8 rows of 128 B).  V (MN-major): LBO = 16 KB between the 64-column
-    // halves of D, SBO = 1024 between groups of 8 keys.
+    // (8 rows of 128 B).  V (MN-major): LBO = 16 KB between the 128-byte
+    // column boxes of D (16-bit D = 128 has two), SBO = 1024 between groups
+    // of 8 keys.  One MMA consumes 32 bytes of K: 16 16-bit or 32 8-bit
+    // elements.
     constexpr uint32_t kHi = ptx::sdesc_hi_sw128(1024);
     const uint32_t q_lo = ptx::sdesc_lo(s_q, 16);
     const uint32_t k_lo = ptx::sdesc_lo(s_ring, 16);
@@ -474,22 +490,25 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
       const uint32_t b0 = k_lo + slot * kTile16;
       const uint32_t d = tmem + sb * kTN;
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
+      for (int kk = 0; kk < D * L::kEs / 32; ++kk) {
         const uint32_t off = ((kk / 4) * L::kBoxBytes + (kk % 4) * 32) >> 4;
-        ptx::mma_ss_elect(d, a0 + off, b0 + off, kHi, idesc_qk,
-                          kk > 0 ? 1u : 0u);
+        ptx::mma_ss_elect<kFp8>(d, a0 + off, b0 + off, kHi, idesc_qk,
+                                kk > 0 ? 1u : 0u);
       }
     };
     // O_t (+)= P V_j : A = P in S region `sb` of TMEM, B = V tile
-    // (MN-major).
+    // (MN-major).  Each MMA takes 32 / kEs keys: 8 TMEM columns of P and
+    // that many 128-byte rows of V.
     auto issue_pv = [&](int t, int sb, int slot, bool acc) {
+      constexpr int kKeys = 32 / L::kEs;
       const uint32_t b0 = v_lo + slot * kTile16;
       const uint32_t d = tmem + 2 * kTN + t * D;
       const uint32_t a = tmem + sb * kTN;
 #pragma unroll
-      for (int kk = 0; kk < kTN / 16; ++kk) {
-        ptx::mma_ts_elect(d, a + kk * 8, b0 + ((kk * 16 * 128) >> 4), kHi,
-                          idesc_pv, (acc || kk > 0) ? 1u : 0u);
+      for (int kk = 0; kk < kTN / kKeys; ++kk) {
+        ptx::mma_ts_elect<kFp8>(d, a + kk * 8,
+                                b0 + ((kk * kKeys * 128) >> 4), kHi, idesc_pv,
+                                (acc || kk > 0) ? 1u : 0u);
       }
     };
 
@@ -766,9 +785,11 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
 
         // Pass 2: P = 2^(s*c - m_new) and its row sum, packed to 16 bits into
         // TMEM over S_t (32 scores -> 16 columns, key 2e+1 | key 2e in column
-        // e).  S is re-read from TMEM in 32-column chunks, the next chunk's
-        // load in flight while this one is computed; P chunk q only
-        // overwrites S columns already consumed.
+        // e; FP8: E4M3, 32 scores -> 8 columns, key 4e in the low byte of
+        // column e).  S is re-read from TMEM in 32-column chunks, the next
+        // chunk's load in flight while this one is computed; P chunk q only
+        // overwrites S columns already consumed.  The row sum is taken from
+        // the fp32 P.  P <= 2^tau = 256 stays inside E4M3's range (448).
         const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
         float sm[4] = {0.f, 0.f, 0.f, 0.f};
         {
@@ -779,25 +800,49 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
           for (int q = 0; q < kTN / 32; ++q) {
             uint32_t* cur = buf[q & 1];
             if (q + 1 < kTN / 32) ptx::tmem_ld32(t_s + 32 * (q + 1), buf[(q + 1) & 1]);
-            uint32_t pk[16];
+            if constexpr (kFp8) {
+              uint32_t pk[8];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              float x0, x1;
-              ptx::ffma2(x0, x1, __uint_as_float(cur[2 * e]),
-                         __uint_as_float(cur[2 * e + 1]), c, neg_m);
-              if (masked) {
-                if (hidden(32 * q + 2 * e)) x0 = -INFINITY;
-                if (hidden(32 * q + 2 * e + 1)) x1 = -INFINITY;
+              for (int e = 0; e < 8; ++e) {
+                float x[4];
+                ptx::ffma2(x[0], x[1], __uint_as_float(cur[4 * e]),
+                           __uint_as_float(cur[4 * e + 1]), c, neg_m);
+                ptx::ffma2(x[2], x[3], __uint_as_float(cur[4 * e + 2]),
+                           __uint_as_float(cur[4 * e + 3]), c, neg_m);
+                if (masked) {
+#pragma unroll
+                  for (int a = 0; a < 4; ++a)
+                    if (hidden(32 * q + 4 * e + a)) x[a] = -INFINITY;
+                }
+                float pe[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) pe[a] = ptx::ex2(x[a]);
+                ptx::fadd2(sm[0], sm[1], pe[0], pe[1]);
+                ptx::fadd2(sm[2], sm[3], pe[2], pe[3]);
+                pk[e] = ptx::pack4_e4m3(pe[0], pe[1], pe[2], pe[3]);
               }
-              const float p0 = ptx::ex2(x0);
-              const float p1 = ptx::ex2(x1);
-              if (e & 1)
-                ptx::fadd2(sm[2], sm[3], p0, p1);
-              else
-                ptx::fadd2(sm[0], sm[1], p0, p1);
-              pk[e] = ptx::pack2<kBF16>(p0, p1);
+              ptx::tmem_st8(t_s + 8 * q, pk);
+            } else {
+              uint32_t pk[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                float x0, x1;
+                ptx::ffma2(x0, x1, __uint_as_float(cur[2 * e]),
+                           __uint_as_float(cur[2 * e + 1]), c, neg_m);
+                if (masked) {
+                  if (hidden(32 * q + 2 * e)) x0 = -INFINITY;
+                  if (hidden(32 * q + 2 * e + 1)) x1 = -INFINITY;
+                }
+                const float p0 = ptx::ex2(x0);
+                const float p1 = ptx::ex2(x1);
+                if (e & 1)
+                  ptx::fadd2(sm[2], sm[3], p0, p1);
+                else
+                  ptx::fadd2(sm[0], sm[1], p0, p1);
+                pk[e] = ptx::pack2<kBF16>(p0, p1);
+              }
+              ptx::tmem_st16(t_s + 16 * q, pk);
             }
-            ptx::tmem_st16(t_s + 16 * q, pk);
             if (q + 1 < kTN / 32) ptx::tmem_wait_ld();
           }
         }
@@ -851,7 +896,8 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
       if (!live) {
         // Padding rows only: nothing to store.
       } else if (p.o_part == nullptr) {
-        const float inv_l = ptx::rcp(l_run);
+        const float inv_l =
+            kFp8 ? ptx::rcp(l_run) * p.o_scale : ptx::rcp(l_run);
         const long long row = static_cast<long long>(q_plane) * p.Sq + q_row;
         uint4* orow =
             reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + row * D);
@@ -878,7 +924,8 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
         // in fp32, and the range's natural-log LSE; a row that sees no key
         // of the range gets O = 0 and LSE = -inf.
         const bool empty = !(l_run > 0.f);
-        const float inv_l = empty ? 0.f : ptx::rcp(l_run);
+        const float inv_l =
+            empty ? 0.f : (kFp8 ? ptx::rcp(l_run) * p.o_scale : ptx::rcp(l_run));
         const long long prow =
             (static_cast<long long>(w.split) * p.B * p.Hq + q_plane) * p.Sq +
             q_row;

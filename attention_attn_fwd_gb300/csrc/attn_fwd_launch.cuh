@@ -9,12 +9,13 @@ namespace attn {
 // library) keeps its own "attribute set" flag per kernel.
 namespace {
 
-template <int D, bool kBF16, bool kPack, bool kSplit, bool kWindow>
+template <int D, bool kBF16, bool kPack, bool kSplit, bool kWindow,
+          bool kFp8>
 cudaError_t launch_variant(const CUtensorMap& q, const CUtensorMap& k,
                            const CUtensorMap& v, const FwdParams& p, int grid,
                            cudaStream_t stream) {
-  auto kernel = attn_fwd_sm103_kernel<D, kBF16, kPack, kSplit, kWindow>;
-  const int smem = Layout<D, kPack>::kSmemBytes;
+  auto kernel = attn_fwd_sm103_kernel<D, kBF16, kPack, kSplit, kWindow, kFp8>;
+  const int smem = Layout<D, kPack, kFp8>::kSmemBytes;
   // The attribute is per device; setting it again is cheap and idempotent.
   static thread_local int configured_device = -1;
   int dev = 0;
@@ -37,32 +38,37 @@ cudaError_t launch_variant(const CUtensorMap& q, const CUtensorMap& k,
 
 // Dtype, split-KV and window dispatch of one (D, tile mode) variant:
 // split-KV when the parameters carry partial-result buffers, the window
-// variant when a window is set.
-template <int D, bool kPack, bool kSplit, bool kWindow>
+// variant when a window is set.  FP8 inputs always write bf16.
+template <int D, bool kPack, bool kSplit, bool kWindow, bool kFp8>
 cudaError_t launch_dtype(bool bf16, const CUtensorMap& q, const CUtensorMap& k,
                          const CUtensorMap& v, const FwdParams& p, int grid,
                          cudaStream_t stream) {
-  return bf16 ? launch_variant<D, true, kPack, kSplit, kWindow>(q, k, v, p,
-                                                                grid, stream)
-              : launch_variant<D, false, kPack, kSplit, kWindow>(q, k, v, p,
+  if constexpr (kFp8) {
+    return launch_variant<D, true, kPack, kSplit, kWindow, true>(q, k, v, p,
                                                                  grid, stream);
+  } else {
+    return bf16 ? launch_variant<D, true, kPack, kSplit, kWindow, false>(
+                      q, k, v, p, grid, stream)
+                : launch_variant<D, false, kPack, kSplit, kWindow, false>(
+                      q, k, v, p, grid, stream);
+  }
 }
 
-template <int D, bool kPack>
+template <int D, bool kPack, bool kFp8 = false>
 cudaError_t launch_mode(bool bf16, const CUtensorMap& q, const CUtensorMap& k,
                         const CUtensorMap& v, const FwdParams& p, int grid,
                         cudaStream_t stream) {
   const bool split = p.o_part != nullptr;
   const bool window = p.window > 0;
   if (split)
-    return window ? launch_dtype<D, kPack, true, true>(bf16, q, k, v, p, grid,
-                                                       stream)
-                  : launch_dtype<D, kPack, true, false>(bf16, q, k, v, p, grid,
-                                                        stream);
-  return window ? launch_dtype<D, kPack, false, true>(bf16, q, k, v, p, grid,
-                                                      stream)
-                : launch_dtype<D, kPack, false, false>(bf16, q, k, v, p, grid,
-                                                       stream);
+    return window ? launch_dtype<D, kPack, true, true, kFp8>(bf16, q, k, v, p,
+                                                             grid, stream)
+                  : launch_dtype<D, kPack, true, false, kFp8>(bf16, q, k, v, p,
+                                                              grid, stream);
+  return window ? launch_dtype<D, kPack, false, true, kFp8>(bf16, q, k, v, p,
+                                                            grid, stream)
+                : launch_dtype<D, kPack, false, false, kFp8>(bf16, q, k, v, p,
+                                                             grid, stream);
 }
 
 }  // namespace

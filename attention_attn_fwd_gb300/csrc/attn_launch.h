@@ -9,10 +9,10 @@
 
 namespace attn {
 
-// Dynamic shared memory one CTA of the (D, packed) variant needs.
-int fwd_smem_bytes(int D, bool pack);
-// K/V stages (pairs of ring slots) of the (D, packed) variant.
-int fwd_stages(int D, bool pack);
+// Dynamic shared memory one CTA of the (D, packed, FP8) variant needs.
+int fwd_smem_bytes(int D, bool pack, bool fp8 = false);
+// K/V stages (pairs of ring slots) of the (D, packed, FP8) variant.
+int fwd_stages(int D, bool pack, bool fp8 = false);
 
 // One entry per kernel translation unit: head dimension x tile mode (two
 // 128-row Q tiles, or the query heads of a GQA group packed into one).
@@ -30,6 +30,15 @@ cudaError_t launch_fwd_d128_packed(bool bf16, const CUtensorMap& q,
                                    const CUtensorMap& k, const CUtensorMap& v,
                                    const FwdParams& p, int grid,
                                    cudaStream_t stream);
+// E4M3 inputs, D = 128, bf16 output.
+cudaError_t launch_fwd_d128_fp8(const CUtensorMap& q, const CUtensorMap& k,
+                                const CUtensorMap& v, const FwdParams& p,
+                                int grid, cudaStream_t stream);
+cudaError_t launch_fwd_d128_fp8_packed(const CUtensorMap& q,
+                                       const CUtensorMap& k,
+                                       const CUtensorMap& v,
+                                       const FwdParams& p, int grid,
+                                       cudaStream_t stream);
 
 // Backward pass: row pass (D, lse2 into p.lse2 / p.delta), dK/dV kernel,
 // dQ kernel, in that order on `stream` (attn_bwd.cu).  `d` maps dO like `q`

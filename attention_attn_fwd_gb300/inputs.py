@@ -3,7 +3,9 @@
 This module holds no attention arithmetic: it only names the workloads and
 draws their inputs.  Q, K and V are drawn in that order from a seeded CPU
 ``torch.Generator`` as float32 N(0, 1) samples and then rounded to the
-workload's dtype, so the CUDA path and the CPU oracle see identical values.
+workload's dtype (for "e4m3", torch's float8_e4m3fn rounding: the samples
+are the codes, a descale factor of 1), so the CUDA path and the CPU oracle
+see identical values.
 """
 from dataclasses import dataclass, replace
 import math
@@ -20,7 +22,7 @@ class Workload:
     Sq: int
     Skv: int
     D: int
-    dtype: str          # "f16" or "bf16"
+    dtype: str          # "f16", "bf16" or "e4m3" (FP8 inputs, bf16 output)
     causal: bool
     input_pos: int = 0
     window: int = 0     # sliding window in keys (causal only), 0: none
@@ -31,7 +33,14 @@ class Workload:
 
     @property
     def torch_dtype(self):
-        return torch.float16 if self.dtype == "f16" else torch.bfloat16
+        """Element type of Q, K and V."""
+        return {"f16": torch.float16, "bf16": torch.bfloat16,
+                "e4m3": torch.float8_e4m3fn}[self.dtype]
+
+    @property
+    def out_dtype(self):
+        """Element type of O."""
+        return torch.bfloat16 if self.dtype == "e4m3" else self.torch_dtype
 
     def flops(self) -> float:
         """4*B*Hq*Sq*Skv*D, halved for causal (the reported convention)."""
@@ -54,11 +63,13 @@ class Workload:
         return 4.0 * self.D * self.visible_pairs()
 
     def io_bytes(self) -> int:
-        """Q, K, V read once; O written once; LSE written once (fp32)."""
-        e = 2
+        """Q, K, V read once; O written once (16-bit); LSE written once
+        (fp32)."""
+        e = 1 if self.dtype == "e4m3" else 2
         q = self.B * self.Hq * self.Sq * self.D * e
+        o = self.B * self.Hq * self.Sq * self.D * 2
         kv = 2 * self.B * self.Hkv * self.Skv * self.D * e
-        return 2 * q + kv + 4 * self.B * self.Hq * self.Sq
+        return q + o + kv + 4 * self.B * self.Hq * self.Sq
 
     def with_(self, **kw) -> "Workload":
         return replace(self, **kw)
@@ -78,6 +89,10 @@ PREFILL_CHUNK = Workload("prefill_B8_Hq32_Hkv8_Sq512_pos3584_Skv4096_D128_bf16",
 # last 4096 positions).
 WINDOW_32K = Workload("window_B1_Hq32_Hkv4_S32768_W4096_D128_bf16", 1, 32, 4,
                       32768, 32768, 128, "bf16", True, 0, 4096)
+
+# The bench workload with FP8 (E4M3) inputs and a bf16 output.
+GQA_8K_FP8 = Workload("gqa_B1_Hq32_Hkv4_S8192_D128_e4m3_causal", 1, 32, 4,
+                      8192, 8192, 128, "e4m3", True)
 
 # One new token per sequence against a full 4096-key cache (the decode step
 # after the prefill chunk above); the split-KV path's workload.

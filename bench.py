@@ -409,10 +409,12 @@ def run_reference(args):
 
 # ------------------------------------------------------- split-KV decode
 DECODE_SETS = 4
-def run_decode(args):
+def run_decode(args, fp8=False):
     """Split-KV decode step: HBM-bound, reported in GB/s of algorithmic
     traffic (Q, K, V read once; O and LSE written once) against the measured
     copy bandwidth.  One kernel per step (partials and their merge).
+    ``fp8``: the same step with E4M3 Q/K/V (half the K/V bytes) through
+    attn_fwd_fp8, bf16 O.
 
     Steps rotate over DECODE_SETS independent input sets whose total is
     several times L2, so every step reads its K/V from HBM.  (A flush write
@@ -428,15 +430,16 @@ def run_decode(args):
     if ws > 1:
         torch.cuda.set_device(local)
     dev = torch.device("cuda", torch.cuda.current_device())
-    w = DECODE
+    w = DECODE.with_(name=DECODE.name.replace("bf16", "e4m3"),
+                     dtype="e4m3") if fp8 else DECODE
     sets = []
     for i in range(DECODE_SETS):
         q, k, v = (t.to(dev) for t in make_qkv(w, seed=i))
-        o = torch.empty_like(q)
+        o = torch.empty(q.shape, dtype=w.out_dtype, device=dev)
         lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
         sets.append((q, k, v, o, lse))
     stream = torch.cuda.current_stream(dev)
-    dt = attn.ATTN_BF16
+    dt = attn.ATTN_E4M3 if fp8 else attn.ATTN_BF16
     splits, ws_bytes = attn.attn_splitkv_plan(w.B, w.Hq, w.Hkv, w.Sq, w.Skv,
                                               w.D, 1, w.input_pos, dt,
                                               args.splits)
@@ -444,14 +447,20 @@ def run_decode(args):
 
     def step(i):
         q, k, v, o, lse = sets[i % DECODE_SETS]
-        st = attn.attn_fwd_splitkv(
-            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-            lse.data_ptr(), w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.scale, 1,
-            w.input_pos, dt, splits, work.data_ptr(), ws_bytes,
-            stream.cuda_stream)
+        if fp8:
+            st = attn.attn_fwd_fp8(
+                q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                lse.data_ptr(), w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.scale,
+                1.0, 1.0, 1.0, 1, w.input_pos, 0, splits, work.data_ptr(),
+                ws_bytes, stream.cuda_stream)
+        else:
+            st = attn.attn_fwd_splitkv(
+                q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                lse.data_ptr(), w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.scale,
+                1, w.input_pos, dt, splits, work.data_ptr(), ws_bytes,
+                stream.cuda_stream)
         if st != attn.ATTN_OK:
-            raise RuntimeError("attn_fwd_splitkv: " +
-                               attn.attn_status_string(st))
+            raise RuntimeError("decode step: " + attn.attn_status_string(st))
 
     for i in range(args.warmup):
         step(i)
@@ -471,7 +480,8 @@ def run_decode(args):
     gbs = w.io_bytes() / (ms * 1e-3) / 1e9
     _, hbm, src = peaks()
     out = {
-        "metric": "attention decode (split-KV) GB/s of algorithmic traffic",
+        "metric": "attention decode (split-KV) GB/s of algorithmic traffic"
+                  + (", FP8 inputs" if fp8 else ""),
         "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 5), "higher_is_better": True,
@@ -482,6 +492,7 @@ def run_decode(args):
             "l2": "inputs larger than L2: %d rotating input sets, %.0f MB"
                   % (DECODE_SETS, DECODE_SETS * w.io_bytes() / 1e6),
             "algorithmic_bytes_per_step": w.io_bytes(),
+            "tokens_per_s": round(w.B / (ms * 1e-3), 1),
             "tflops_formula": round(w.flops() / (ms * 1e-3) / 1e12, 2)}),
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
                      "unit": "GB/s", "frac": round(gbs / hbm, 4),
@@ -561,6 +572,82 @@ def run_window(args):
                      "peak": peak, "unit": "TFLOP/s",
                      "frac": round(tflops / peak, 4),
                      "peak_source": "%s bf16 dense burst (cuBLAS)" % src,
+                     "traffic": None},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------ FP8 forward
+def run_fp8(args):
+    """The headline GQA 8k causal forward with E4M3 Q/K/V (descale 1) and a
+    bf16 O through attn_fwd_fp8; TFLOPS with the causal-halved FLOPs,
+    against the dense FP8 peak taken as the measured bf16 burst peak x 2
+    (the nominal FP8 / bf16 ratio, 4.5 / 2.25 PFLOP/s).  L2 flushed between
+    timed steps (the FP8 inputs, ~50 MB, would fit in it)."""
+    import torch
+
+    import attention_attn_fwd_gb300 as attn
+    from attention_attn_fwd_gb300.inputs import GQA_8K_FP8, make_qkv
+
+    ws, rank, local = dist_info()
+    if ws > 1:
+        torch.cuda.set_device(local)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = GQA_8K_FP8
+    q, k, v = (t.to(dev) for t in make_qkv(w, seed=0))
+    o = torch.empty(q.shape, dtype=w.out_dtype, device=dev)
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        st = attn.attn_fwd_fp8(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+            lse.data_ptr(), w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.scale, 1.0,
+            1.0, 1.0, 1, w.input_pos, 0, 0, 0, 0, stream.cuda_stream)
+        if st != attn.ATTN_OK:
+            raise RuntimeError("attn_fwd_fp8: " + attn.attn_status_string(st))
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(dev.index) as clocks:
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    st, code = attn.attn_device_status()
+    if st != attn.ATTN_OK:
+        raise RuntimeError("device status %d code %#x" % (st, code))
+    ms = sum(s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)) / args.steps
+    tflops = w.flops() / (ms * 1e-3) / 1e12
+    bf16_peak, _, src = peaks()
+    peak = 2.0 * bf16_peak
+    out = {
+        "metric": "attention fwd TFLOPS on 1 GB300 (causal-halved FLOPs), "
+                  "FP8 E4M3 inputs",
+        "value": round(tflops, 1), "unit": "TFLOPS", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic: Q/K/V ~ N(0,1) from a seeded CPU generator, "
+                "rounded to E4M3",
+        "config": config_dict(w, {
+            "out_dtype": "bf16",
+            "l2": "flushed between timed steps (256 MiB write, untimed)"}),
+        "roofline": {"bound": "tensor", "achieved": round(tflops, 1),
+                     "peak": round(peak, 1), "unit": "TFLOP/s",
+                     "frac": round(tflops / peak, 4),
+                     "peak_source": "%s bf16 dense burst (cuBLAS) x 2, the "
+                                    "nominal FP8/bf16 ratio" % src,
                      "traffic": None},
         "gpu_launches": args.steps,
         "clocks": clocks.summary(),
@@ -660,12 +747,14 @@ def main():
                     help="CPU-oracle baseline budget in seconds")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload",
-                    choices=["gqa8k", "decode", "window", "bwd"],
+                    choices=["gqa8k", "decode", "window", "bwd", "fp8",
+                             "decode_fp8"],
                     default="gqa8k",
                     help="gqa8k: the headline causal GQA forward (default); "
                          "decode: the split-KV decode step; window: causal "
                          "GQA 32k with a 4096-key sliding window; bwd: the "
-                         "backward pass of gqa8k")
+                         "backward pass of gqa8k; fp8: gqa8k with E4M3 "
+                         "inputs; decode_fp8: decode with E4M3 inputs")
     ap.add_argument("--splits", type=int, default=0,
                     help="split count for --workload decode (0: automatic)")
     args = ap.parse_args()
@@ -675,6 +764,10 @@ def main():
         run_reference(args)
     elif args.workload == "decode":
         run_decode(args)
+    elif args.workload == "decode_fp8":
+        run_decode(args, fp8=True)
+    elif args.workload == "fp8":
+        run_fp8(args)
     elif args.workload == "window":
         run_window(args)
     elif args.workload == "bwd":

@@ -36,7 +36,11 @@ typedef struct CUstream_st* attn_stream_t;
 /* Element type of Q, K, V and O. */
 typedef enum {
   ATTN_F16 = 0,  /* IEEE binary16 */
-  ATTN_BF16 = 1  /* bfloat16 */
+  ATTN_BF16 = 1, /* bfloat16 */
+  ATTN_E4M3 = 2  /* OCP FP8 E4M3 ("e4m3fn") inputs with a bfloat16 O: only
+                    attn_fwd_fp8, attn_splitkv_plan and attn_tile_config
+                    take it; elsewhere ATTN_ERR_INVALID_ARG (ATTN_ERR_-
+                    UNSUPPORTED for attn_bwd) */
 } attn_dtype_t;
 
 /* Return codes.  Everything but ATTN_OK leaves O and LSE untouched. */
@@ -149,6 +153,42 @@ attn_status_t attn_fwd_splitkv_window(const void* Q, const void* K,
                                       attn_dtype_t dtype, int num_splits,
                                       void* workspace, size_t workspace_bytes,
                                       attn_stream_t stream);
+
+/*
+ * attn_fwd_fp8 — attention forward with 8-bit floating-point inputs.
+ * "Flash Attention from Scratch", section "What's Next", names FP8 tensor
+ * cores as future work without defining a format; the reading taken: Q, K
+ * and V hold OCP E4M3 codes (sign, 4-bit exponent with bias 7, 3-bit
+ * mantissa, no infinities, S.1111.111 is NaN; torch.float8_e4m3fn) with one
+ * fp32 descale factor per tensor, and the call computes the operation of
+ * attn_fwd_window on the real values
+ *   Q = q_descale * Q8,  K = k_descale * K8,  V = v_descale * V8.
+ * Both products run on the FP8 tensor cores with fp32 accumulation; the
+ * softmax weights are rounded to E4M3 for the P.V product (the row sums
+ * use them unrounded), which bounds the accuracy: each weight carries up to
+ * 2^-4 relative rounding (absolute 2^-10 below 2^-6).  The LSE is exact to
+ * fp32 rounding.
+ *
+ * Q, K, V  device, layouts as attn_fwd, one byte per element (read);
+ * O        device, [B, Hq, Sq, D] bfloat16 (written);
+ * LSE      device fp32 [B, Hq, Sq] or NULL: ln-sum-exp of the scores
+ *          scale * q_descale * k_descale * Q8.K8 (written);
+ * D        128 only (else ATTN_ERR_UNSUPPORTED);
+ * scale, q_descale, k_descale, v_descale  finite, any sign; the product
+ *          scale * q_descale * k_descale must be finite in fp32;
+ * causal, input_pos, window  as attn_fwd_window;
+ * num_splits  0: one pass (workspace ignored); >= 1: the split-KV form of
+ *          attn_fwd_splitkv_window with a count from attn_splitkv_plan
+ *          (dtype ATTN_E4M3) and its workspace rules;
+ * Other rules and errors as attn_fwd.
+ */
+attn_status_t attn_fwd_fp8(const void* Q, const void* K, const void* V,
+                           void* O, float* LSE, int B, int Hq, int Hkv,
+                           int Sq, int Skv, int D, float scale,
+                           float q_descale, float k_descale, float v_descale,
+                           int causal, int input_pos, int window,
+                           int num_splits, void* workspace,
+                           size_t workspace_bytes, attn_stream_t stream);
 
 /*
  * attn_splitkv_plan — split count and workspace size for attn_fwd_splitkv.
