@@ -75,7 +75,9 @@ class Workload:
         return replace(self, **kw)
 
 
-# The pages' workload shapes (see the design doc for the list and its sources).
+# Named workloads: a small case the oracle checks in full, causal MHA at 4k
+# and causal GQA (32 query heads over 4 K/V heads) at 8k with D = 128, and a
+# KV-cache prefill chunk whose queries start at input_pos = 3584.
 SMALL = Workload("small_B1_H2_S128_D64_f16", 1, 2, 2, 128, 128, 64, "f16", False)
 MHA_4K = Workload("mha_B1_H32_S4096_D128_f16_causal", 1, 32, 32, 4096, 4096,
                   128, "f16", True)
