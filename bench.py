@@ -30,6 +30,9 @@ METRIC = ("attention fwd TFLOPS on 1 GB300 (causal-halved FLOPs) and % of "
           "dense bf16 peak")
 UNIT = "TFLOPS"
 FLUSH_BYTES = 256 << 20  # > 129 MB L2
+# ex2.approx.ftz.f32 results per clock per SM, measured on GB300 with a
+# probe kernel (one CTA per SM, dependent-free ex2 streams).
+EX2_PER_CLK_PER_SM = 32
 KERNEL_SOURCES = ["attention_attn_fwd_gb300/csrc/attn_fwd_kernel.cuh",
                   "attention_attn_fwd_gb300/csrc/sm103_ptx.cuh"]
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles",
@@ -128,6 +131,21 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(busy) if busy else None,
                 "sm_max_mhz": smax, "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+def exp2_roofline(w, ms, clocks, sms):
+    """One exp2 per visible score: achieved rate against the SFU peak at the
+    SM clock sampled during the timed region."""
+    n = w.visible_pairs()
+    mhz = clocks.get("sm_mhz") or clocks.get("sm_max_mhz")
+    if not mhz or not sms:
+        return {"exp2_per_step": n, "frac": None}
+    peak = EX2_PER_CLK_PER_SM * sms * mhz * 1e6
+    rate = n / (ms * 1e-3)
+    return {"exp2_per_step": n, "achieved_per_s": round(rate, 0),
+            "peak_per_s": round(peak, 0), "frac": round(rate / peak, 4),
+            "peak_source": "%d ex2/clk/SM (measured) x %d SMs x %.0f MHz"
+                           % (EX2_PER_CLK_PER_SM, sms, mhz)}
 
 
 def dist_info():
@@ -314,7 +332,10 @@ def run_ours(args):
                 w.exact_flops() / (kernel_ms * 1e-3) / 1e12, 2),
             "ms_per_step_p50": round(statistics.median(times_ms), 4),
             "ms_per_step_max": round(max(times_ms), 4),
-            "wall_s_timed_region": round(wall, 4)}),
+            "wall_s_timed_region": round(wall, 4),
+            "exp2_roofline": exp2_roofline(
+                w, kernel_ms, clk,
+                torch.cuda.get_device_properties(dev).multi_processor_count)}),
         "roofline": {
             "bound": "tensor", "achieved": round(achieved, 2),
             "peak": peak_tf, "unit": "TFLOP/s",
