@@ -459,6 +459,18 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return d;
 }
 
+// Per-thread register allocation of the calling warpgroup (all four warps
+// execute the same call).  inc waits until the CTA's pool holds enough
+// registers released by dec calls.
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // Four floats -> four E4M3 codes in one word, round to nearest even with
 // saturation to +-448; x0 goes to the lowest byte (the lowest-indexed
 // element in memory / tensor memory).
