@@ -254,7 +254,12 @@ size_t attn_noalloc_scratch_bytes(void);
  * workspace        device, 256-byte aligned, at least
  *                  attn_bwd_workspace_bytes(B, Hq, Sq) bytes (per-row
  *                  lse2 and D); contents need no initialisation;
- * Three kernels are enqueued on `stream` (row pass, dK/dV, dQ); every
+ * Three kernels: the row pass and the dK/dV kernel on `stream`, the dQ
+ * kernel on an internal stream forked from `stream` after the row pass and
+ * joined back into it (event record / wait), so the two run concurrently
+ * and later work on `stream` waits for both; this works under stream
+ * capture.  The first call on a host thread and device creates that
+ * internal stream and its two events (make it before any capture).  Every
  * output element has one writer, so results are deterministic.  Sq = 0
  * writes zero dK, dV.  Errors as attn_fwd.
  */

@@ -111,6 +111,47 @@ def test_bwd_deterministic():
         assert torch.equal(x, y)
 
 
+def test_bwd_side_stream_and_graph():
+    """The dQ kernel runs on an internal stream forked from the caller's:
+    a call on a user stream, and a replay of the call captured into a CUDA
+    graph, give the bit-identical gradients of a default-stream call."""
+    w = W("streams", 1, 8, 2, 384, 640, 128, "bf16", True, 256)
+    q, k, v = (t.cuda() for t in make_qkv(w, seed=45))
+    do = make_do(w, seed=45).cuda()
+    o, lse = attn.fwd(q, k, v, scale=w.scale, causal=True,
+                      input_pos=w.input_pos)
+    ref = attn.bwd(q, k, v, o, lse, do, scale=w.scale, causal=True,
+                   input_pos=w.input_pos)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    outs = tuple(torch.full_like(t, 7.0) for t in ref)
+    ws = torch.empty(attn.attn_bwd_workspace_bytes(w.B, w.Hq, w.Sq),
+                     dtype=torch.uint8, device="cuda")
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        got = attn.bwd(q, k, v, o, lse, do, scale=w.scale, causal=True,
+                       input_pos=w.input_pos, dq=outs[0], dk=outs[1],
+                       dv=outs[2], workspace=ws)
+    s.synchronize()
+    for x, y in zip(ref, got):
+        assert torch.equal(x, y)
+    for t in outs:
+        t.fill_(7.0)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        attn.bwd(q, k, v, o, lse, do, scale=w.scale, causal=True,
+                 input_pos=w.input_pos, dq=outs[0], dk=outs[1], dv=outs[2],
+                 workspace=ws)
+    for t in outs:
+        t.fill_(7.0)
+    g.replay()
+    torch.cuda.synchronize()
+    assert attn.attn_device_status() == (0, 0)
+    for x, y in zip(ref, outs):
+        assert torch.equal(x, y)
+
+
 def test_bwd_full_size_gqa8k():
     """GQA 8k causal: dQ on sampled rows against the oracle; dK and dV at
     every element through exact identities -- each row of dS sums to zero,
