@@ -26,6 +26,16 @@ cudaError_t launch_variant(const CUtensorMap& q, const CUtensorMap& k,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                smem);
     if (err != cudaSuccess) return err;
+    if constexpr (kWindow) {
+      // These variants split the launch's registers with setmaxnreg, which
+      // only adds up when every thread launches with cfg::kRegsLaunch: a
+      // build that allocated fewer would leave the increase waiting
+      // forever, so refuse to launch it.
+      cudaFuncAttributes attr{};
+      err = cudaFuncGetAttributes(&attr, kernel);
+      if (err != cudaSuccess) return err;
+      if (attr.numRegs != cfg::kRegsLaunch) return cudaErrorInvalidConfiguration;
+    }
     configured_device = dev;
   }
   cudaLaunchConfig_t cfg = {};
