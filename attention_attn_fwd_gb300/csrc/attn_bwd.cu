@@ -81,13 +81,17 @@ cudaError_t run(const CUtensorMap& q, const CUtensorMap& k,
                 const void* dO, const float* LSE, const BwdParams& p,
                 cudaStream_t stream) {
   static thread_local int cfg_dkdv = -1, cfg_dq = -1;
-  const long long rows = static_cast<long long>(p.B) * p.Hq * p.sq_pad;
+  const long long planes = static_cast<long long>(p.B) * p.Hq;
+  const long long rows = planes * p.Sq;
+  const long long pad_rows = planes * (p.sq_pad - p.Sq);
   float* lse2 = const_cast<float*>(p.lse2);
   float* delta = const_cast<float*>(p.delta);
-  const long long blocks = (rows * 32 + 255) / 256;
+  // Warps: one per 8 rows, then one per 32 padding rows.
+  const long long warps = (rows + 7) / 8 + (pad_rows + 31) / 32;
+  const long long blocks = (warps * 32 + 255) / 256;
   attn_bwd_prep_kernel<D, kBF16><<<static_cast<unsigned>(blocks), 256, 0,
                                    stream>>>(O, dO, LSE, lse2, delta, rows,
-                                             p.Sq, p.sq_pad);
+                                             planes, p.Sq, p.sq_pad);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
 

@@ -137,55 +137,95 @@ __device__ __forceinline__ int next_key_tile(const BwdParams& p, int m,
 }
 
 // ------------------------------------------------------------- row pass
-// D_i = sum_d dO_id O_id and lse2_i = LSE_i log2(e), one warp per row of
-// the padded [planes, sq_pad] arrays; rows past Sq get lse2 = +inf (so
-// P = 0 there) and D = 0, and the tile loops read whole tiles unchecked.
+// D_i = sum_d dO_id O_id and lse2_i = LSE_i log2(e) into the padded
+// [planes, sq_pad] arrays; rows past Sq get lse2 = +inf (so P = 0 there) and
+// D = 0, and the tile loops read whole tiles unchecked.  The first warps
+// take kRows consecutive rows each of the flat [planes * Sq] row space
+// (contiguous in O and dO): lane l reads the 16-byte chunks l, l + 32, ...
+// of that block, so each load instruction of the warp covers 512
+// contiguous bytes and every lane has 2 * kRows * D / 256 loads in flight;
+// the lanes holding pieces of one row then reduce among themselves.  The
+// warps after them fill the padding rows, 32 per warp.
 template <int D, bool kBF16>
 __global__ void __launch_bounds__(256)
     attn_bwd_prep_kernel(const void* __restrict__ O,
                          const void* __restrict__ dO,
                          const float* __restrict__ LSE,
                          float* __restrict__ lse2, float* __restrict__ delta,
-                         long long padded_rows, int Sq, int sq_pad) {
-  constexpr int kPer = D / 32;  // elements per lane (2 or 4)
-  const long long prow =
+                         long long rows, long long planes, int Sq,
+                         int sq_pad) {
+  constexpr int kRows = 8;                       // rows per warp
+  constexpr int kRowChunks = D * 2 / 16;         // 16-byte chunks per row
+  constexpr int kPerLane = kRows * kRowChunks / 32;
+  static_assert(kRowChunks <= 32 && kPerLane >= 1, "row pass layout");
+  const long long warp =
       (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
-  if (prow >= padded_rows) return;
-  const long long plane = prow / sq_pad;
-  const int r = static_cast<int>(prow % sq_pad);
-  if (r >= Sq) {
-    if (lane == 0) {
+  const long long row_warps = (rows + kRows - 1) / kRows;
+  if (warp >= row_warps) {
+    const int pad = sq_pad - Sq;
+    const long long i = (warp - row_warps) * 32 + lane;
+    if (pad > 0 && i < planes * pad) {
+      const long long prow = (i / pad) * sq_pad + Sq + i % pad;
       delta[prow] = 0.f;
       lse2[prow] = INFINITY;
     }
     return;
   }
-  const long long row = plane * Sq + r;
-  const uint16_t* o = static_cast<const uint16_t*>(O) + row * D + lane * kPer;
-  const uint16_t* g = static_cast<const uint16_t*>(dO) + row * D + lane * kPer;
-  float acc = 0.f;
+  const long long row0 = warp * kRows;
+  const uint4* o = reinterpret_cast<const uint4*>(
+      static_cast<const uint16_t*>(O) + row0 * D);
+  const uint4* g = reinterpret_cast<const uint4*>(
+      static_cast<const uint16_t*>(dO) + row0 * D);
+  uint4 ov[kPerLane], gv[kPerLane];
 #pragma unroll
-  for (int e = 0; e < kPer; e += 2) {
-    const uint32_t ov = *reinterpret_cast<const uint32_t*>(o + e);
-    const uint32_t gv = *reinterpret_cast<const uint32_t*>(g + e);
-    float2 of, gf;
-    if constexpr (kBF16) {
-      of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov));
-      gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gv));
+  for (int k = 0; k < kPerLane; ++k) {
+    const int c = lane + 32 * k;
+    if (row0 + c / kRowChunks < rows) {
+      ov[k] = __ldg(o + c);
+      gv[k] = __ldg(g + c);
     } else {
-      of = __half22float2(*reinterpret_cast<const __half2*>(&ov));
-      gf = __half22float2(*reinterpret_cast<const __half2*>(&gv));
+      ov[k] = make_uint4(0u, 0u, 0u, 0u);
+      gv[k] = ov[k];
     }
-    acc = fmaf(of.x, gf.x, acc);
-    acc = fmaf(of.y, gf.y, acc);
   }
+  float acc[kPerLane];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1)
-    acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
-    delta[prow] = acc;
-    lse2[prow] = LSE[row] * bwd::kLog2e;
+  for (int k = 0; k < kPerLane; ++k) {
+    const uint32_t* a = reinterpret_cast<const uint32_t*>(&ov[k]);
+    const uint32_t* b = reinterpret_cast<const uint32_t*>(&gv[k]);
+    acc[k] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float2 of, gf;
+      if constexpr (kBF16) {
+        of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a[e]));
+        gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b[e]));
+      } else {
+        of = __half22float2(*reinterpret_cast<const __half2*>(&a[e]));
+        gf = __half22float2(*reinterpret_cast<const __half2*>(&b[e]));
+      }
+      acc[k] = fmaf(of.x, gf.x, acc[k]);
+      acc[k] = fmaf(of.y, gf.y, acc[k]);
+    }
+  }
+  // Lanes l .. l + kRowChunks - 1 (aligned) hold the pieces of one row.
+#pragma unroll
+  for (int off = kRowChunks / 2; off > 0; off >>= 1) {
+#pragma unroll
+    for (int k = 0; k < kPerLane; ++k)
+      acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], off);
+  }
+  if (lane % kRowChunks == 0) {
+#pragma unroll
+    for (int k = 0; k < kPerLane; ++k) {
+      const long long row = row0 + (lane + 32 * k) / kRowChunks;
+      if (row < rows) {
+        const long long prow = (row / Sq) * sq_pad + row % Sq;
+        delta[prow] = acc[k];
+        lse2[prow] = LSE[row] * bwd::kLog2e;
+      }
+    }
   }
 }
 
