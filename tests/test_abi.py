@@ -166,3 +166,63 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(attn, "_lib", None)
     with pytest.raises(attn.AttnError, match="not built"):
         attn.load_library()
+
+
+def test_fp8_tile_config_and_plan(lib):
+    """E4M3 inputs: 128-byte rows at D = 128 give 16 KB tiles (twice the
+    ring slots of bf16 at D = 128); D = 64 is not implemented."""
+    c8 = attn.attn_tile_config(1, 32, 4, 8192, 8192, 128, 1, 0, attn.ATTN_E4M3)
+    c16 = attn.attn_tile_config(1, 32, 4, 8192, 8192, 128, 1, 0,
+                                attn.ATTN_BF16)
+    assert c8["block_m"] == c16["block_m"] and c8["grid"] == c16["grid"]
+    assert c8["stages"] == 2 * c16["stages"]
+    assert c8["smem_bytes"] < c16["smem_bytes"]
+    with pytest.raises(attn.AttnError):
+        attn.attn_tile_config(1, 2, 2, 128, 128, 64, 0, 0, attn.ATTN_E4M3)
+    ns, ws = attn.attn_splitkv_plan(2, 8, 2, 1, 1000, 128, 1, 999,
+                                    attn.ATTN_E4M3, 5)
+    assert (ns, ws) == attn.attn_splitkv_plan(2, 8, 2, 1, 1000, 128, 1, 999,
+                                              attn.ATTN_BF16, 5)
+
+
+def fp8_call(**kw):
+    a = dict(Q=BAD, K=BAD + 0x100000, V=BAD + 0x200000, O=BAD + 0x300000,
+             LSE=0, B=1, Hq=2, Hkv=2, Sq=128, Skv=128, D=128, scale=0.125,
+             q_descale=1.0, k_descale=1.0, v_descale=1.0, causal=0,
+             input_pos=0, window=0, num_splits=0, workspace=0,
+             workspace_bytes=0, stream=0)
+    a.update(kw)
+    return attn.attn_fwd_fp8(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=64), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(q_descale=float("nan")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(k_descale=float("inf")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(v_descale=float("-inf")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=1e30, q_descale=1e30), attn.ATTN_ERR_INVALID_ARG),
+    (dict(num_splits=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Hq=3), attn.ATTN_ERR_INVALID_ARG),
+    (dict(window=4), attn.ATTN_ERR_INVALID_ARG),          # window, no causal
+    (dict(Q=BAD + 8), attn.ATTN_ERR_ALIGNMENT),
+    (dict(Sq=0), attn.ATTN_OK),
+    (dict(B=0, Q=0, K=0, V=0, O=0), attn.ATTN_OK),
+])
+def test_fp8_argument_checks(lib, kw, code):
+    assert fp8_call(**kw) == code
+
+
+def test_e4m3_refused_by_16_bit_entry_points(lib):
+    assert call(dtype=attn.ATTN_E4M3, D=128) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_fwd_window(BAD, BAD + 0x100000, BAD + 0x200000,
+                                BAD + 0x300000, 0, 1, 2, 2, 128, 128, 128,
+                                0.1, 1, 0, 0, attn.ATTN_E4M3, 0) == \
+        attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_fwd_splitkv(BAD, BAD + 0x100000, BAD + 0x200000,
+                                 BAD + 0x300000, 0, 1, 2, 2, 1, 1000, 128,
+                                 0.1, 1, 999, attn.ATTN_E4M3, 2,
+                                 BAD + 0x400000, 1 << 20, 0) == \
+        attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_bwd(BAD, BAD, BAD, BAD, BAD, BAD, BAD, BAD, BAD, 1, 2,
+                         2, 128, 128, 128, 0.1, 1, 0, 0, attn.ATTN_E4M3,
+                         BAD, 1 << 20, 0) == attn.ATTN_ERR_UNSUPPORTED
