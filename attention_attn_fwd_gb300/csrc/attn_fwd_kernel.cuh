@@ -21,7 +21,10 @@
 //   warps 8-11 the same for Q tile 1
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 and O1 (D columns each)
 // from 256.  P_t (16-bit) overwrites the first 64 columns of S_t and is the
-// A operand of O_t += P_t V straight from TMEM.  With the query heads of a
+// A operand of O_t += P_t V straight from TMEM.  At D = 64 the O tiles need
+// only 128 columns, so three S buffers [0,384) rotate between the two Q
+// tiles and O starts at 384: a tile's next S goes to the free buffer and is
+// computed while its softmax still works on the current one.  With the query heads of a
 // GQA group packed into tile 0 (few query rows), there is no tile 1: its S
 // region double-buffers the scores of tile 0 and its shared memory goes to
 // the K/V ring.
@@ -124,9 +127,10 @@ struct Layout {
   static constexpr int kQOff = 0;
   static constexpr int kRingOff = kQOff + kQTiles * kTileBytes;
   static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
-  // barriers: q_full[2], full[S], empty[S], s_full[2], p_full[2], o_full[2],
-  // drain[1], q_free[2]
-  static constexpr int kNumBars = 2 + 2 * kSlots + 2 + 2 + 2 + 1 + 2;
+  // barriers: q_full[2], full[S], empty[S], s_full[6] (two S regions, or
+  // three shared S buffers with one barrier per tile and buffer),
+  // p_full[2], o_full[2], drain[1], q_free[2], pv_done[2]
+  static constexpr int kNumBars = 2 + 2 * kSlots + 6 + 2 + 2 + 1 + 2 + 2;
   // misc: TMEM base, abort flag, per-tile "merge here" flags
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
   static constexpr int kBytes = kMiscOff + 16;
@@ -363,6 +367,10 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
   static_assert(!kFp8 || kBF16, "FP8 inputs give a bf16 output");
   using L = Layout<D, kPack, kFp8>;
   constexpr bool kHoldS = kWindow;  // S row kept in registers (see cfg)
+  // Three S buffers shared by the two Q tiles (D = 64: O needs 128 columns).
+  constexpr bool kTriple = D == 64 && !kPack;
+  constexpr int kOCol = kTriple ? 3 * cfg::kTN : 2 * cfg::kTN;  // first O column
+  static_assert(kOCol + 2 * D <= cfg::kTmemCols, "TMEM columns");
   using namespace cfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -374,11 +382,12 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
   const uint32_t bar_q = bar0;                         // [2]
   const uint32_t bar_full = bar0 + 8 * 2;              // [kSlots]
   const uint32_t bar_empty = bar_full + 8 * L::kSlots; // [kSlots]
-  const uint32_t bar_s = bar_empty + 8 * L::kSlots;    // [2]
-  const uint32_t bar_p = bar_s + 8 * 2;                // [2]
+  const uint32_t bar_s = bar_empty + 8 * L::kSlots;    // [6]: [3 * t + buffer]
+  const uint32_t bar_p = bar_s + 8 * 6;                // [2]
   const uint32_t bar_o = bar_p + 8 * 2;                // [2]
   const uint32_t bar_drain = bar_o + 8 * 2;            // [1]
   const uint32_t bar_qfree = bar_drain + 8;            // [2]
+  const uint32_t bar_pvdone = bar_qfree + 8 * 2;       // [2] every PV but a unit's last
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<int*>(smem + L::kMiscOff + 4);
 
@@ -518,7 +527,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
     auto issue_pv = [&](int t, int sb, int slot, bool acc) {
       constexpr int kKeys = 32 / L::kEs;
       const uint32_t b0 = v_lo + slot * kTile16;
-      const uint32_t d = tmem + 2 * kTN + t * D;
+      const uint32_t d = tmem + kOCol + t * D;
       const uint32_t a = tmem + sb * kTN;
 #pragma unroll
       for (int kk = 0; kk < kTN / kKeys; ++kk) {
@@ -531,6 +540,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
     int it = 0;               // ring items consumed so far
     int q_uses[2] = {0, 0};   // Q tile loads consumed, per tile
     int p_waits[2] = {0, 0};  // P-ready phases consumed, per tile
+    int s_issued = 0;         // kTriple: S MMAs issued (buffer = count % 3)
     for (int k = 0; k * u_step < p.num_units && ok; ++k) {
       const int u = unit_index(k, u_first, u_step);
       if (u >= p.num_units) continue;
@@ -596,6 +606,89 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
           }
         }
         it = it0 + 2 * n;
+        continue;
+      }
+      if constexpr (kTriple) {
+        // Per K/V step j: S_0(j+1), PV_0(j), S_1(j+1), PV_1(j).  S MMA
+        // number i goes to buffer i % 3; with two S issues between any S
+        // and its own PV, the buffer an S overwrites was last read by a PV
+        // issued (and, in issue order, executed) before it.  So a tile's
+        // next S is computed while its softmax works on the current one.
+        // Each PV but a unit's last commits to pv_done[t], which the softmax
+        // waits on before it may rescale O.
+        int pbuf[2] = {0, 0};  // buffer holding each tile's current S / P
+        ok = __all_sync(0xffffffffu,
+                        wait_bounded(bar_full + 8 * (it % nslots),
+                                     (it / nslots) & 1, abort_flag, p, 2));
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok) break;
+          if (w.n[t] == 0) continue;
+          ok = __all_sync(0xffffffffu,
+                          wait_bounded(bar_q + 8 * t, q_uses[t] & 1,
+                                       abort_flag, p, 2));
+          if (!ok) break;
+          ++q_uses[t];
+          ptx::tc_fence_after();
+          const int b = s_issued % 3;
+          issue_qk(t, b, it % nslots);
+          ptx::tc_commit_elect(bar_s + 8 * (3 * t + b));
+          pbuf[t] = b;
+          ++s_issued;
+          if (w.n[t] == 1) ptx::tc_commit_elect(bar_qfree + 8 * t);
+          issued_any = true;
+        }
+        if (!ok) break;
+        ptx::tc_commit_elect(bar_empty + 8 * (it % nslots));
+        const int it0 = it;
+        for (int j = 0; j < w.n_kv && ok; ++j) {
+          const int it_v = it0 + 2 * j + 1;
+          const int slot_v = it_v % nslots;
+          const int it_k = it0 + 2 * j + 2;
+          const int slot_k = it_k % nslots;
+          ok = __all_sync(0xffffffffu,
+                          wait_bounded(bar_full + 8 * slot_v,
+                                       (it_v / nslots) & 1, abort_flag, p,
+                                       2));
+          if (!ok) break;
+          bool k_ready = false;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (!ok) break;
+            if (j >= w.n[t]) continue;
+            int nb = -1;
+            if (j + 1 < w.n[t]) {
+              if (!k_ready) {
+                ok = __all_sync(0xffffffffu,
+                                wait_bounded(bar_full + 8 * slot_k,
+                                             (it_k / nslots) & 1, abort_flag,
+                                             p, 2));
+                if (!ok) break;
+                k_ready = true;
+              }
+              ptx::tc_fence_after();
+              nb = s_issued % 3;
+              issue_qk(t, nb, slot_k);
+              ptx::tc_commit_elect(bar_s + 8 * (3 * t + nb));
+              ++s_issued;
+              if (j + 1 == w.n[t] - 1) ptx::tc_commit_elect(bar_qfree + 8 * t);
+            }
+            ok = __all_sync(0xffffffffu,
+                            wait_bounded(bar_p + 8 * t, p_waits[t] & 1,
+                                         abort_flag, p, 2));
+            if (!ok) break;
+            ++p_waits[t];
+            ptx::tc_fence_after();
+            issue_pv(t, pbuf[t], slot_v, j > 0);
+            ptx::tc_commit_elect(j == w.n[t] - 1 ? bar_o + 8 * t
+                                                 : bar_pvdone + 8 * t);
+            if (nb >= 0) pbuf[t] = nb;
+          }
+          if (!ok) break;
+          ptx::tc_commit_elect(bar_empty + 8 * slot_v);
+          if (j + 1 < w.n_kv) ptx::tc_commit_elect(bar_empty + 8 * slot_k);
+        }
+        it = it0 + 2 * w.n_kv;
         continue;
       }
       // S_t = Q_t K_0^T for both tiles.
@@ -677,7 +770,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
     const int t = warp / 4 - 1;             // Q tile of this warpgroup
     const int r = threadIdx.x % 128;        // row within the tile
     const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
-    const uint32_t t_o = tmem + lane_off + 2 * kTN + t * D;
+    const uint32_t t_o = tmem + lane_off + kOCol + t * D;
     const float c = p.scale_log2;
     // Packed query heads fill only group*Sq rows of the tile: a warp whose
     // 32 rows are all padding keeps in step (waits, arrivals) but computes
@@ -689,13 +782,19 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
     int s_waits = 0;   // S-ready phases consumed (packed: S region 0)
     int s_waits1 = 0;  // packed: S-ready phases of S region 1
     int o_waits = 0;   // O-done phases consumed
-    int pv_waits = 0;  // packed: per-step PV-done phases consumed
+    int pv_waits = 0;  // packed, kTriple: per-step PV-done phases consumed
+    int s_before = 0;           // kTriple: S MMAs of this CTA's earlier units
+    int s_uses[3] = {0, 0, 0};  // kTriple: this tile's uses of each buffer
 
     for (int k = 0; k * u_step < p.num_units && ok; ++k) {
       const int u = unit_index(k, u_first, u_step);
       if (u >= p.num_units) continue;
       const Unit w = decode_unit<kPack, kWindow>(p, u);
       const int n = t ? w.n[1] : w.n[0];
+      // kTriple: the MMA warp issues n[0] + n[1] S MMAs for this unit, in
+      // the order S_0(0), S_1(0), then S_0(j+1), S_1(j+1) during step j.
+      const int s_unit = s_before;
+      s_before += w.n[0] + w.n[1];
       if (n == 0) continue;
       const int ms = t ? w.ms[1] : w.ms[0];
       const int wl = kWindow ? (t ? w.wl[1] : w.wl[0]) : 0;
@@ -714,20 +813,40 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
       float l_run = 0.f;        // running sum of 2^(s*c - m_run)
 
       for (int j = 0; j < n; ++j) {
-        // S region of this step: the tile's own, or (packed) alternating.
-        const int sb = kPack ? (j & 1) : t;
+        // S region of this step: the tile's own, (packed) alternating, or
+        // (kTriple) the buffer of this tile's S MMA number s_unit + rel.
+        int sb = kPack ? (j & 1) : t;
+        if constexpr (kTriple) {
+          const int n0 = w.n[0], n1 = w.n[1];
+          int rel = 0;
+          if (j > 0)
+            rel = (n0 > 0) + (n1 > 0) + max(0, min(j - 1, n0 - 1)) +
+                  max(0, min(j - 1, n1 - 1));
+          if (t == 1 && j < n0) ++rel;
+          sb = (s_unit + rel) % 3;
+        }
         const uint32_t t_s = tmem + lane_off + sb * kTN;
         const bool odd = kPack && sb == 1;
-        ok = __all_sync(0xffffffffu,
-                        wait_bounded(bar_s + 8 * sb,
-                                     (odd ? s_waits1 : s_waits) & 1,
-                                     abort_flag, p, 3));
-        if (!ok) break;
-        if (odd) ++s_waits1; else ++s_waits;
+        if constexpr (kTriple) {
+          // One barrier per (tile, buffer): its phases are this tile's uses
+          // of the buffer only, each awaited in turn.
+          ok = __all_sync(0xffffffffu,
+                          wait_bounded(bar_s + 8 * (3 * t + sb),
+                                       s_uses[sb] & 1, abort_flag, p, 3));
+          if (!ok) break;
+          ++s_uses[sb];
+        } else {
+          ok = __all_sync(0xffffffffu,
+                          wait_bounded(bar_s + 8 * sb,
+                                       (odd ? s_waits1 : s_waits) & 1,
+                                       abort_flag, p, 3));
+          if (!ok) break;
+          if (odd) ++s_waits1; else ++s_waits;
+        }
         ptx::tc_fence_after();
         if (!live) {
           ptx::tc_fence_before();
-          ptx::mbar_arrive(bar_p + 8 * sb);
+          ptx::mbar_arrive(bar_p + 8 * (kTriple ? t : sb));
           continue;
         }
 
@@ -877,13 +996,13 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
           }
         }
 
-        if (kPack && j > 0) {
-          // Packed: S_j was issued before PV_{j-1}, so wait for that PV's
-          // own commit before O may be touched (every step, to keep the
-          // phases in step).
+        if ((kPack || kTriple) && j > 0) {
+          // Packed / kTriple: S_j was issued before PV_{j-1}, so wait for
+          // that PV's own commit before O may be touched (every step, to
+          // keep the phases in step).
           ok = __all_sync(0xffffffffu,
-                          wait_bounded(bar_o + 8, pv_waits & 1, abort_flag,
-                                       p, 3));
+                          wait_bounded(kTriple ? bar_pvdone + 8 * t : bar_o + 8,
+                                       pv_waits & 1, abort_flag, p, 3));
           if (!ok) break;
           ++pv_waits;
           ptx::tc_fence_after();
@@ -891,7 +1010,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
         if (j > 0 && __any_sync(0xffffffffu, m_new != m_run)) {
           // Correction: O_t *= alpha.  The previous PV into O_t is complete:
           // it was issued before this tile's S_t, whose commit we waited on
-          // (packed: its own commit, waited on just above).
+          // (packed, kTriple: its own commit, waited on just above).
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) {
             uint32_t o[32];
@@ -908,7 +1027,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
         l_run += (sm[0] + sm[1]) + (sm[2] + sm[3]);
         m_run = m_new;
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar_p + 8 * sb);
+        ptx::mbar_arrive(bar_p + 8 * (kTriple ? t : sb));
       }
       if (!ok) break;
 
