@@ -108,13 +108,6 @@ static_assert(128 * kRegsControl + 256 * kRegsSoftmax <=
 constexpr float kLn2 = 0.6931471805599453f;
 }  // namespace cfg
 
-// Compile-time flag passed to generic lambdas (selects a masked or an
-// unmasked copy of a loop).
-template <bool B>
-struct BoolTag {
-  static constexpr bool value = B;
-};
-
 // Shared memory of one CTA: Q tiles, the K/V slot ring, mbarriers.  The
 // packed variant has one Q tile and fills the rest of the 227 KB with ring
 // slots (a decode step is bound by the K/V bytes in flight per SM).  Rows

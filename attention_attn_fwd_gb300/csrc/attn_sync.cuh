@@ -8,6 +8,14 @@
 
 namespace attn {
 
+// Compile-time flag passed to generic lambdas, to compile a loop twice (for
+// instance with and without a mask test the compiler would otherwise turn
+// into a select on every element).
+template <bool B>
+struct BoolTag {
+  static constexpr bool value = B;
+};
+
 // Bounded wait.  Returns false if the CTA is aborting or the wait ran out.
 // After one immediate test the thread sleeps in try_wait (woken when the
 // phase completes, or after at most 20 us), so waiting warps do not take
