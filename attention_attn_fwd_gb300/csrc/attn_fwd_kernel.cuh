@@ -93,12 +93,12 @@ constexpr int kSoftmaxWarp0 = 4;  // warps 4-7: Q tile 0, warps 8-11: Q tile 1
 constexpr int kTmemCols = 512;
 constexpr float kRescaleTau = 8.0f;  // lazy rescale threshold (log2 units)
 // Register split of the variants that hold a whole S row (128 fp32) in
-// registers from the max pass to the exp pass (the sliding-window ones,
-// where it measured 4 % faster; elsewhere re-reading S from TMEM was 2 %
-// faster): the launch gives every thread kRegsLaunch; warpgroup 0 (MMA
-// issuer, producer, two idle warps) drops to kRegsControl and the two
-// softmax warpgroups rise to kRegsSoftmax.  The shares must add up to the
-// launch allocation exactly, or the increase would wait forever.
+// registers from the max pass to the exp pass (all two-tile variants: 1-5 %
+// faster than re-reading S from TMEM; the packed ones re-read): the launch
+// gives every thread kRegsLaunch; warpgroup 0 (MMA issuer, producer, two
+// idle warps) drops to kRegsControl and the two softmax warpgroups rise to
+// kRegsSoftmax.  The shares must add up to the launch allocation exactly,
+// or the increase would wait forever.
 constexpr int kRegsLaunch = 168;
 constexpr int kRegsControl = 72;
 constexpr int kRegsSoftmax = 216;
@@ -366,7 +366,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
                           const FwdParams p) {
   static_assert(!kFp8 || kBF16, "FP8 inputs give a bf16 output");
   using L = Layout<D, kPack, kFp8>;
-  constexpr bool kHoldS = kWindow;  // S row kept in registers (see cfg)
+  constexpr bool kHoldS = !kPack;  // S row kept in registers (see cfg)
   // Three S buffers shared by the two Q tiles (D = 64: O needs 128 columns).
   constexpr bool kTriple = D == 64 && !kPack;
   constexpr int kOCol = kTriple ? 3 * cfg::kTN : 2 * cfg::kTN;  // first O column

@@ -26,7 +26,7 @@ cudaError_t launch_variant(const CUtensorMap& q, const CUtensorMap& k,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                smem);
     if (err != cudaSuccess) return err;
-    if constexpr (kWindow) {
+    if constexpr (!kPack) {
       // These variants split the launch's registers with setmaxnreg, which
       // only adds up when every thread launches with cfg::kRegsLaunch: a
       // build that allocated fewer would leave the increase waiting
