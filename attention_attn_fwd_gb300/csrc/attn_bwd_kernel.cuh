@@ -107,6 +107,21 @@ __device__ __forceinline__ void ffma2v(float& y0, float& y1, float x0,
       : "f"(x0), "f"(x1), "f"(m), "f"(a0), "f"(a1));
 }
 
+// ((a0, a1) - (b0, b1)) * (p0, p1) as two packed f32x2 instructions (four
+// scalar ones would take the FMA pipe's issue slots twice).
+__device__ __forceinline__ void sub_mul2(float& y0, float& y1, float a0,
+                                         float a1, float b0, float b1,
+                                         float p0, float p1) {
+  asm("{\n\t.reg .b64 a, b, pp, y;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "mov.b64 pp, {%6, %7};\n\t"
+      "sub.rn.ftz.f32x2 y, a, b;\n\t"
+      "mul.rn.ftz.f32x2 y, y, pp;\n\t"
+      "mov.b64 {%0, %1}, y;\n\t}"
+      : "=f"(y0), "=f"(y1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(p0), "f"(p1));
+}
+
 // 16-bit pair (as packed by ptx::pack2) back to two floats.
 template <bool kBF16>
 __device__ __forceinline__ float2 unpack2(uint32_t v) {
@@ -696,9 +711,11 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const float2 pp = unpack2<kBF16>(pk[16 * k + e]);
-          dk[16 * k + e] = ptx::pack2<kBF16>(
-              pp.x * (__uint_as_float(dv[2 * e]) - dl[2 * e]),
-              pp.y * (__uint_as_float(dv[2 * e + 1]) - dl[2 * e + 1]));
+          float d0, d1;
+          sub_mul2(d0, d1, __uint_as_float(dv[2 * e]),
+                   __uint_as_float(dv[2 * e + 1]), dl[2 * e], dl[2 * e + 1],
+                   pp.x, pp.y);
+          dk[16 * k + e] = ptx::pack2<kBF16>(d0, d1);
         }
       }
       ptx::mbar_arrive(bar_ve);  // done with this step's vectors
@@ -1044,9 +1061,10 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const float2 pp = unpack2<kBF16>(pk[16 * kh + e]);
-          dk[16 * kh + e] =
-              ptx::pack2<kBF16>(pp.x * (__uint_as_float(dv[2 * e]) - dlt),
-                                pp.y * (__uint_as_float(dv[2 * e + 1]) - dlt));
+          float d0, d1;
+          sub_mul2(d0, d1, __uint_as_float(dv[2 * e]),
+                   __uint_as_float(dv[2 * e + 1]), dlt, dlt, pp.x, pp.y);
+          dk[16 * kh + e] = ptx::pack2<kBF16>(d0, d1);
         }
       }
       ptx::mbar_arrive(bar_x);
