@@ -19,15 +19,18 @@
 //   warps 2-3  idle
 //   warps 4-7  softmax + correction + epilogue for Q tile 0 (TMEM lanes 0-127)
 //   warps 8-11 the same for Q tile 1
+// In the two-tile variants warps 0-3 give up registers (setmaxnreg) so that
+// each softmax thread holds its row's 128 scores between the max and exp
+// passes.
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 and O1 (D columns each)
 // from 256.  P_t (16-bit) overwrites the first 64 columns of S_t and is the
 // A operand of O_t += P_t V straight from TMEM.  At D = 64 the O tiles need
 // only 128 columns, so three S buffers [0,384) rotate between the two Q
 // tiles and O starts at 384: a tile's next S goes to the free buffer and is
-// computed while its softmax still works on the current one.  With the query heads of a
-// GQA group packed into tile 0 (few query rows), there is no tile 1: its S
-// region double-buffers the scores of tile 0 and its shared memory goes to
-// the K/V ring.
+// computed while its softmax still works on the current one.  With the
+// query heads of a GQA group packed into tile 0 (few query rows), there is
+// no tile 1: its S region double-buffers the scores of tile 0 and its
+// shared memory goes to the K/V ring.
 //
 // Every mbarrier wait is bounded: on timeout the waiter raises a CTA-wide
 // abort flag and a device status word, every role stops issuing work, waits
