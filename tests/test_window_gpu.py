@@ -34,6 +34,7 @@ CASES = [
     # two heads per CTA (even group), same rows
     W("pair_w129", 1, 8, 2, 700, 700, 128, "bf16", 0, 129),
     W("pair_offset_w384", 1, 4, 2, 300, 1100, 128, "bf16", 800, 384),
+    W("pair_d64_w200", 1, 8, 2, 600, 900, 64, "bf16", 300, 200),
     # 256 rows of one head per CTA
     W("rows_w200", 1, 4, 4, 600, 600, 64, "f16", 0, 200),
     W("rows_odd_group_w333", 1, 3, 1, 260, 900, 64, "f16", 500, 333),
