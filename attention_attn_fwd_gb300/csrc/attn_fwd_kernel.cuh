@@ -774,7 +774,12 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
     const int r = threadIdx.x % 128;        // row within the tile
     const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const uint32_t t_o = tmem + lane_off + kOCol + t * D;
-    const float c = p.scale_log2;
+    // Score factor (log2 units).  A zero scale is replaced by 1e-30: the
+    // weights stay uniform (every score times it is far below one ulp of
+    // the exponent), and a masked -inf score times it stays -inf instead of
+    // becoming NaN, so the exp pass needs no mask of its own once pass 1
+    // has written -inf into the held scores.
+    const float c = p.scale_log2 > 0.f ? p.scale_log2 : 1e-30f;
     // Packed query heads fill only group*Sq rows of the tile: a warp whose
     // 32 rows are all padding keeps in step (waits, arrivals) but computes
     // nothing.  Its P rows stay whatever S left there, which only reaches
@@ -932,12 +937,12 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
         // chunk's load in flight while this one is computed (P chunk q only
         // overwrites S columns already consumed).  The row sum is taken from
         // the fp32 P.  P <= 2^tau = 256 stays inside E4M3's range (448).
-        // Masked columns are forced to -inf after the scaling (a zero scale
-        // would turn the -inf of pass 1 into NaN).  The pass is compiled
-        // twice, with and without the mask test: left to the compiler, the
-        // test inside the unrolled loop became a compare and select on every
-        // score of every tile (about 2 ALU instructions per score, 15 % of
-        // the step time), though only tiles at the causal edge need it.
+        // Held scores (kHoldS) carry pass 1's -inf into the exp pass.
+        // Re-read ones (packed) are masked again after the scaling, in a
+        // second copy of the pass used only for masked tiles: left to the
+        // compiler, the mask test inside the unrolled loop became a compare
+        // and select on every score of every tile (about 2 ALU instructions
+        // per score, 15 % of the step time).
         const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
         float sm[4] = {0.f, 0.f, 0.f, 0.f};
         auto exp_pass = [&](auto mask_tag) {
@@ -1003,10 +1008,15 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
             }
           }
         };
-        if (masked)
-          exp_pass(BoolTag<true>{});
-        else
+        if constexpr (kHoldS) {
+          // Masked columns already hold -inf (pass 1).
           exp_pass(BoolTag<false>{});
+        } else {
+          if (masked)
+            exp_pass(BoolTag<true>{});
+          else
+            exp_pass(BoolTag<false>{});
+        }
 
         if ((kPack || kTriple) && j > 0) {
           // Packed / kTriple: S_j was issued before PV_{j-1}, so wait for
