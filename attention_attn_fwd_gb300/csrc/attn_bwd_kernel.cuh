@@ -500,7 +500,8 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       }
       const long long vbase =
           static_cast<long long>(qplane0 + hm / p.q_tiles) * p.sq_pad + m * kT;
-      const float4 l4 = reinterpret_cast<const float4*>(p.lse2 + vbase)[lane];
+      float4 l4 = reinterpret_cast<const float4*>(p.lse2 + vbase)[lane];
+      l4.x = -l4.x; l4.y = -l4.y; l4.z = -l4.z; l4.w = -l4.w;
       const float4 d4 = reinterpret_cast<const float4*>(p.delta + vbase)[lane];
       reinterpret_cast<float4*>(vec)[lane] = l4;
       reinterpret_cast<float4*>(vec + kT)[lane] = d4;
@@ -649,34 +650,42 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       if (!ok) break;
       ptx::tc_fence_after();
       uint32_t pk[32];
+      uint32_t sv[2][32];
+      ptx::tmem_ld32(t_st + 32 * (2 * h), sv[0]);
+      ptx::tmem_ld32(t_st + 32 * (2 * h + 1), sv[1]);
+      ptx::tmem_wait_ld();
+      auto p_pass = [&](auto mask_tag) {
+        constexpr bool kMasked = decltype(mask_tag)::value;
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int q = 2 * h + k;
-        uint32_t sv[32];
-        ptx::tmem_ld32(t_st + 32 * q, sv);
-        float lv[32];
+        for (int k = 0; k < 2; ++k) {
+          const int q = 2 * h + k;
+          float lv[32];  // -lse2 of the query columns
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 t4 = v_l[8 * q + i];
-          lv[4 * i] = t4.x;
-          lv[4 * i + 1] = t4.y;
-          lv[4 * i + 2] = t4.z;
-          lv[4 * i + 3] = t4.w;
-        }
-        ptx::tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int j = 32 * q + 2 * e;
-          float x0, x1;
-          ffma2v(x0, x1, __uint_as_float(sv[2 * e]),
-                 __uint_as_float(sv[2 * e + 1]), c, -lv[2 * e], -lv[2 * e + 1]);
-          if (!full) {
-            if (static_cast<unsigned>(j - jlo) >= span) x0 = -INFINITY;
-            if (static_cast<unsigned>(j + 1 - jlo) >= span) x1 = -INFINITY;
+          for (int i = 0; i < 8; ++i) {
+            const float4 t4 = v_l[8 * q + i];
+            lv[4 * i] = t4.x;
+            lv[4 * i + 1] = t4.y;
+            lv[4 * i + 2] = t4.z;
+            lv[4 * i + 3] = t4.w;
           }
-          pk[16 * k + e] = ptx::pack2<kBF16>(ptx::ex2(x0), ptx::ex2(x1));
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int j = 32 * q + 2 * e;
+            float x0, x1;
+            ffma2v(x0, x1, __uint_as_float(sv[k][2 * e]),
+                   __uint_as_float(sv[k][2 * e + 1]), c, lv[2 * e], lv[2 * e + 1]);
+            if constexpr (kMasked) {
+              if (static_cast<unsigned>(j - jlo) >= span) x0 = -INFINITY;
+              if (static_cast<unsigned>(j + 1 - jlo) >= span) x1 = -INFINITY;
+            }
+            pk[16 * k + e] = ptx::pack2<kBF16>(ptx::ex2(x0), ptx::ex2(x1));
+          }
         }
-      }
+      };
+      if (full)
+        p_pass(BoolTag<false>{});
+      else
+        p_pass(BoolTag<true>{});
       ptx::mbar_arrive(bar_xa);
       ok = __all_sync(0xffffffffu,
                       wait_bounded(bar_xa, s & 1, abort_flag, p, 3));
@@ -1027,43 +1036,51 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       ptx::tc_fence_after();
       const uint32_t t_s = tmem + lane_off + (s & 1) * kT;
       uint32_t pk[32];
+      uint32_t sv[2][32];
+      ptx::tmem_ld32(t_s + 32 * (2 * h), sv[0]);
+      ptx::tmem_ld32(t_s + 32 * (2 * h + 1), sv[1]);
+      ptx::tmem_wait_ld();
+      auto p_pass = [&](auto mask_tag) {
+        constexpr bool kMasked = decltype(mask_tag)::value;
 #pragma unroll
-      for (int kh = 0; kh < 2; ++kh) {
-        const int q = 2 * h + kh;
-        uint32_t sv[32];
-        ptx::tmem_ld32(t_s + 32 * q, sv);
-        ptx::tmem_wait_ld();
+        for (int kh = 0; kh < 2; ++kh) {
+          const int q = 2 * h + kh;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int k = 32 * q + 2 * e;
-          float x0, x1;
-          ptx::ffma2(x0, x1, __uint_as_float(sv[2 * e]),
-                     __uint_as_float(sv[2 * e + 1]), c, neg_l);
-          if (!full) {
-            if (static_cast<unsigned>(k - lo) >= span) x0 = -INFINITY;
-            if (static_cast<unsigned>(k + 1 - lo) >= span) x1 = -INFINITY;
+          for (int e = 0; e < 16; ++e) {
+            const int k = 32 * q + 2 * e;
+            float x0, x1;
+            ptx::ffma2(x0, x1, __uint_as_float(sv[kh][2 * e]),
+                       __uint_as_float(sv[kh][2 * e + 1]), c, neg_l);
+            if constexpr (kMasked) {
+              if (static_cast<unsigned>(k - lo) >= span) x0 = -INFINITY;
+              if (static_cast<unsigned>(k + 1 - lo) >= span) x1 = -INFINITY;
+            }
+            pk[16 * kh + e] = ptx::pack2<kBF16>(ptx::ex2(x0), ptx::ex2(x1));
           }
-          pk[16 * kh + e] = ptx::pack2<kBF16>(ptx::ex2(x0), ptx::ex2(x1));
         }
-      }
+      };
+      if (full)
+        p_pass(BoolTag<false>{});
+      else
+        p_pass(BoolTag<true>{});
       // dS = P (dP - D), 16-bit, over dP.
       ok = __all_sync(0xffffffffu,
                       wait_bounded(bar_dp, s & 1, abort_flag, p, 3));
       if (!ok) break;
       ptx::tc_fence_after();
       uint32_t dk[32];
+      uint32_t dv[2][32];
+      ptx::tmem_ld32(t_dp + 32 * (2 * h), dv[0]);
+      ptx::tmem_ld32(t_dp + 32 * (2 * h + 1), dv[1]);
+      ptx::tmem_wait_ld();
 #pragma unroll
       for (int kh = 0; kh < 2; ++kh) {
-        const int q = 2 * h + kh;
-        uint32_t dv[32];
-        ptx::tmem_ld32(t_dp + 32 * q, dv);
-        ptx::tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const float2 pp = unpack2<kBF16>(pk[16 * kh + e]);
           float d0, d1;
-          sub_mul2(d0, d1, __uint_as_float(dv[2 * e]),
-                   __uint_as_float(dv[2 * e + 1]), dlt, dlt, pp.x, pp.y);
+          sub_mul2(d0, d1, __uint_as_float(dv[kh][2 * e]),
+                   __uint_as_float(dv[kh][2 * e + 1]), dlt, dlt, pp.x, pp.y);
           dk[16 * kh + e] = ptx::pack2<kBF16>(d0, d1);
         }
       }
