@@ -653,6 +653,15 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       uint32_t sv[2][32];
       ptx::tmem_ld32(t_st + 32 * (2 * h), sv[0]);
       ptx::tmem_ld32(t_st + 32 * (2 * h + 1), sv[1]);
+      float lv0[32];  // -lse2 of the first chunk's query columns
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 t4 = v_l[8 * (2 * h) + i];
+        lv0[4 * i] = t4.x;
+        lv0[4 * i + 1] = t4.y;
+        lv0[4 * i + 2] = t4.z;
+        lv0[4 * i + 3] = t4.w;
+      }
       ptx::tmem_wait_ld();
       auto p_pass = [&](auto mask_tag) {
         constexpr bool kMasked = decltype(mask_tag)::value;
@@ -662,11 +671,18 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
           float lv[32];  // -lse2 of the query columns
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const float4 t4 = v_l[8 * q + i];
-            lv[4 * i] = t4.x;
-            lv[4 * i + 1] = t4.y;
-            lv[4 * i + 2] = t4.z;
-            lv[4 * i + 3] = t4.w;
+            if (k == 0) {
+              lv[4 * i] = lv0[4 * i];
+              lv[4 * i + 1] = lv0[4 * i + 1];
+              lv[4 * i + 2] = lv0[4 * i + 2];
+              lv[4 * i + 3] = lv0[4 * i + 3];
+            } else {
+              const float4 t4 = v_l[8 * q + i];
+              lv[4 * i] = t4.x;
+              lv[4 * i + 1] = t4.y;
+              lv[4 * i + 2] = t4.z;
+              lv[4 * i + 3] = t4.w;
+            }
           }
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -702,27 +718,44 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       if (!ok) break;
       ptx::tc_fence_after();
       uint32_t dk[32];
+      uint32_t dv[2][32];
+      ptx::tmem_ld32(t_dpt + 32 * (2 * h), dv[0]);
+      ptx::tmem_ld32(t_dpt + 32 * (2 * h + 1), dv[1]);
+      float dl0[32];  // D of the first chunk's query columns
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 t4 = v_d[8 * (2 * h) + i];
+        dl0[4 * i] = t4.x;
+        dl0[4 * i + 1] = t4.y;
+        dl0[4 * i + 2] = t4.z;
+        dl0[4 * i + 3] = t4.w;
+      }
+      ptx::tmem_wait_ld();
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int q = 2 * h + k;
-        uint32_t dv[32];
-        ptx::tmem_ld32(t_dpt + 32 * q, dv);
         float dl[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float4 t4 = v_d[8 * q + i];
-          dl[4 * i] = t4.x;
-          dl[4 * i + 1] = t4.y;
-          dl[4 * i + 2] = t4.z;
-          dl[4 * i + 3] = t4.w;
+          if (k == 0) {
+            dl[4 * i] = dl0[4 * i];
+            dl[4 * i + 1] = dl0[4 * i + 1];
+            dl[4 * i + 2] = dl0[4 * i + 2];
+            dl[4 * i + 3] = dl0[4 * i + 3];
+          } else {
+            const float4 t4 = v_d[8 * q + i];
+            dl[4 * i] = t4.x;
+            dl[4 * i + 1] = t4.y;
+            dl[4 * i + 2] = t4.z;
+            dl[4 * i + 3] = t4.w;
+          }
         }
-        ptx::tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const float2 pp = unpack2<kBF16>(pk[16 * k + e]);
           float d0, d1;
-          sub_mul2(d0, d1, __uint_as_float(dv[2 * e]),
-                   __uint_as_float(dv[2 * e + 1]), dl[2 * e], dl[2 * e + 1],
+          sub_mul2(d0, d1, __uint_as_float(dv[k][2 * e]),
+                   __uint_as_float(dv[k][2 * e + 1]), dl[2 * e], dl[2 * e + 1],
                    pp.x, pp.y);
           dk[16 * k + e] = ptx::pack2<kBF16>(d0, d1);
         }
