@@ -270,8 +270,8 @@ struct DkdvLayout : BwdTiles<D> {
   static constexpr int kVecOff = kDoOff + kDoSlots * T::kTileBytes;
   static constexpr int kBarOff = kVecOff + 2 * bwd::kT * 4;
   // kv_full, q_full[QS], q_empty[QS], do_full[DS], do_empty[DS], s_ready,
-  // dp_ready, p_ready, ds_ready, acc_done, drain, xa, xb, vec_full, vec_free
-  static constexpr int kNumBars = 1 + 2 * kQSlots + 2 * kDoSlots + 10;
+  // dp_ready, p_ready, ds_ready, acc_done, drain, vec_full, vec_free
+  static constexpr int kNumBars = 1 + 2 * kQSlots + 2 * kDoSlots + 8;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -293,8 +293,8 @@ struct DqLayout : BwdTiles<D> {
   static constexpr int kVOff = kKOff + kKSlots * T::kTileBytes;
   static constexpr int kBarOff = kVOff + kVSlots * T::kTileBytes;
   // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_ready[2],
-  // dp_ready, ds_ready, acc_done, drain, x
-  static constexpr int kNumBars = 1 + 2 * kKSlots + 2 * kVSlots + 7;
+  // dp_ready, ds_ready, acc_done, drain
+  static constexpr int kNumBars = 1 + 2 * kKSlots + 2 * kVSlots + 6;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -388,9 +388,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
   const uint32_t bar_ds = bar_p + 8;
   const uint32_t bar_acc = bar_ds + 8;
   const uint32_t bar_drain = bar_acc + 8;
-  const uint32_t bar_xa = bar_drain + 8;  // both halves loaded S^T
-  const uint32_t bar_xb = bar_xa + 8;     // both halves loaded dP^T
-  const uint32_t bar_vf = bar_xb + 8;     // step vectors staged
+  const uint32_t bar_vf = bar_drain + 8;  // step vectors staged
   const uint32_t bar_ve = bar_vf + 8;     // step vectors consumed
   float* vec = reinterpret_cast<float*>(smem + L::kVecOff);  // lse2, D
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
@@ -408,8 +406,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumBars; ++i) {
       const uint32_t bar = bar0 + 8 * i;
-      const bool work = bar == bar_p || bar == bar_ds || bar == bar_xa ||
-                        bar == bar_xb || bar == bar_ve;
+      const bool work = bar == bar_p || bar == bar_ds || bar == bar_ve;
       ptx::mbar_init(bar, work ? kWork : 1);
     }
     *abort_flag = 0;
@@ -551,7 +548,8 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
                          bool acc) {
 #pragma unroll
       for (int kk = 0; kk < kT / 16; ++kk)
-        ptx::mma_ts_elect(d, a_tmem + kk * 8, b_mn + ((kk * 16 * 128) >> 4),
+        ptx::mma_ts_elect(d, a_tmem + (kk / 4) * 64 + (kk % 4) * 8,
+                          b_mn + ((kk * 16 * 128) >> 4),
                           kHi, idesc_acc, (acc || kk > 0) ? 1u : 0u);
     };
     bool ok = __all_sync(0xffffffffu,
@@ -617,9 +615,11 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     __syncwarp();
   } else if (warp >= kWorkWarp0) {
     // ----------------------------------------- P^T, dS^T and epilogue
-    // Half h takes query columns [64h, 64h+64) of its key row.  A half's
-    // 16-bit stores land on fp32 columns the other half reads, so each pass
-    // loads all it needs, the halves meet on an mbarrier, then store.
+    // Half h takes query columns [64h, 64h+64) of its key row.  Each pass
+    // loads both of the half's 32-column chunks before one wait, then
+    // stores its 16-bit results into the first 32 of those 64 columns,
+    // which no other warp reads: the halves never wait for each other.
+    // The dV / dK MMAs read P^T / dS^T from columns 0..31 and 64..95.
     const int h = (warp - kWorkWarp0) / 4;
     const int r = (warp % 4) * 32 + lane;  // key row in the tile
     const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
@@ -702,13 +702,10 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
         p_pass(BoolTag<false>{});
       else
         p_pass(BoolTag<true>{});
-      ptx::mbar_arrive(bar_xa);
-      ok = __all_sync(0xffffffffu,
-                      wait_bounded(bar_xa, s & 1, abort_flag, p, 3));
-      if (!ok) break;
-      // 16-bit P^T of query columns 64h.. into TMEM columns 32h..
-      ptx::tmem_st16(t_st + 32 * h, pk);
-      ptx::tmem_st16(t_st + 32 * h + 16, pk + 16);
+      // 16-bit P^T of query columns 64h.. into TMEM columns 64h..64h+31,
+      // which only this half has read.
+      ptx::tmem_st16(t_st + 64 * h, pk);
+      ptx::tmem_st16(t_st + 64 * h + 16, pk + 16);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar_p);
@@ -761,12 +758,8 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
         }
       }
       ptx::mbar_arrive(bar_ve);  // done with this step's vectors
-      ptx::mbar_arrive(bar_xb);
-      ok = __all_sync(0xffffffffu,
-                      wait_bounded(bar_xb, s & 1, abort_flag, p, 3));
-      if (!ok) break;
-      ptx::tmem_st16(t_dpt + 32 * h, dk);
-      ptx::tmem_st16(t_dpt + 32 * h + 16, dk + 16);
+      ptx::tmem_st16(t_dpt + 64 * h, dk);
+      ptx::tmem_st16(t_dpt + 64 * h + 16, dk + 16);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar_ds);
@@ -838,7 +831,6 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
   const uint32_t bar_ds = bar_dp + 8;
   const uint32_t bar_acc = bar_ds + 8;
   const uint32_t bar_drain = bar_acc + 8;
-  const uint32_t bar_x = bar_drain + 8;  // both halves loaded dP
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<int*>(smem + L::kMiscOff + 4);
 
@@ -852,7 +844,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumBars; ++i) {
       const uint32_t bar = bar0 + 8 * i;
-      ptx::mbar_init(bar, (bar == bar_ds || bar == bar_x) ? kWork : 1);
+      ptx::mbar_init(bar, bar == bar_ds ? kWork : 1);
     }
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -999,7 +991,8 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       const uint32_t k_mn = ptx::sdesc_lo(k_tile(s), L::kBoxBytes);
 #pragma unroll
       for (int kk = 0; kk < kT / 16; ++kk)
-        ptx::mma_ts_elect(t_dq, t_dp + kk * 8, k_mn + ((kk * 16 * 128) >> 4),
+        ptx::mma_ts_elect(t_dq, t_dp + (kk / 4) * 64 + (kk % 4) * 8,
+                          k_mn + ((kk * 16 * 128) >> 4),
                           kHi, idesc_acc, (s > 0 || kk > 0) ? 1u : 0u);
       ptx::tc_commit_elect(bar_ke + 8 * (s % L::kKSlots));
       // dP(s+1) into the dP region (after dQ(s) in issue order).
@@ -1032,9 +1025,10 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     __syncwarp();
   } else if (warp >= kWorkWarp0) {
     // -------------------------------------------- dS and the epilogue
-    // Half h takes key columns [64h, 64h+64) of its query row; the 16-bit
-    // dS stores land on fp32 dP columns the other half reads, so the halves
-    // meet on an mbarrier between loading dP and storing dS.
+    // Half h takes key columns [64h, 64h+64) of its query row; its 16-bit
+    // dS goes into the first 32 of those dP columns, after both of its dP
+    // chunks are loaded, so the halves never wait for each other.  The dQ
+    // MMA reads dS from columns 0..31 and 64..95.
     const int h = (warp - kWorkWarp0) / 4;
     const int r = (warp % 4) * 32 + lane;  // query row in the tile
     const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
@@ -1117,12 +1111,8 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
           dk[16 * kh + e] = ptx::pack2<kBF16>(d0, d1);
         }
       }
-      ptx::mbar_arrive(bar_x);
-      ok = __all_sync(0xffffffffu,
-                      wait_bounded(bar_x, s & 1, abort_flag, p, 3));
-      if (!ok) break;
-      ptx::tmem_st16(t_dp + 32 * h, dk);
-      ptx::tmem_st16(t_dp + 32 * h + 16, dk + 16);
+      ptx::tmem_st16(t_dp + 64 * h, dk);
+      ptx::tmem_st16(t_dp + 64 * h + 16, dk + 16);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar_ds);
