@@ -47,7 +47,8 @@ cudaError_t side_stream(SideStream** out) {
 }
 
 template <class Kernel>
-cudaError_t set_smem(Kernel kernel, int smem, int* configured) {
+cudaError_t set_smem(Kernel kernel, int smem, int* configured,
+                     int regs_required = 0) {
   // The attribute is per device; set it once per device and kernel.
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -57,6 +58,14 @@ cudaError_t set_smem(Kernel kernel, int smem, int* configured) {
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                smem);
     if (err != cudaSuccess) return err;
+    if (regs_required > 0) {
+      // A kernel that splits its registers with setmaxnreg needs exactly
+      // the launch allocation the split adds up to.
+      cudaFuncAttributes attr{};
+      err = cudaFuncGetAttributes(&attr, kernel);
+      if (err != cudaSuccess) return err;
+      if (attr.numRegs != regs_required) return cudaErrorInvalidConfiguration;
+    }
     *configured = dev;
   }
   return cudaSuccess;
@@ -97,11 +106,11 @@ cudaError_t run(const CUtensorMap& q, const CUtensorMap& k,
 
   auto dkdv = attn_bwd_dkdv_kernel<D, kBF16>;
   const int smem_kv = DkdvLayout<D>::kSmemBytes;
-  err = set_smem(dkdv, smem_kv, &cfg_dkdv);
+  err = set_smem(dkdv, smem_kv, &cfg_dkdv, 168);
   if (err != cudaSuccess) return err;
   auto dq = attn_bwd_dq_kernel<D, kBF16>;
   const int smem_q = DqLayout<D>::kSmemBytes;
-  err = set_smem(dq, smem_q, &cfg_dq);
+  err = set_smem(dq, smem_q, &cfg_dq, 168);
   if (err != cudaSuccess) return err;
   SideStream* side = nullptr;
   err = side_stream(&side);

@@ -21,11 +21,13 @@
 // is deterministic.
 //
 // Roles (384 threads): warp 0 TMEM allocator and tcgen05.mma issuer, warp 1
-// TMA producer, warps 4-11 the element-wise work and the epilogue -- two
-// warpgroups on the same TMEM rows (one row per thread), each taking 64 of
-// a tile's 128 columns, so that two warps per scheduler hide each other's
-// latencies; warps 2-3 idle.  Every mbarrier wait is bounded as in the
-// forward kernel.
+// TMA producer, warp 2 (dK/dV kernel) per-step vector staging, warps 4-11
+// the element-wise work and the epilogue -- two warpgroups on the same TMEM
+// rows (one row per thread), each taking 64 of a tile's 128 columns, so
+// that two warps per scheduler hide each other's latencies.  Warps 0-3 give
+// up registers with setmaxnreg (72 each) so that the element-wise warps get
+// 216: the launch allocation of 168 per thread, split.  Every mbarrier wait
+// is bounded as in the forward kernel.
 #pragma once
 
 #include <cstdint>
@@ -353,8 +355,9 @@ __device__ __forceinline__ void store_cols(uint32_t t_acc, float mul,
 // see the most queries, so they start first), (b, K/V head) = u % (B*Hkv).
 // Steps: the (query head of the group, query tile m) pairs that see tile
 // n, in order.  TMEM: S^T [0,128), dP^T [128,256), dV [256,256+D),
-// dK [256+D, 256+2D); P^T and dS^T (16-bit) overwrite the first 64 columns
-// of S^T and dP^T and are the A operands of dV += P^T dO and dK += dS^T Q.
+// dK [256+D, 256+2D); P^T and dS^T (16-bit) overwrite columns 0-31 and
+// 64-95 of S^T and dP^T and are the A operands of dV += P^T dO and
+// dK += dS^T Q.
 // Software pipeline: the element-wise pass is split at "P ready" and "dS
 // ready" (P stays in registers, 16-bit, for the dS half), so the tensor
 // pipe runs dV(s) and S^T(s+1) while dS(s) is computed, and dK(s) and
@@ -421,6 +424,8 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  if (warp < kWorkWarp0) {
+  ptx::setmaxnreg_dec<72>();
   if (warp == kLoadWarp) {
     // -------------------------------------------------------- producer
     if (lane == 0) {
@@ -613,7 +618,9 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       drain_wait(bar_drain, 0, p);
     }
     __syncwarp();
-  } else if (warp >= kWorkWarp0) {
+  }
+  } else {
+    ptx::setmaxnreg_inc<216>();
     // ----------------------------------------- P^T, dS^T and epilogue
     // Half h takes query columns [64h, 64h+64) of its key row.  Each pass
     // loads both of the half's 32-column chunks before one wait, then
@@ -799,7 +806,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
 // last rows see the most keys), plane (b, query head) = u % (B*Hq).  Steps:
 // the key tiles n that tile m sees, in order.  TMEM: S double-buffered in
 // [0,128) and [128,256), dP [256,384), dQ [384,384+D); dS (16-bit)
-// overwrites the first 64 columns of dP and is the A operand of
+// overwrites columns 0-31 and 64-95 of dP and is the A operand of
 // dQ += dS K.  Software pipeline: S(s+2) is issued as soon as step s's
 // element-wise pass is done, so P(s+1) can be computed while the tensor
 // pipe runs dQ(s) and dP(s+1).
@@ -858,6 +865,8 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  if (warp < kWorkWarp0) {
+  ptx::setmaxnreg_dec<72>();
   if (warp == kLoadWarp) {
     // -------------------------------------------------------- producer
     if (lane == 0) {
@@ -1023,7 +1032,9 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       drain_wait(bar_drain, 0, p);
     }
     __syncwarp();
-  } else if (warp >= kWorkWarp0) {
+  }
+  } else {
+    ptx::setmaxnreg_inc<216>();
     // -------------------------------------------- dS and the epilogue
     // Half h takes key columns [64h, 64h+64) of its query row; its 16-bit
     // dS goes into the first 32 of those dP columns, after both of its dP
