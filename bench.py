@@ -601,6 +601,93 @@ def run_window(args):
         print(json.dumps(out), flush=True)
 
 
+# ------------------------------------------------------ per-config table
+def run_table(args):
+    """Every named forward workload (the small case, causal MHA 4k, causal
+    GQA 8k, the KV-cache prefill chunk, the B4 H16 non-causal sweep) timed
+    the same way as the headline line: L2 flushed between steps, CUDA events
+    around each launch, medians and 95th percentiles.  One JSON line whose
+    `table` lists the configurations; `value` repeats the GQA 8k median."""
+    import torch
+
+    import attention_attn_fwd_gb300 as attn
+    from attention_attn_fwd_gb300.inputs import ALL, GQA_8K, make_qkv
+
+    ws, rank, local = dist_info()
+    if ws > 1:
+        torch.cuda.set_device(local)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    peak, _, src = peaks()
+    rows, headline = [], None
+    with ClockSampler(dev.index) as clocks:
+        for w in ALL:
+            q, k, v = (t.to(dev) for t in make_qkv(w, seed=0))
+            o = torch.empty_like(q)
+            lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32,
+                              device=dev)
+            dt = attn.ATTN_BF16 if w.dtype == "bf16" else attn.ATTN_F16
+
+            def step():
+                st = attn.attn_fwd(
+                    q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                    lse.data_ptr(), w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D,
+                    w.scale, int(w.causal), w.input_pos, dt,
+                    stream.cuda_stream)
+                if st != attn.ATTN_OK:
+                    raise RuntimeError("attn_fwd: " +
+                                       attn.attn_status_string(st))
+
+            for _ in range(args.warmup):
+                flush.fill_(1.0)
+                step()
+            torch.cuda.synchronize()
+            ev = [(torch.cuda.Event(enable_timing=True),
+                   torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+            for i, (a_, b_) in enumerate(ev):
+                flush.fill_(float(i))
+                a_.record(stream)
+                step()
+                b_.record(stream)
+            torch.cuda.synchronize()
+            t = sorted(a_.elapsed_time(b_) for a_, b_ in ev)
+            p50, p95 = t[len(t) // 2], t[min(len(t) - 1, int(0.95 * len(t)))]
+            tf = w.flops() / (p50 * 1e-3) / 1e12
+            rows.append({
+                "workload": w.name, "ms_p50": round(p50, 5),
+                "ms_p95": round(p95, 5), "tflops": round(tf, 1),
+                "tflops_exact": round(w.exact_flops() / (p50 * 1e-3) / 1e12,
+                                      1),
+                "pct_of_peak": round(100.0 * tf / peak, 2)})
+            if w.name == GQA_8K.name:
+                headline = tf
+            del q, k, v, o, lse
+    st, code = attn.attn_device_status()
+    if st != attn.ATTN_OK:
+        raise RuntimeError("device status %d code %#x" % (st, code))
+    out = {
+        "metric": "attention fwd TFLOPS per configuration (median launch, "
+                  "causal-halved FLOPs)",
+        "value": round(headline, 1), "unit": "TFLOPS", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 / f16 (per row)",
+        "data": "synthetic: Q/K/V ~ N(0,1) from a seeded CPU generator",
+        "config": {"workload": "all named forward workloads",
+                   "l2": "flushed between timed steps (256 MiB write, "
+                         "untimed)"},
+        "roofline": {"bound": "tensor", "peak": peak, "unit": "TFLOP/s",
+                     "peak_source": "%s bf16 dense burst (cuBLAS)" % src},
+        "table": rows,
+        "gpu_launches": args.steps * len(rows),
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
 # ------------------------------------------------------------ FP8 forward
 def run_fp8(args):
     """The headline GQA 8k causal forward with E4M3 Q/K/V (descale 1) and a
@@ -769,13 +856,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload",
                     choices=["gqa8k", "decode", "window", "bwd", "fp8",
-                             "decode_fp8"],
+                             "decode_fp8", "table"],
                     default="gqa8k",
                     help="gqa8k: the headline causal GQA forward (default); "
                          "decode: the split-KV decode step; window: causal "
                          "GQA 32k with a 4096-key sliding window; bwd: the "
                          "backward pass of gqa8k; fp8: gqa8k with E4M3 "
-                         "inputs; decode_fp8: decode with E4M3 inputs")
+                         "inputs; decode_fp8: decode with E4M3 inputs; "
+                         "table: every named forward workload, one row each")
     ap.add_argument("--splits", type=int, default=0,
                     help="split count for --workload decode (0: automatic)")
     args = ap.parse_args()
@@ -793,6 +881,8 @@ def main():
         run_window(args)
     elif args.workload == "bwd":
         run_bwd(args)
+    elif args.workload == "table":
+        run_table(args)
     else:
         run_ours(args)
 
