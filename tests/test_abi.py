@@ -226,3 +226,21 @@ def test_e4m3_refused_by_16_bit_entry_points(lib):
     assert attn.attn_bwd(BAD, BAD, BAD, BAD, BAD, BAD, BAD, BAD, BAD, 1, 2,
                          2, 128, 128, 128, 0.1, 1, 0, 0, attn.ATTN_E4M3,
                          BAD, 1 << 20, 0) == attn.ATTN_ERR_UNSUPPORTED
+
+
+def test_bwd_workspace_bytes(lib):
+    """Two fp32 vectors (lse2 and D) per query row, each row plane padded
+    to whole 128-row tiles, each vector rounded up to 256 bytes; 0 for
+    negative sizes (the documented contract of attn_bwd_workspace_bytes)."""
+    def expect(B, Hq, Sq):
+        rows = B * Hq * (-(-Sq // 128) * 128)
+        return 2 * (-(-(rows * 4) // 256) * 256)
+
+    for B, Hq, Sq in [(1, 2, 64), (1, 2, 128), (1, 2, 129), (2, 32, 8192),
+                      (3, 5, 1), (1, 1, 0), (0, 4, 100)]:
+        assert attn.attn_bwd_workspace_bytes(B, Hq, Sq) == expect(B, Hq, Sq)
+    for bad in [(-1, 2, 64), (1, -2, 64), (1, 2, -64)]:
+        assert attn.attn_bwd_workspace_bytes(*bad) == 0
+    # Padding: every Sq in one 128-row tile needs the same workspace.
+    assert len({attn.attn_bwd_workspace_bytes(1, 4, s)
+                for s in range(1, 129)}) == 1
