@@ -40,6 +40,9 @@ CASES = [
     W("chunk_ragged", 1, 4, 2, 200, 700, 128, "bf16", True, 300),
     W("chunk_rows_mode", 1, 3, 1, 130, 513, 64, "bf16", True, 383),
     W("short_keys", 1, 2, 2, 5, 129, 128, "f16", True, 124),
+    # the remaining D = 64 variants: packed bf16, one head per tile f16
+    W("decode_d64_bf16", 2, 8, 2, 1, 900, 64, "bf16", True, 899),
+    W("chunk_d64_f16", 1, 4, 2, 200, 700, 64, "f16", True, 300),
 ]
 
 

@@ -31,6 +31,7 @@ CASES = [
     W("decode_w256", 2, 8, 2, 1, 1000, 128, "f16", 999, 256),
     W("packed_rows_w50", 1, 16, 4, 20, 500, 128, "f16", 480, 50),
     W("packed_d64_w129", 3, 4, 2, 7, 700, 64, "bf16", 690, 129),
+    W("packed_d64_f16_w90", 2, 8, 2, 5, 600, 64, "f16", 595, 90),
     # two heads per CTA (even group), same rows
     W("pair_w129", 1, 8, 2, 700, 700, 128, "bf16", 0, 129),
     W("pair_offset_w384", 1, 4, 2, 300, 1100, 128, "bf16", 800, 384),
@@ -67,6 +68,11 @@ SPLIT_CASES = [
     W("split_decode_w1", 1, 4, 2, 1, 777, 64, "f16", 776, 1),
     W("split_chunk_w500", 1, 4, 2, 200, 1500, 128, "bf16", 1300, 500),
     W("split_rows_w257", 1, 3, 1, 130, 900, 64, "f16", 770, 257),
+    # every remaining (D, dtype, packed) combination with split and window
+    W("split_decode_d64_bf16_w200", 2, 8, 2, 1, 1500, 64, "bf16", 1499, 200),
+    W("split_rows_d64_bf16_w300", 1, 3, 1, 130, 900, 64, "bf16", 770, 300),
+    W("split_chunk_f16_w400", 1, 4, 2, 200, 1500, 128, "f16", 1300, 400),
+    W("split_decode_f16_w300", 2, 8, 2, 1, 2000, 128, "f16", 1999, 300),
 ]
 
 
