@@ -116,6 +116,7 @@ CASES = [
     (W("window_offset", 1, 8, 2, 400, 900, True, 500, 300), (0.9, 1.1, 1.0)),
     (W("packed_decode_rows", 2, 32, 4, 4, 777, True, 773), (1.0, 0.5, 1.0)),
     (W("packed_noncausal", 1, 8, 2, 5, 700, False), (2.0, 1.0, 0.25)),
+    (W("packed_window", 2, 8, 2, 6, 900, True, 894, 200), (1.0, 1.0, 1.0)),
     (W("one_key", 1, 2, 1, 3, 1, False), (1.0, 1.0, 1.0)),
 ]
 
@@ -135,6 +136,19 @@ def test_splitkv_decode(splits):
     q8, k8, v8 = make_qkv(w, seed=52)
     o, lse = run_fp8(w, q8, k8, v8, 1.0, 1.0, 0.5, splits=splits)
     q, k, v = decoded(w, q8, k8, v8, 1.0, 1.0, 0.5)
+    compare(w, o, lse, q, k, v, w.scale)
+
+
+@pytest.mark.parametrize("w,splits", [
+    (W("splitkv_chunk_rows", 1, 4, 2, 100, 2000, True, 1900), 3),
+    (W("splitkv_decode_window", 2, 8, 2, 1, 3000, True, 2999, 500), 4),
+], ids=["chunk_rows", "decode_window"])
+def test_splitkv_remaining_variants(w, splits):
+    """Split-KV with one head per tile (no window) and packed with a window:
+    with the cases above, every FP8 variant has a parity case."""
+    q8, k8, v8 = make_qkv(w, seed=55)
+    o, lse = run_fp8(w, q8, k8, v8, splits=splits)
+    q, k, v = decoded(w, q8, k8, v8, 1.0, 1.0, 1.0)
     compare(w, o, lse, q, k, v, w.scale)
 
 
