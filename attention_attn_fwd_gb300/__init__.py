@@ -20,6 +20,7 @@ __all__ = [
     "attn_fwd_splitkv", "attn_fwd_splitkv_window",
     "attn_splitkv_plan", "attn_fwd_splitkv_noalloc",
     "attn_noalloc_scratch_bytes", "attn_status_string", "attn_device_status",
+    "attn_stream_status", "attn_selftest_wait_timeout",
     "attn_tile_config", "attn_version", "attn_bwd", "attn_bwd_workspace_bytes",
     "fwd", "fwd_splitkv", "fwd_fp8", "bwd",
     "library_path", "load_library",
@@ -110,6 +111,12 @@ def load_library():
         lib.attn_fwd_fp8.restype = i
         lib.attn_noalloc_scratch_bytes.argtypes = []
         lib.attn_noalloc_scratch_bytes.restype = sz
+        lib.attn_stream_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+        lib.attn_stream_status.restype = i
+        lib.attn_selftest_wait_timeout.argtypes = [
+            vp, vp, vp, vp, vp, i, i, i, i, i, i, ctypes.c_float, i, i, i,
+            ctypes.c_ulonglong, vp]
+        lib.attn_selftest_wait_timeout.restype = i
         _lib = lib
         return lib
 
@@ -219,6 +226,28 @@ def attn_device_status():
     code = ctypes.c_uint(0)
     st = int(load_library().attn_device_status(ctypes.byref(code)))
     return st, int(code.value)
+
+
+def attn_stream_status(stream=0):
+    """(status, code) of the device status word, read after the work on
+    ``stream`` (an integer handle, 0 = the legacy default stream) and
+    cleared of the bits it reports."""
+    code = ctypes.c_uint(0)
+    st = int(load_library().attn_stream_status(stream or None,
+                                                ctypes.byref(code)))
+    return st, int(code.value)
+
+
+def attn_selftest_wait_timeout(Q, K, V, O, LSE, B, Hq, Hkv, Sq, Skv, D,
+                               scale, causal, input_pos, dtype, timeout_ns,
+                               stream) -> int:
+    """Raw C-ABI call of the bounded-wait self-test launch (a forward whose
+    first CTA withholds its first K tile; waits give up after
+    ``timeout_ns``)."""
+    return int(load_library().attn_selftest_wait_timeout(
+        Q or None, K or None, V or None, O or None, LSE or None, B, Hq, Hkv,
+        Sq, Skv, D, float(scale), int(causal), int(input_pos), int(dtype),
+        int(timeout_ns), stream or None))
 
 
 def attn_tile_config(B, Hq, Hkv, Sq, Skv, D, causal, input_pos, dtype):

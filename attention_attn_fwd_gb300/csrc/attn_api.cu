@@ -32,7 +32,12 @@ cudaError_t g_encode_err = cudaSuccess;
 
 std::mutex g_status_mu;
 unsigned int* g_status_ptr[kMaxDevices] = {};
+unsigned long long g_status_ctx[kMaxDevices] = {};  // context of the entry
 int g_num_sms[kMaxDevices] = {};
+
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   std::call_once(g_encode_once, [] {
@@ -46,14 +51,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return g_encode;
 }
 
-// Address of the status word on the current device (looked up once).
+// Address of the status word on the current device, looked up once per
+// device and context (a device reset replaces the context, and the module
+// holding the word is loaded again, possibly elsewhere).
 unsigned int* status_ptr(int dev) {
   if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  unsigned long long ctx = 0;
+  if (!attn::current_context_id(&ctx)) return nullptr;
   std::lock_guard<std::mutex> lock(g_status_mu);
-  if (g_status_ptr[dev] == nullptr) {
+  if (g_status_ptr[dev] == nullptr || g_status_ctx[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_attn_status) != cudaSuccess) return nullptr;
     g_status_ptr[dev] = static_cast<unsigned int*>(p);
+    g_status_ctx[dev] = ctx;
   }
   return g_status_ptr[dev];
 }
@@ -206,6 +216,36 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }  // namespace
 
 namespace attn {
+bool current_context_id(unsigned long long* id) {
+  std::call_once(g_ctx_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000,
+                                         cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000,
+                                         cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+  });
+  if (g_ctx_current == nullptr || g_ctx_id == nullptr) return false;
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS) return false;
+  if (ctx == nullptr) {
+    // No context bound to this thread yet: cudaSetDevice binds (and if
+    // needed creates) the current device's primary context.
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess)
+      return false;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  }
+  return g_ctx_id(ctx, id) == CUDA_SUCCESS;
+}
+
 int fwd_smem_bytes(int D, bool pack, bool fp8) {
   if (fp8)
     return pack ? Layout<128, true, true>::kSmemBytes
@@ -322,8 +362,10 @@ attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
                              attn_dtype_t dtype, unsigned int* status, int sms,
                              int splits, int split_tiles, float* o_part,
                              float* lse_part, unsigned long long* merge_ctr,
-                             cudaStream_t stream, float o_scale = 1.f) {
-  CUtensorMap tq, tk, tv;
+                             cudaStream_t stream, float o_scale = 1.f,
+                             unsigned long long timeout = 0,
+                             int withhold_first_load = 0) {
+  CUtensorMap tq, tk, tv, to;
   const long long q_planes = static_cast<long long>(s.B) * s.Hq;
   const long long kv_planes = static_cast<long long>(s.B) * s.Hkv;
   const bool pack = pack_gqa(s);
@@ -334,6 +376,16 @@ attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
   if (!q_ok || !make_map(&tk, K, dtype, s.D, s.Skv, kv_planes) ||
       !make_map(&tv, V, dtype, s.D, s.Skv, kv_planes))
     return ATTN_ERR_CUDA;
+  // O (16-bit; bf16 for E4M3 inputs), stored by TMA in 64-column boxes by
+  // the two-tile one-pass variants.  The packed and split-KV variants store
+  // per thread and never read this map.
+  if (!pack && o_part == nullptr) {
+    if (!make_map(&to, O, dtype == ATTN_E4M3 ? ATTN_BF16 : dtype, s.D, s.Sq,
+                  q_planes))
+      return ATTN_ERR_CUDA;
+  } else {
+    to = tq;
+  }
 
   attn::FwdParams p{};
   p.B = s.B;
@@ -364,27 +416,33 @@ attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
   p.merge_seq = merge_ctr != nullptr ? next_merge_seq() : 0u;
   p.num_units = static_cast<int>(grid_size(s) * splits);
   p.status = status;
-  p.timeout_ns = timeout_ns();
+  p.timeout_ns = timeout != 0 ? timeout : timeout_ns();
+  p.withhold_first_load = withhold_first_load;
 
   // Persistent launch: at most one CTA per SM, each walking its units.
   const int grid = static_cast<int>(std::min<long long>(p.num_units, sms));
   const bool bf16 = dtype == ATTN_BF16;
   const cudaError_t err =
       dtype == ATTN_E4M3
-          ? (pack ? attn::launch_fwd_d128_fp8_packed(tq, tk, tv, p, grid, stream)
-                  : attn::launch_fwd_d128_fp8(tq, tk, tv, p, grid, stream))
+          ? (pack ? attn::launch_fwd_d128_fp8_packed(tq, tk, tv, to, p, grid,
+                                                   stream)
+                  : attn::launch_fwd_d128_fp8(tq, tk, tv, to, p, grid, stream))
       : s.D == 64
-          ? (pack ? attn::launch_fwd_d64_packed(bf16, tq, tk, tv, p, grid, stream)
-                  : attn::launch_fwd_d64(bf16, tq, tk, tv, p, grid, stream))
-          : (pack ? attn::launch_fwd_d128_packed(bf16, tq, tk, tv, p, grid, stream)
-                  : attn::launch_fwd_d128(bf16, tq, tk, tv, p, grid, stream));
+          ? (pack ? attn::launch_fwd_d64_packed(bf16, tq, tk, tv, to, p, grid,
+                                              stream)
+                  : attn::launch_fwd_d64(bf16, tq, tk, tv, to, p, grid, stream))
+          : (pack ? attn::launch_fwd_d128_packed(bf16, tq, tk, tv, to, p, grid,
+                                               stream)
+                  : attn::launch_fwd_d128(bf16, tq, tk, tv, to, p, grid, stream));
   return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 // attn_fwd / attn_fwd_window.
 attn_status_t fwd_impl(const Shape& s, const void* Q, const void* K,
                        const void* V, void* O, float* LSE, float scale,
-                       attn_dtype_t dtype, attn_stream_t stream) {
+                       attn_dtype_t dtype, attn_stream_t stream,
+                       unsigned long long timeout = 0,
+                       int withhold_first_load = 0) {
   // E4M3 inputs need their descale factors: attn_fwd_fp8 only.
   if (dtype == ATTN_E4M3) return ATTN_ERR_INVALID_ARG;
   attn_status_t st = check_scalars(s, scale, dtype);
@@ -397,7 +455,14 @@ attn_status_t fwd_impl(const Shape& s, const void* Q, const void* K,
   const int tiles = (s.Skv + attn::cfg::kTN - 1) / attn::cfg::kTN;
   return launch_forward(s, Q, K, V, O, LSE, scale, dtype, status, sms, 1,
                         tiles, nullptr, nullptr, nullptr,
-                        reinterpret_cast<cudaStream_t>(stream));
+                        reinterpret_cast<cudaStream_t>(stream), 1.f, timeout,
+                        withhold_first_load);
+}
+
+// Clears the status bits a status query has reported (bits set since, by
+// kernels on other streams, stay).
+__global__ void clear_status_bits(unsigned int* status, unsigned int bits) {
+  atomicAnd(status, ~bits);
 }
 
 // attn_fwd_splitkv / attn_fwd_splitkv_window.
@@ -710,6 +775,40 @@ attn_status_t attn_device_status(unsigned int* code) {
   }
   if (code != nullptr) *code = v;
   return v != 0 ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+attn_status_t attn_stream_status(attn_stream_t stream, unsigned int* code) {
+  if (code != nullptr) *code = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  unsigned int* status = status_ptr(dev);
+  if (status == nullptr) return ATTN_ERR_CUDA;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  // Ordered after the work already on `stream`; other streams keep running.
+  unsigned int v = 0;
+  if (cudaMemcpyAsync(&v, status, sizeof(v), cudaMemcpyDeviceToHost, cs) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(cs) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (v != 0) {
+    clear_status_bits<<<1, 1, 0, cs>>>(status, v);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  if (code != nullptr) *code = v;
+  return v != 0 ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+attn_status_t attn_selftest_wait_timeout(const void* Q, const void* K,
+                                         const void* V, void* O, float* LSE,
+                                         int B, int Hq, int Hkv, int Sq,
+                                         int Skv, int D, float scale,
+                                         int causal, int input_pos,
+                                         attn_dtype_t dtype,
+                                         unsigned long long timeout_ns,
+                                         attn_stream_t stream) {
+  if (timeout_ns == 0) return ATTN_ERR_INVALID_ARG;
+  const Shape s{B, Hq, Hkv, Sq, Skv, D, causal != 0, input_pos};
+  return fwd_impl(s, Q, K, V, O, LSE, scale, dtype, stream, timeout_ns, 1);
 }
 
 attn_status_t attn_tile_config(int B, int Hq, int Hkv, int Sq, int Skv, int D,

@@ -5,8 +5,9 @@ namespace attn {
 
 cudaError_t launch_fwd_d128(bool bf16, const CUtensorMap& q,
                             const CUtensorMap& k, const CUtensorMap& v,
-                            const FwdParams& p, int grid, cudaStream_t stream) {
-  return launch_mode<128, false>(bf16, q, k, v, p, grid, stream);
+                            const CUtensorMap& o, const FwdParams& p, int grid,
+                            cudaStream_t stream) {
+  return launch_mode<128, false>(bf16, q, k, v, o, p, grid, stream);
 }
 
 }  // namespace attn

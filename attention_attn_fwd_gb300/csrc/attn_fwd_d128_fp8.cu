@@ -5,9 +5,10 @@
 namespace attn {
 
 cudaError_t launch_fwd_d128_fp8(const CUtensorMap& q, const CUtensorMap& k,
-                                const CUtensorMap& v, const FwdParams& p,
-                                int grid, cudaStream_t stream) {
-  return launch_mode<128, false, true>(true, q, k, v, p, grid, stream);
+                                const CUtensorMap& v, const CUtensorMap& o,
+                                const FwdParams& p, int grid,
+                                cudaStream_t stream) {
+  return launch_mode<128, false, true>(true, q, k, v, o, p, grid, stream);
 }
 
 }  // namespace attn

@@ -6,8 +6,9 @@ namespace attn {
 
 cudaError_t launch_fwd_d128_packed(bool bf16, const CUtensorMap& q,
                                    const CUtensorMap& k, const CUtensorMap& v,
-                                   const FwdParams& p, int grid, cudaStream_t stream) {
-  return launch_mode<128, true>(bf16, q, k, v, p, grid, stream);
+                                   const CUtensorMap& o, const FwdParams& p,
+                                   int grid, cudaStream_t stream) {
+  return launch_mode<128, true>(bf16, q, k, v, o, p, grid, stream);
 }
 
 }  // namespace attn

@@ -80,6 +80,10 @@ struct FwdParams {
   unsigned int merge_seq;         // nonzero, distinct per call
   unsigned int* status;    // device status word (timeouts)
   unsigned long long timeout_ns;
+  // Self-test of the bounded waits (0 in every normal launch): CTA 0's
+  // producer never loads its first K tile, so that CTA's MMA warp waits for
+  // a tile that cannot arrive until the wait runs out and the CTA aborts.
+  int withhold_first_load;
 };
 
 namespace cfg {
@@ -129,7 +133,12 @@ struct Layout {
       kPack ? (kChunks == 2 ? 6 : 13) : (kChunks == 2 ? 4 : 8);
   static constexpr int kQOff = 0;
   static constexpr int kRingOff = kQOff + kQTiles * kTileBytes;
-  static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
+  // Output staging of the two-tile variants: per Q tile one 128-row x
+  // 128-byte box (64 16-bit columns of O, 128-byte swizzle), written by the
+  // tile's softmax threads and stored to global memory by TMA.
+  static constexpr int kStageTileBytes = kPack ? 0 : 128 * 128;
+  static constexpr int kStageOff = kRingOff + kSlots * kTileBytes;
+  static constexpr int kBarOff = kStageOff + 2 * kStageTileBytes;
   // barriers: q_full[2], full[S], empty[S], s_full[6] (two S regions, or
   // three shared S buffers with one barrier per tile and buffer),
   // p_full[2], o_full[2], drain[1], q_free[2], pv_done[2]
@@ -366,10 +375,14 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
     attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v,
+                          const __grid_constant__ CUtensorMap tm_o,
                           const FwdParams p) {
   static_assert(!kFp8 || kBF16, "FP8 inputs give a bf16 output");
   using L = Layout<D, kPack, kFp8>;
   constexpr bool kHoldS = !kPack;  // S row kept in registers (see cfg)
+  // O leaves through shared memory and TMA stores (two-tile one-pass
+  // variants); split-KV partials and packed tiles are stored per thread.
+  constexpr bool kStageO = !kPack && !kSplit;
   // Three S buffers shared by the two Q tiles (D = 64: O needs 128 columns).
   constexpr bool kTriple = D == 64 && !kPack;
   constexpr int kOCol = kTriple ? 3 * cfg::kTN : 2 * cfg::kTN;  // first O column
@@ -439,6 +452,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
     bool ok = true;
     int it = 0;               // ring items (K_0, V_0, K_1, ...) issued so far
     int q_loads[2] = {0, 0};  // Q tile loads issued so far, per tile
+    const bool withhold = p.withhold_first_load != 0 && blockIdx.x == 0;
     for (int k = 0; k * u_step < p.num_units && ok; ++k) {
       const int u = unit_index(k, u_first, u_step);
       if (u >= p.num_units) continue;
@@ -470,6 +484,10 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
                                          abort_flag, p, 1));
             if (!ok) break;
           }
+          if (withhold && it == 0) {  // self-test: item 0 never arrives
+            ++it;
+            continue;
+          }
           const uint32_t dst = s_ring + slot * L::kTileBytes;
           ptx::mbar_arrive_expect_tx_elect(bar_full + 8 * slot, L::kTileBytes);
           for (int c = 0; c < L::kChunks; ++c)
@@ -485,7 +503,8 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
       for (int t = 0; t < 2; ++t)
         if (q_loads[t] > 0) drain_wait(bar_q + 8 * t, (q_loads[t] - 1) & 1, p);
       for (int i = max(0, it - nslots); i < it; ++i)
-        drain_wait(bar_full + 8 * (i % nslots), (i / nslots) & 1, p);
+        if (!(withhold && i == 0))
+          drain_wait(bar_full + 8 * (i % nslots), (i / nslots) & 1, p);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -1066,6 +1085,51 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
 
       if (!live) {
         // Padding rows only: nothing to store.
+      } else if constexpr (kStageO) {
+        // O / l in 16 bits through this tile's staging box: each thread
+        // writes its row's 16-byte chunks at the 128-byte-swizzled places
+        // (chunk c of row r at c ^ (r % 8): a warp's 32 rows cover every
+        // bank once per 8 rows), then one thread stores the box with TMA
+        // (rows >= Sq fall outside the tensor and are not written).  Per
+        // thread row stores touched 32 lines per warp instruction and took
+        // 4-5x longer.  D = 128 takes two boxes (columns 0-63, 64-127): the
+        // second waits until TMA has read the first out of the buffer.
+        const float inv_l =
+            kFp8 ? ptx::rcp(l_run) * p.o_scale : ptx::rcp(l_run);
+        const uint32_t stage = s_base + L::kStageOff + t * L::kStageTileBytes;
+        const uint32_t row_base = stage + r * 128;
+        const uint32_t sw = r % 8;
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+          uint32_t o[64];
+          ptx::tmem_ld32(t_o + 64 * h, o);
+          ptx::tmem_ld32(t_o + 64 * h + 32, o + 32);
+          ptx::tmem_wait_ld();
+          // The buffer is free once TMA has read the previous box out of it.
+          if (r == 0) ptx::bulk_wait_group_read_all();
+          ptx::named_barrier_sync(1 + t, kTM);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t wv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              wv[e] = ptx::pack2<kBF16>(
+                  __uint_as_float(o[8 * c + 2 * e]) * inv_l,
+                  __uint_as_float(o[8 * c + 2 * e + 1]) * inv_l);
+            ptx::st_shared_v4(row_base + ((c ^ sw) << 4), wv[0], wv[1], wv[2],
+                              wv[3]);
+          }
+          ptx::fence_proxy_async_smem();
+          ptx::named_barrier_sync(1 + t, kTM);
+          if (r == 0) {
+            ptx::tma_store_3d(&tm_o, stage, 64 * h, m0, q_plane);
+            ptx::bulk_commit_group();
+          }
+        }
+        if (p.lse != nullptr && row_ok) {
+          const long long row = static_cast<long long>(q_plane) * p.Sq + q_row;
+          p.lse[row] = (m_run + ptx::lg2(l_run)) * kLn2;
+        }
       } else if (p.o_part == nullptr) {
         const float inv_l =
             kFp8 ? ptx::rcp(l_run) * p.o_scale : ptx::rcp(l_run);
@@ -1139,6 +1203,11 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
         }
       }
       ptx::tc_fence_before();
+    }
+    // Output boxes still being stored must be read out of shared memory
+    // (and written) before the CTA exits.
+    if constexpr (kStageO) {
+      if (r == 0) ptx::bulk_wait_group_all();
     }
   }
 

@@ -12,8 +12,8 @@ namespace {
 template <int D, bool kBF16, bool kPack, bool kSplit, bool kWindow,
           bool kFp8>
 cudaError_t launch_variant(const CUtensorMap& q, const CUtensorMap& k,
-                           const CUtensorMap& v, const FwdParams& p, int grid,
-                           cudaStream_t stream) {
+                           const CUtensorMap& v, const CUtensorMap& o,
+                           const FwdParams& p, int grid, cudaStream_t stream) {
   auto kernel = attn_fwd_sm103_kernel<D, kBF16, kPack, kSplit, kWindow, kFp8>;
   const int smem = Layout<D, kPack, kFp8>::kSmemBytes;
   // The attribute is per device; setting it again is cheap and idempotent.
@@ -43,7 +43,7 @@ cudaError_t launch_variant(const CUtensorMap& q, const CUtensorMap& k,
   cfg.blockDim = dim3(cfg::kThreads, 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, kernel, q, k, v, p);
+  return cudaLaunchKernelEx(&cfg, kernel, q, k, v, o, p);
 }
 
 // Dtype, split-KV and window dispatch of one (D, tile mode) variant:
@@ -51,33 +51,33 @@ cudaError_t launch_variant(const CUtensorMap& q, const CUtensorMap& k,
 // variant when a window is set.  FP8 inputs always write bf16.
 template <int D, bool kPack, bool kSplit, bool kWindow, bool kFp8>
 cudaError_t launch_dtype(bool bf16, const CUtensorMap& q, const CUtensorMap& k,
-                         const CUtensorMap& v, const FwdParams& p, int grid,
-                         cudaStream_t stream) {
+                         const CUtensorMap& v, const CUtensorMap& o,
+                         const FwdParams& p, int grid, cudaStream_t stream) {
   if constexpr (kFp8) {
-    return launch_variant<D, true, kPack, kSplit, kWindow, true>(q, k, v, p,
+    return launch_variant<D, true, kPack, kSplit, kWindow, true>(q, k, v, o, p,
                                                                  grid, stream);
   } else {
     return bf16 ? launch_variant<D, true, kPack, kSplit, kWindow, false>(
-                      q, k, v, p, grid, stream)
+                      q, k, v, o, p, grid, stream)
                 : launch_variant<D, false, kPack, kSplit, kWindow, false>(
-                      q, k, v, p, grid, stream);
+                      q, k, v, o, p, grid, stream);
   }
 }
 
 template <int D, bool kPack, bool kFp8 = false>
 cudaError_t launch_mode(bool bf16, const CUtensorMap& q, const CUtensorMap& k,
-                        const CUtensorMap& v, const FwdParams& p, int grid,
-                        cudaStream_t stream) {
+                        const CUtensorMap& v, const CUtensorMap& o,
+                        const FwdParams& p, int grid, cudaStream_t stream) {
   const bool split = p.o_part != nullptr;
   const bool window = p.window > 0;
   if (split)
-    return window ? launch_dtype<D, kPack, true, true, kFp8>(bf16, q, k, v, p,
+    return window ? launch_dtype<D, kPack, true, true, kFp8>(bf16, q, k, v, o, p,
                                                              grid, stream)
-                  : launch_dtype<D, kPack, true, false, kFp8>(bf16, q, k, v, p,
+                  : launch_dtype<D, kPack, true, false, kFp8>(bf16, q, k, v, o, p,
                                                               grid, stream);
-  return window ? launch_dtype<D, kPack, false, true, kFp8>(bf16, q, k, v, p,
+  return window ? launch_dtype<D, kPack, false, true, kFp8>(bf16, q, k, v, o, p,
                                                             grid, stream)
-                : launch_dtype<D, kPack, false, false, kFp8>(bf16, q, k, v, p,
+                : launch_dtype<D, kPack, false, false, kFp8>(bf16, q, k, v, o, p,
                                                              grid, stream);
 }
 

@@ -13,6 +13,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/attn.h"
+#include "attn_launch.h"
 
 namespace {
 
@@ -24,21 +25,28 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};  // context of the entry
 
 // Device address of the scratch array on the current device.  In host code
 // the array's name is only a host-side stand-in, so the address is looked
-// up once per device with that device current.
+// up with that device current, once per device and context: a device reset
+// replaces the context and loads the library's module (and the array) again,
+// possibly at another address, so an entry of an earlier context is never
+// used.
 attn_status_t scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  unsigned long long ctx = 0;
+  if (!attn::current_context_id(&ctx)) return ATTN_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (g_scratch_ptr[dev] == nullptr || g_scratch_ctx[dev] != ctx) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess ||
         ptr == nullptr)
       return ATTN_ERR_CUDA;
     g_scratch_ptr[dev] = ptr;
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_ptr[dev];
   return ATTN_OK;
@@ -62,12 +70,16 @@ attn_status_t attn_fwd_splitkv_noalloc(const void* Q, const void* K,
                                        input_pos, dtype, &splits, &need);
   if (st != ATTN_OK) return st;
   if (B == 0 || Sq == 0) return ATTN_OK;
+  // Like attn_fwd_splitkv: a positive count must be one the plan keeps.
+  if (num_splits > 0 && splits != num_splits) return ATTN_ERR_INVALID_ARG;
   if (need > kNoAllocScratchBytes) return ATTN_ERR_UNSUPPORTED;
   void* scratch = nullptr;
   st = scratch_address(&scratch);
   if (st != ATTN_OK) return st;
   // Every partial result the merge reads is written first by the forward
-  // kernel, so the scratch needs no clearing between calls.
+  // kernel, and the merge counters carry a per-call tag (a counter left by
+  // an earlier call restarts), so the scratch needs no clearing between
+  // calls.
   return attn_fwd_splitkv(Q, K, V, O, LSE, B, Hq, Hkv, Sq, Skv, D, scale,
                           causal, input_pos, dtype, splits, scratch,
                           kNoAllocScratchBytes, stream);

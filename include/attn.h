@@ -19,6 +19,8 @@
  *     the scale defaulting to 1/sqrt(D) on the Python side.
  *
  * No function here allocates device memory; the caller owns every buffer.
+ * (attn_fwd_splitkv_noalloc's scratch is a fixed array compiled into the
+ * library, which every GPU that loads it holds, not an allocation.)
  */
 #ifndef ATTN_FWD_GB300_ATTN_H
 #define ATTN_FWD_GB300_ATTN_H
@@ -211,15 +213,17 @@ attn_status_t attn_splitkv_plan(int B, int Hq, int Hkv, int Sq, int Skv, int D,
  * library until the process exits) instead of a caller workspace.  The
  * pages have no counterpart; this is a deployment convenience.
  *
- * Arguments as attn_fwd_splitkv without the workspace; num_splits <= 0
- * lets the library choose.  Returns ATTN_ERR_UNSUPPORTED when the partial
- * results of the planned split count (see attn_splitkv_plan) need more
- * than the scratch holds.  The first call on a device looks up the
- * scratch address on that device (no allocation); make that first call
- * before any stream capture.  All calls share the one scratch array and it
- * keeps the last call's contents (nothing in it has to start at zero):
- * calls whose kernels overlap on the GPU race on it, so issue them on one
- * stream or otherwise order them.
+ * Arguments as attn_fwd_splitkv without the workspace: num_splits <= 0
+ * lets the library choose, and a positive count must be one that
+ * attn_splitkv_plan keeps (otherwise ATTN_ERR_INVALID_ARG).  Returns
+ * ATTN_ERR_UNSUPPORTED when the partial results of that split count need
+ * more than the scratch holds.  The first call on a device (and the first
+ * after a device reset, which replaces the context) looks up the scratch
+ * address on that device (no allocation); make that first call before any
+ * stream capture.  All calls share the one scratch array and it keeps the
+ * last call's contents (nothing in it has to start at zero): calls whose
+ * kernels overlap on the GPU race on it, so issue them on one stream or
+ * otherwise order them.
  */
 attn_status_t attn_fwd_splitkv_noalloc(const void* Q, const void* K,
                                        const void* V, void* O, float* LSE,
@@ -284,8 +288,48 @@ const char* attn_status_string(attn_status_t status);
  * wait has run out since the last call; otherwise a non-zero code
  * (bits 0-7: 1 = wait timed out; bits 8-15: the pipeline role that gave
  * up) and the function returns ATTN_ERR_TIMEOUT.  code may be NULL.
+ * Every wait of every kernel in flight ORs into the one word, so the
+ * device-wide form sees them all; attn_stream_status below waits for one
+ * stream only.
  */
 attn_status_t attn_device_status(unsigned int* code);
+
+/*
+ * attn_stream_status — the same query ordered on one stream: waits for the
+ * work already enqueued on `stream` (cudaStreamSynchronize of that stream
+ * only; other streams keep running), reads the status word and enqueues on
+ * `stream` the clearing of exactly the bits it reports.  The word is one
+ * per device, shared by every stream and call, so a wait that ran out in a
+ * kernel of another stream, finished before the read, is reported here too;
+ * bits 8-15 name the role that gave up (in the forward kernel 1 producer,
+ * 2 MMA issuer, 3 softmax, 4 epilogue, 5 split-KV merge; OR-ed when
+ * several gave up).  Not for use while `stream` is being captured.  code
+ * may be NULL.
+ */
+attn_status_t attn_stream_status(attn_stream_t stream, unsigned int* code);
+
+/*
+ * attn_selftest_wait_timeout — exercises the kernel's bounded-wait abort
+ * path on demand.  Launches the attn_fwd kernel for these arguments (same
+ * meaning and checks as attn_fwd) with two changes: every pipeline wait
+ * gives up after timeout_ns (> 0) instead of the library default, and the
+ * first CTA never loads its first K tile, so its MMA issuer waits for a
+ * tile that cannot arrive.  That wait runs out, the CTA's roles stop,
+ * drain what they have in flight (bounded), free TMEM and exit; the other
+ * CTAs finish normally.  Nothing faults or hangs and the context stays
+ * usable: the timeout is reported by the next attn_device_status() or
+ * attn_stream_status() (ATTN_ERR_TIMEOUT, bit 0 set, role bits non-zero),
+ * and the rows of the first CTA's work units in O and LSE are left
+ * undefined.  For tests of the failure path only.
+ */
+attn_status_t attn_selftest_wait_timeout(const void* Q, const void* K,
+                                         const void* V, void* O, float* LSE,
+                                         int B, int Hq, int Hkv, int Sq,
+                                         int Skv, int D, float scale,
+                                         int causal, int input_pos,
+                                         attn_dtype_t dtype,
+                                         unsigned long long timeout_ns,
+                                         attn_stream_t stream);
 
 /*
  * attn_tile_config — the tile configuration attn_fwd would launch for these

@@ -72,6 +72,10 @@ class Oracle:
             dp, dp, dp, dp, L, L, L, L, L, L, ctypes.c_double, ctypes.c_int,
             L, L, ctypes.POINTER(ctypes.c_int64), L, dp]
         lib.attn_oracle_bwd_dq_rows.restype = ctypes.c_int
+        lib.attn_oracle_bwd_dkdv_rows.argtypes = [
+            dp, dp, dp, dp, L, L, L, L, L, L, ctypes.c_double, ctypes.c_int,
+            L, L, ctypes.POINTER(ctypes.c_int64), L, dp, dp]
+        lib.attn_oracle_bwd_dkdv_rows.restype = ctypes.c_int
         lib.attn_oracle_decode_e4m3.argtypes = [
             ctypes.POINTER(ctypes.c_uint8), L, ctypes.c_double, dp]
         lib.attn_oracle_decode_e4m3.restype = ctypes.c_int
@@ -163,6 +167,28 @@ class Oracle:
             raise ValueError("oracle rejected the arguments (code %d)" % rc)
         return dq
 
+    def backward_dkdv_rows(self, q, k, v, do, scale, causal, input_pos, keys,
+                           window=0):
+        """(dK, dV) of key rows (b, kvh, j) given as an (n, 3) int array:
+        two [n, D] arrays."""
+        q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+        B, Hq, Hkv, Sq, Skv, D = _shapes(q, k, v)
+        if do.shape != q.shape:
+            raise ValueError("do must have the shape of q")
+        keys = np.ascontiguousarray(
+            np.asarray(keys, dtype=np.int64).reshape(-1, 3))
+        n = keys.shape[0]
+        dk = np.zeros((n, D), np.float64)
+        dv = np.zeros((n, D), np.float64)
+        rc = self._lib.attn_oracle_bwd_dkdv_rows(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(do), B, Hq, Hkv, Sq, Skv, D,
+            float(scale), int(bool(causal)), int(input_pos), int(window),
+            keys.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n, _ptr(dk),
+            _ptr(dv))
+        if rc != 0:
+            raise ValueError("oracle rejected the arguments (code %d)" % rc)
+        return dk, dv
+
     def decode_e4m3(self, x8, descale=1.0):
         """E4M3 codes (a torch float8_e4m3fn / uint8 tensor or a uint8
         array) times ``descale``, as a float64 array of the same shape."""
@@ -215,6 +241,12 @@ def backward(q, k, v, do, scale, causal=False, input_pos=0, window=0):
 def backward_dq_rows(q, k, v, do, scale, causal, input_pos, rows, window=0):
     return default().backward_dq_rows(q, k, v, do, scale, causal, input_pos,
                                       rows, window)
+
+
+def backward_dkdv_rows(q, k, v, do, scale, causal, input_pos, keys,
+                       window=0):
+    return default().backward_dkdv_rows(q, k, v, do, scale, causal,
+                                        input_pos, keys, window)
 
 
 def decode_e4m3(x8, descale=1.0):

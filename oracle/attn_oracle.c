@@ -381,6 +381,118 @@ int attn_oracle_bwd_dq_rows(const double* Q, const double* K, const double* V,
 }
 
 /*
+ * dK and dV of selected key rows only (the same chain rule as
+ * attn_oracle_bwd, gathered per key instead of scattered per query row).
+ * Key j of K/V head kvh receives from every query row (h, i) of the heads
+ * h of its group:
+ *   dV_j = sum_{h,i} P_hij dO_hi
+ *   dK_j = scale * sum_{h,i} P_hij (dO_hi . V_j - sum_k P_hik dO_hi . V_k) Q_hi
+ * The inner sum over k needs the query row's whole probability row, so the
+ * query rows of each K/V group that a requested key belongs to are visited
+ * once (first pass: that row sum and the row's weights on the requested
+ * keys), then every requested key sums over them (second pass).
+ * keys_bkj holds n triplets (b, kvh, j); dK_rows[r*D ..), dV_rows[r*D ..).
+ */
+int attn_oracle_bwd_dkdv_rows(const double* Q, const double* K,
+                              const double* V, const double* dO, long B,
+                              long Hq, long Hkv, long Sq, long Skv, long D,
+                              double scale, int causal, long input_pos,
+                              long window, const int64_t* keys_bkj, long n,
+                              double* dK_rows, double* dV_rows) {
+  if (!check_shape(B, Hq, Hkv, Sq, Skv, D, causal, input_pos, window))
+    return ORACLE_BAD_ARG;
+  for (long r = 0; r < n; ++r) {
+    const int64_t b = keys_bkj[3 * r], kvh = keys_bkj[3 * r + 1],
+                  j = keys_bkj[3 * r + 2];
+    if (b < 0 || b >= B || kvh < 0 || kvh >= Hkv || j < 0 || j >= Skv)
+      return ORACLE_BAD_ARG;
+  }
+  const long group = Hq / Hkv;
+  const long qrows = group * Sq;  /* query rows of one K/V group */
+  for (long x = 0; x < n * D; ++x) {
+    dK_rows[x] = 0.0;
+    dV_rows[x] = 0.0;
+  }
+  long* sel = (long*)malloc(sizeof(long) * (size_t)(n > 0 ? n : 1));
+  double* pdp = (double*)malloc(sizeof(double) * (size_t)qrows);
+  double* psel =
+      (double*)malloc(sizeof(double) * (size_t)qrows * (size_t)(n > 0 ? n : 1));
+  int failed = (!sel || !pdp || !psel);
+  /* One K/V group (b, kvh) at a time: the requested keys in it ... */
+  for (long first = 0; first < n && !failed; ++first) {
+    const int64_t gb = keys_bkj[3 * first], gk = keys_bkj[3 * first + 1];
+    int seen = 0;
+    for (long r = 0; r < first; ++r)
+      if (keys_bkj[3 * r] == gb && keys_bkj[3 * r + 1] == gk) seen = 1;
+    if (seen) continue;
+    long m = 0;
+    for (long r = first; r < n; ++r)
+      if (keys_bkj[3 * r] == gb && keys_bkj[3 * r + 1] == gk) sel[m++] = r;
+    const double* v = V + (gb * Hkv + gk) * Skv * D;
+    /* ... first pass over the group's query rows ... */
+#pragma omp parallel
+    {
+      double* score = (double*)malloc(sizeof(double) * (size_t)Skv);
+      double* prob = (double*)malloc(sizeof(double) * (size_t)Skv);
+      double* out = (double*)malloc(sizeof(double) * (size_t)D);
+      if (!score || !prob || !out) {
+#pragma omp atomic write
+        failed = 1;
+      } else {
+#pragma omp for schedule(dynamic, 8)
+        for (long rr = 0; rr < qrows; ++rr) {
+          const long h = gk * group + rr / Sq, i = rr % Sq;
+          const double* dout = dO + ((gb * Hq + h) * Sq + i) * D;
+          double lse;
+          oracle_row(Q, K, V, Hq, Hkv, Sq, Skv, D, scale, causal, input_pos,
+                     window, gb, h, i, score, prob, out, &lse);
+          double s_pdp = 0.0;
+          for (long jj = 0; jj < Skv; ++jj) {
+            if (prob[jj] == 0.0) continue;
+            double dot = 0.0;
+            for (long d = 0; d < D; ++d) dot += dout[d] * v[jj * D + d];
+            s_pdp += prob[jj] * dot;
+          }
+          pdp[rr] = s_pdp;
+          for (long t = 0; t < m; ++t)
+            psel[rr * m + t] = prob[keys_bkj[3 * sel[t] + 2]];
+        }
+      }
+      free(score);
+      free(prob);
+      free(out);
+    }
+    if (failed) break;
+    /* ... second pass: each requested key sums over those rows. */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long t = 0; t < m; ++t) {
+      const long r = sel[t];
+      const long j = keys_bkj[3 * r + 2];
+      double* dk = dK_rows + r * D;
+      double* dv = dV_rows + r * D;
+      for (long rr = 0; rr < qrows; ++rr) {
+        const double pj = psel[rr * m + t];
+        if (pj == 0.0) continue;
+        const long h = gk * group + rr / Sq, i = rr % Sq;
+        const double* q = Q + ((gb * Hq + h) * Sq + i) * D;
+        const double* dout = dO + ((gb * Hq + h) * Sq + i) * D;
+        double dp = 0.0;
+        for (long d = 0; d < D; ++d) dp += dout[d] * v[j * D + d];
+        const double ds = pj * (dp - pdp[rr]);
+        for (long d = 0; d < D; ++d) {
+          dk[d] += scale * ds * q[d];
+          dv[d] += pj * dout[d];
+        }
+      }
+    }
+  }
+  free(sel);
+  free(pdp);
+  free(psel);
+  return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
+}
+
+/*
  * FP8 inputs.  "Flash Attention from Scratch", section "What's Next", names
  * FP8 tensor cores as future work and defines no format; the reading taken
  * is the 8-bit E4M3 format of the OCP "8-bit Floating Point Specification"

@@ -365,6 +365,19 @@ def pin_bwd_torch_autograd(orc):
         np.testing.assert_allclose(dq_rows, ref[0][rows[:, 0], rows[:, 1],
                                                    rows[:, 2]],
                                    rtol=0, atol=1e-12, err_msg="dQ rows")
+        # The key-sampled dK / dV (every key of the last K/V head, every
+        # third key of the others, in shuffled order) against the same
+        # library gradients.
+        keys = [(bb, kh, j) for bb in range(B) for kh in range(Hkv)
+                for j in range(Skv) if kh == Hkv - 1 or j % 3 == 0]
+        keys = np.array(keys)[rng.permutation(len(keys))]
+        dk_rows, dv_rows = orc.backward_dkdv_rows(q, k, v, do, 0.45, causal,
+                                                  pos, keys, W)
+        sel = (keys[:, 0], keys[:, 1], keys[:, 2])
+        np.testing.assert_allclose(dk_rows, ref[1][sel], rtol=0, atol=1e-12,
+                                   err_msg="dK rows")
+        np.testing.assert_allclose(dv_rows, ref[2][sel], rtol=0, atol=1e-12,
+                                   err_msg="dV rows")
 
 
 def pin_bwd_finite_differences(orc):
@@ -403,6 +416,11 @@ def pin_bwd_single_key(orc):
     assert np.all(dq == 0.0) and np.all(dk == 0.0)
     want = do.reshape(B, Hkv, Hq // Hkv, Sq, D).sum(axis=(2, 3))
     np.testing.assert_allclose(dv[:, :, 0], want, rtol=0, atol=1e-12)
+    keys = np.array([(bb, kh, 0) for bb in range(B) for kh in range(Hkv)])
+    dk_rows, dv_rows = orc.backward_dkdv_rows(q, k, v, do, 0.9, True, 0, keys)
+    assert np.all(dk_rows == 0.0)
+    np.testing.assert_allclose(dv_rows, want.reshape(-1, D), rtol=0,
+                               atol=1e-12)
 
 
 # FP8 (E4M3) inputs: the oracle's own decoder, then the definition above.

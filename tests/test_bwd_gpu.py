@@ -153,10 +153,12 @@ def test_bwd_side_stream_and_graph():
 
 
 def test_bwd_full_size_gqa8k():
-    """GQA 8k causal: dQ on sampled rows against the oracle; dK and dV at
-    every element through exact identities -- each row of dS sums to zero,
-    so sum_j dK_j = 0, and each row of P sums to one, so sum_j dV_j equals
-    the sum of dO over the group's query heads and rows."""
+    """GQA 8k causal: dQ on sampled query rows and dK, dV on sampled key
+    rows of one K/V head against the oracle, each row's largest error
+    normalised by that row's largest oracle value; dK and dV at every
+    element through exact identities -- each row of dS sums to zero, so
+    sum_j dK_j = 0, and each row of P sums to one, so sum_j dV_j equals the
+    sum of dO over the group's query heads and rows."""
     w = GQA_8K
     q, k, v = make_qkv(w, seed=0)
     do = make_do(w, seed=0)
@@ -167,6 +169,25 @@ def test_bwd_full_size_gqa8k():
     got = dq[idx[:, 0], idx[:, 1], idx[:, 2]].double().cpu().numpy()
     e = float(np.max(np.abs(got - ref))) / float(np.max(np.abs(ref)))
     assert e <= TOL_REL["bf16"], ("dQ rows", e)
+    e_row = np.max(np.abs(got - ref), axis=1) / np.max(np.abs(ref), axis=1)
+    assert float(e_row.max()) <= TOL_REL["bf16"], ("dQ per row", e_row.max())
+    # Key rows of the last K/V head: tile edges (128-key tiles), the last
+    # key (seen by one query row per head) and random keys.
+    rng = np.random.default_rng(6)
+    kvh = w.Hkv - 1
+    js = {0, 1, 127, 128, 129, 4095, 4096, w.Skv - 129, w.Skv - 128,
+          w.Skv - 2, w.Skv - 1}
+    js |= set(int(x) for x in rng.integers(0, w.Skv, 21))
+    keys = np.array([(0, kvh, j) for j in sorted(js)], dtype=np.int64)
+    ref_dk, ref_dv = oracle.backward_dkdv_rows(q, k, v, do, w.scale, True, 0,
+                                               keys)
+    kidx = torch.from_numpy(keys).cuda()
+    for name, g, r in (("dK", dk, ref_dk), ("dV", dv, ref_dv)):
+        got = g[kidx[:, 0], kidx[:, 1], kidx[:, 2]].double().cpu().numpy()
+        assert np.all(np.isfinite(got))
+        e_row = np.max(np.abs(got - r), axis=1) / np.max(np.abs(r), axis=1)
+        assert float(e_row.max()) <= TOL_REL["bf16"], (name, e_row.max(),
+                                                       keys[e_row.argmax()])
     g = w.Hq // w.Hkv
     dk64, dv64 = dk.double(), dv.double()
     s_dk = dk64.sum(dim=2)

@@ -52,6 +52,14 @@ MUTANTS = {
     "bwd_rows_rowsum_dropped": (
         "const double ds = prob[j] * (score[j] - pdp);",
         "const double ds = prob[j] * score[j];"),
+    "bwd_keys_rowsum_dropped": ("const double ds = pj * (dp - pdp[rr]);",
+                                "const double ds = pj * dp;"),
+    "bwd_keys_dv_uses_ds": ("dv[d] += pj * dout[d];", "dv[d] += ds * dout[d];"),
+    "bwd_keys_dk_scale_dropped": ("dk[d] += scale * ds * q[d];",
+                                  "dk[d] += ds * q[d];"),
+    "bwd_keys_wrong_group_head": (
+        "const long h = gk * group + rr / Sq, i = rr % Sq;\n        const double* q",
+        "const long h = rr / Sq, i = rr % Sq;\n        const double* q"),
     "e4m3_bias_8": ("ldexp((double)(8u + m), (int)e - 10)",
                     "ldexp((double)(8u + m), (int)e - 11)"),
     "e4m3_no_implicit_bit": ("ldexp((double)(8u + m), (int)e - 10)",
