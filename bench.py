@@ -16,7 +16,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -35,8 +34,10 @@ FLUSH_BYTES = 256 << 20  # > 129 MB L2
 EX2_PER_CLK_PER_SM = 32
 KERNEL_SOURCES = ["attention_attn_fwd_gb300/csrc/attn_fwd_kernel.cuh",
                   "attention_attn_fwd_gb300/csrc/sm103_ptx.cuh"]
+# DRAM bytes of one headline launch from an ncu capture (data file written
+# from the capture's summary; see the .md of the same name for the command).
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles",
-                               "attn_fwd_sm103_gqa8k_traffic.md")
+                               "attn_fwd_sm103_gqa8k_traffic.json")
 
 
 def kernel_source_hash():
@@ -48,17 +49,20 @@ def kernel_source_hash():
 
 
 def measured_traffic():
-    """DRAM bytes per launch from the committed ncu summary, or None when
-    the summary is missing or the kernel source changed since the capture."""
+    """(DRAM bytes per launch, source label) from the committed ncu capture
+    data, or (None, reason) when it is missing or the kernel source changed
+    since the capture (the counters then describe another kernel)."""
     try:
-        text = open(TRAFFIC_PROFILE).read()
-    except OSError:
-        return None
-    m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
-    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
-        return None
-    return int(m_bytes.group(1))
+        with open(TRAFFIC_PROFILE) as f:
+            d = json.load(f)
+        h, nbytes = str(d["kernel_source_hash"]), int(d["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError, TypeError):
+        return None, "no capture data"
+    if h != kernel_source_hash():
+        return None, "capture of kernel source %s, not the current %s" % (
+            h, kernel_source_hash())
+    return nbytes, "ncu capture (dram__bytes_read.sum + dram__bytes_write.sum)" \
+        " of kernel source %s" % h
 
 
 def peaks():
@@ -318,6 +322,7 @@ def run_ours(args):
     e2e_value = whole_job_rate(flops, e2e_ms, ws) / 1e12
     peak_tf, _, peak_src = peaks()
     achieved = flops / (kernel_ms * 1e-3) / 1e12  # one launch, one GPU
+    traffic, traffic_src = measured_traffic()
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT,
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
@@ -341,7 +346,8 @@ def run_ours(args):
             "peak": peak_tf, "unit": "TFLOP/s",
             "frac": round(achieved / peak_tf, 4),
             "peak_source": "%s bf16 dense burst (cuBLAS)" % peak_src,
-            "traffic": measured_traffic(),
+            "traffic": traffic,
+            "traffic_source": traffic_src,
             "algorithmic_bytes": w.io_bytes()},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -53,6 +53,17 @@ def rel_err(got, ref):
     return float(np.max(np.abs(g - ref))) / max(denom, 1e-30)
 
 
+def row_err(got, ref):
+    """Per sampled row: max |got - ref| over the row, divided by the row's
+    largest oracle value, or by 1 % of the largest over all sampled rows
+    when the row's own is smaller (a row whose exact gradient is near zero,
+    such as dQ of the first causal query, which sees one key, carries the
+    rounding of terms as large as its neighbours')."""
+    row_max = np.max(np.abs(ref), axis=1)
+    floor = 0.01 * float(row_max.max())
+    return np.max(np.abs(got - ref), axis=1) / np.maximum(row_max, floor)
+
+
 CASES = [
     W("small_noncausal", 1, 2, 2, 128, 128, 64, "f16", False),
     W("causal_gqa_ragged", 1, 8, 2, 300, 300, 128, "bf16", True),
@@ -169,8 +180,7 @@ def test_bwd_full_size_gqa8k():
     got = dq[idx[:, 0], idx[:, 1], idx[:, 2]].double().cpu().numpy()
     e = float(np.max(np.abs(got - ref))) / float(np.max(np.abs(ref)))
     assert e <= TOL_REL["bf16"], ("dQ rows", e)
-    e_row = np.max(np.abs(got - ref), axis=1) / np.max(np.abs(ref), axis=1)
-    assert float(e_row.max()) <= TOL_REL["bf16"], ("dQ per row", e_row.max())
+    assert float(row_err(got, ref).max()) <= TOL_REL["bf16"], "dQ per row"
     # Key rows of the last K/V head: tile edges (128-key tiles), the last
     # key (seen by one query row per head) and random keys.
     rng = np.random.default_rng(6)
@@ -185,7 +195,7 @@ def test_bwd_full_size_gqa8k():
     for name, g, r in (("dK", dk, ref_dk), ("dV", dv, ref_dv)):
         got = g[kidx[:, 0], kidx[:, 1], kidx[:, 2]].double().cpu().numpy()
         assert np.all(np.isfinite(got))
-        e_row = np.max(np.abs(got - r), axis=1) / np.max(np.abs(r), axis=1)
+        e_row = row_err(got, r)
         assert float(e_row.max()) <= TOL_REL["bf16"], (name, e_row.max(),
                                                        keys[e_row.argmax()])
     g = w.Hq // w.Hkv
