@@ -20,7 +20,7 @@ __all__ = [
     "attn_fwd_splitkv", "attn_fwd_splitkv_window",
     "attn_splitkv_plan", "attn_fwd_splitkv_noalloc",
     "attn_noalloc_scratch_bytes", "attn_status_string", "attn_device_status",
-    "attn_stream_status", "attn_selftest_wait_timeout",
+    "attn_stream_status", "attn_selftest_wait_timeout", "attn_dispatch",
     "attn_tile_config", "attn_version", "attn_bwd", "attn_bwd_workspace_bytes",
     "fwd", "fwd_splitkv", "fwd_fp8", "bwd",
     "library_path", "load_library",
@@ -49,6 +49,14 @@ class AttnError(RuntimeError):
     def __init__(self, msg, status=None):
         super().__init__(msg)
         self.status = status
+
+
+class _Dispatch(ctypes.Structure):
+    """attn_dispatch_t of include/attn.h."""
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "block_m", "block_n", "q_tiles", "paired", "s_buffers", "stages",
+        "order", "o_store", "hold_scores", "num_splits", "units",
+        "smem_bytes")] + [("name", ctypes.c_char_p)]
 
 
 def library_path() -> str:
@@ -111,6 +119,9 @@ def load_library():
         lib.attn_fwd_fp8.restype = i
         lib.attn_noalloc_scratch_bytes.argtypes = []
         lib.attn_noalloc_scratch_bytes.restype = sz
+        lib.attn_dispatch.argtypes = [i, i, i, i, i, i, i, i, i, i, i,
+                                      ctypes.POINTER(_Dispatch)]
+        lib.attn_dispatch.restype = i
         lib.attn_stream_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
         lib.attn_stream_status.restype = i
         lib.attn_selftest_wait_timeout.argtypes = [
@@ -260,6 +271,21 @@ def attn_tile_config(B, Hq, Hkv, Sq, Skv, D, causal, input_pos, dtype):
         raise AttnError("attn_tile_config: " + attn_status_string(st), st)
     keys = ("block_m", "block_n", "stages", "grid", "smem_bytes")
     return {k: o.value for k, o in zip(keys, out)}
+
+
+def attn_dispatch(B, Hq, Hkv, Sq, Skv, D, causal, input_pos, dtype,
+                  window=0, num_splits=0):
+    """The forward dispatch-table entry for these arguments, as a dict
+    (host only)."""
+    d = _Dispatch()
+    st = int(load_library().attn_dispatch(
+        B, Hq, Hkv, Sq, Skv, D, int(causal), int(input_pos), int(window),
+        int(dtype), int(num_splits), ctypes.byref(d)))
+    if st != ATTN_OK:
+        raise AttnError("attn_dispatch: " + attn_status_string(st), st)
+    out = {n: getattr(d, n) for n, _ in _Dispatch._fields_}
+    out["name"] = d.name.decode()
+    return out
 
 
 def attn_version() -> int:

@@ -115,6 +115,15 @@ long long m_blocks(const Shape& s) {
   return (static_cast<long long>(s.Sq) + rows - 1) / rows;
 }
 
+// Unit order of the two-tile modes.  Heaviest m-block first (a longest-
+// processing-time order over the persistent CTAs) whenever a causal mask
+// makes units differ in work; without a mask every unit is equal, and the
+// m-blocks of one head run together so the K/V in flight stays in L2.  (A
+// causal offset far past the rows also makes units nearly equal -- the
+// prefill chunk's see 29 to 32 key tiles -- yet there the head-major order
+// measured 2 % slower than the balanced one.)
+bool head_major(const Shape& s) { return !s.causal; }
+
 long long grid_size(const Shape& s) {
   if (pack_gqa(s)) return static_cast<long long>(s.B) * s.Hkv;
   const long long units = pair_heads(s) ? static_cast<long long>(s.B) * (s.Hq / 2)
@@ -398,6 +407,7 @@ attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
   p.window = s.causal != 0 ? s.window : 0;
   p.num_m_blocks = static_cast<int>(m_blocks(s));
   p.pair_heads = pair_heads(s);
+  p.head_major = !pack && head_major(s);
   p.pack_gqa = pack;
   p.group = group;
   // D * element-size bytes per row: 128 rows per tile, or group*Sq packed.
@@ -824,6 +834,55 @@ attn_status_t attn_tile_config(int B, int Hq, int Hkv, int Sq, int Skv, int D,
   if (stages) *stages = t.stages;
   if (grid) *grid = static_cast<int>(grid_size(s));
   if (smem_bytes) *smem_bytes = t.smem_bytes;
+  return ATTN_OK;
+}
+
+attn_status_t attn_dispatch(int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                            int causal, int input_pos, int window,
+                            attn_dtype_t dtype, int num_splits,
+                            attn_dispatch_t* out) {
+  if (out == nullptr) return ATTN_ERR_INVALID_ARG;
+  const Shape s{B, Hq, Hkv, Sq, Skv, D, causal != 0, input_pos, window};
+  const attn_status_t st = check_scalars(s, 1.0f, dtype);
+  if (st != ATTN_OK) return st;
+  if (num_splits < 0 || num_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
+  const TileChoice t = choose_tiles(s, dtype);
+  const bool pack = pack_gqa(s);
+  int splits = 1, tiles = 0;
+  if (num_splits > 0) splitkv_shape(s, num_splits, 1, &splits, &tiles);
+  const bool split = num_splits > 0;
+  attn_dispatch_t d{};
+  d.block_m = t.block_m;
+  d.block_n = t.block_n;
+  d.q_tiles = pack ? 1 : 2;
+  d.paired = !pack && pair_heads(s);
+  d.s_buffers = (!pack && s.D == 64) ? 3 : 2;
+  d.stages = t.stages;
+  d.order = (!pack && head_major(s)) ? 1 : 0;
+  d.o_store = (!pack && !split) ? 1 : 0;
+  d.hold_scores = pack ? 0 : 1;
+  d.num_splits = split ? splits : 0;
+  d.units = static_cast<int>(grid_size(s) * splits);
+  d.smem_bytes = t.smem_bytes;
+  // Static names: D x element type x tile mode x order x O store.
+  static const char* const kNames[2][3][3][2][2] = {
+#define ATTN_N(d, e, m, o, st) "d" d "." e "." m "." o "." st
+#define ATTN_O(d, e, m)                                          \
+  {{ATTN_N(d, e, m, "lpt", "rows"), ATTN_N(d, e, m, "lpt", "tma")}, \
+   {ATTN_N(d, e, m, "head-major", "rows"),                       \
+    ATTN_N(d, e, m, "head-major", "tma")}}
+#define ATTN_M(d, e)                                                \
+  {ATTN_O(d, e, "paired-heads"), ATTN_O(d, e, "256-rows"),           \
+   ATTN_O(d, e, "gqa-packed")}
+      {ATTN_M("64", "f16"), ATTN_M("64", "bf16"), ATTN_M("64", "e4m3")},
+      {ATTN_M("128", "f16"), ATTN_M("128", "bf16"), ATTN_M("128", "e4m3")}};
+#undef ATTN_M
+#undef ATTN_O
+#undef ATTN_N
+  const int mode = pack ? 2 : (d.paired ? 0 : 1);
+  d.name =
+      kNames[s.D == 128][static_cast<int>(dtype)][mode][d.order][d.o_store];
+  *out = d;
   return ATTN_OK;
 }
 

@@ -53,6 +53,9 @@ struct FwdParams {
   int window;              // sliding window in keys (causal only), 0: none
   int num_m_blocks;        // m-blocks per head (of 128 or 256 rows)
   int pair_heads;          // a unit = 2 heads x 128 rows (else 1 head x 256)
+  // Unit order: 0 heaviest m-block first, the heads of an m-block in turn;
+  // 1 (units of equal work) the m-blocks of a head (pair) in turn.
+  int head_major;
   // GQA packing (few query rows): one Q tile holds the Sq rows of all
   // `group` query heads of a K/V head, row r = head (r / Sq), position
   // (r % Sq); the second tile is unused.
@@ -180,9 +183,10 @@ __device__ __forceinline__ TileKeys tile_keys(const FwdParams& p, int m0) {
 // One work unit: two 128-row Q tiles.  With an even GQA group the tiles
 // are two query heads of one K/V group at the same rows (identical causal
 // extents and masks, shared K/V tiles); otherwise two consecutive row blocks
-// of one head.  Unit 0 is the heaviest causal m-block (the page's reversed
-// block order); consecutive units are consecutive heads, so the heads of a
-// K/V group run together and find K/V in L2.
+// of one head.  Unit 0 is the heaviest m-block (the page's reversed block
+// order) and consecutive units are consecutive heads, so the heads of a K/V
+// group run together and find K/V in L2; with units of equal work
+// (p.head_major) consecutive units are the m-blocks of one head (pair).
 struct Unit {
   int kb;        // first K/V tile the unit streams (tile j of the unit is
                  // key tile kb + j)
@@ -217,9 +221,14 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
     tk[0] = tile_keys<kWindow>(p, 0);
     tk[1] = TileKeys{0, 0, 0, 0};
   } else {
+    // Heaviest row block first, the heads of a row block in turn; or, when
+    // every unit carries the same work (no mask), the row blocks of a head
+    // in turn, so that the units in flight share a few heads' K/V (which
+    // stay in L2) instead of each streaming its own head's.
     const int per_m = p.pair_heads ? p.B * (p.Hq / 2) : p.B * p.Hq;
-    const int mb = p.num_m_blocks - 1 - u / per_m;
-    const int ub = u % per_m;
+    const int mb = p.head_major ? u % p.num_m_blocks
+                                : p.num_m_blocks - 1 - u / per_m;
+    const int ub = p.head_major ? u / p.num_m_blocks : u % per_m;
     const int b = p.pair_heads ? ub / (p.Hq / 2) : ub / p.Hq;
     const int h0 = p.pair_heads ? 2 * (ub % (p.Hq / 2)) : ub % p.Hq;
     w.kv_plane = b * p.Hkv + h0 / (p.Hq / p.Hkv);

@@ -346,6 +346,46 @@ attn_status_t attn_tile_config(int B, int Hq, int Hkv, int Sq, int Skv, int D,
                                int* block_m, int* block_n, int* stages,
                                int* grid, int* smem_bytes);
 
+/*
+ * attn_dispatch_t / attn_dispatch — the forward dispatch-table entry a call
+ * with these arguments runs, spelled out (host only, no GPU needed).  The
+ * entry is keyed on D, dtype, causal / window, the GQA group size and Sq
+ * (the tile shape and work unit) and on num_splits (one pass or split-KV):
+ *   q_tiles 2, paired 1   two query heads of one K/V group at the same 128
+ *                         rows per unit (even group size);
+ *   q_tiles 2, paired 0   256 consecutive rows of one head per unit;
+ *   q_tiles 1             the group * Sq <= 128 query rows of all heads of
+ *                         a K/V group packed into one tile (few query rows);
+ *   s_buffers             score tiles in TMEM: 2, or 3 rotating between the
+ *                         two Q tiles at D = 64 (O needs only 128 columns);
+ *   order 0               heaviest causal row block first, the heads of a
+ *                         row block in turn (longest-processing-time order
+ *                         over the persistent CTAs); order 1: the row blocks
+ *                         of one head in turn (non-causal: equal units, K/V
+ *                         of the few heads in flight stays in L2);
+ *   o_store 1             O leaves through a 128-byte-swizzled shared-memory
+ *                         box stored by TMA; 0: each softmax thread stores
+ *                         its row (packed tiles, split-KV fp32 partials);
+ *   hold_scores 1         the softmax keeps a row's 128 scores in registers
+ *                         between its max and exp passes (register split).
+ * units is the number of work units (the launch runs min(units, SM count)
+ * persistent CTAs), stages the K/V tiles in flight, smem_bytes the dynamic
+ * shared memory per CTA.  name is a static string naming the entry.
+ * num_splits: 0 for the one-pass forward, else as attn_fwd_splitkv
+ * (planned count; units then count (rows, key range) pairs).  Returns the
+ * validation code the call would; out must be non-NULL.
+ */
+typedef struct {
+  int block_m, block_n, q_tiles, paired, s_buffers, stages;
+  int order, o_store, hold_scores, num_splits, units, smem_bytes;
+  const char* name;
+} attn_dispatch_t;
+
+attn_status_t attn_dispatch(int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                            int causal, int input_pos, int window,
+                            attn_dtype_t dtype, int num_splits,
+                            attn_dispatch_t* out);
+
 /* Library version as major*10000 + minor*100 + patch. */
 int attn_version(void);
 
