@@ -52,9 +52,10 @@ def selftest(w, q, k, v, o, lse, stream):
 def check_timeout_code(st, code):
     assert st == attn.ATTN_ERR_TIMEOUT, (st, code)
     assert code & 0xFF == 1, hex(code)
-    # Producer (1), MMA issuer (2) and softmax (3) all wait on the missing
-    # tile's consequences; whichever run out first OR their numbers.
-    assert 1 <= (code >> 8) & 0xFF <= 3, hex(code)
+    # Producer (1), MMA issuer (2), softmax (3) and output store (4) all
+    # wait on the missing tile's consequences; whichever run out first OR
+    # their numbers in.
+    assert 1 <= (code >> 8) & 0xFF <= 7, hex(code)
 
 
 def test_wait_runs_out_and_context_stays_usable():
