@@ -276,6 +276,9 @@ int fwd_stages(int D, bool pack, bool fp8) {
 namespace {
 
 constexpr int kMaxSplits = 128;
+// Largest key-range count merged inside a thread-block cluster (the
+// portable cluster size).
+constexpr int kMaxClusterSplits = 8;
 constexpr size_t kWorkspaceAlign = 256;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -425,6 +428,11 @@ attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
   p.merge_ctr = merge_ctr;
   p.merge_seq = merge_ctr != nullptr ? next_merge_seq() : 0u;
   p.num_units = static_cast<int>(grid_size(s) * splits);
+  // Packed split-KV whose units all fit in one wave: the key ranges of a
+  // (batch, K/V head) run as one cluster and merge over distributed shared
+  // memory.  (The workspace still has to be valid: it is the fallback.)
+  p.cluster_merge = pack && splits > 1 && splits <= kMaxClusterSplits &&
+                    p.num_units <= sms && o_part != nullptr;
   p.status = status;
   p.timeout_ns = timeout != 0 ? timeout : timeout_ns();
   p.withhold_first_load = withhold_first_load;
@@ -432,8 +440,8 @@ attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
   // Persistent launch: at most one CTA per SM, each walking its units.
   const int grid = static_cast<int>(std::min<long long>(p.num_units, sms));
   const bool bf16 = dtype == ATTN_BF16;
-  const cudaError_t err =
-      dtype == ATTN_E4M3
+  auto launch = [&]() {
+    return dtype == ATTN_E4M3
           ? (pack ? attn::launch_fwd_d128_fp8_packed(tq, tk, tv, to, p, grid,
                                                    stream)
                   : attn::launch_fwd_d128_fp8(tq, tk, tv, to, p, grid, stream))
@@ -444,6 +452,15 @@ attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
           : (pack ? attn::launch_fwd_d128_packed(bf16, tq, tk, tv, to, p, grid,
                                                stream)
                   : attn::launch_fwd_d128(bf16, tq, tk, tv, to, p, grid, stream));
+  };
+  cudaError_t err = launch();
+  if (err != cudaSuccess && p.cluster_merge) {
+    // No cluster of that size could be placed: merge through the
+    // workspace and its counters instead.
+    cudaGetLastError();
+    p.cluster_merge = 0;
+    err = launch();
+  }
   return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -81,6 +81,12 @@ struct FwdParams {
   // completes the set merges the key ranges of that tile's rows into O/LSE.
   unsigned long long* merge_ctr;  // [num_units / num_splits, 2]
   unsigned int merge_seq;         // nonzero, distinct per call
+  // Packed split-KV launch whose units all run at once, one per CTA, the
+  // num_splits key ranges of a (batch, K/V head) forming one thread-block
+  // cluster (rank = key range): each CTA keeps its partial results in its
+  // own shared memory and rank 0 merges them over distributed shared
+  // memory (no global partials, no counters).
+  int cluster_merge;
   unsigned int* status;    // device status word (timeouts)
   unsigned long long timeout_ns;
   // Self-test of the bounded waits (0 in every normal launch): CTA 0's
@@ -338,6 +344,59 @@ __device__ __forceinline__ void merge_tile(const FwdParams& p, int plane0,
       const float4 x = __ldcg(
           reinterpret_cast<const float4*>(p.o_part + (c * rows + row) * D) +
           cg);
+      wsum += wc;
+      acc.x += wc * x.x;
+      acc.y += wc * x.y;
+      acc.z += wc * x.z;
+      acc.w += wc * x.w;
+    }
+    const float inv = ptx::rcp(wsum);
+    uint2 out;
+    out.x = ptx::pack2<kBF16>(acc.x * inv, acc.y * inv);
+    out.y = ptx::pack2<kBF16>(acc.z * inv, acc.w * inv);
+    reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.o) + row * D)[cg] = out;
+    if (cg == 0 && p.lse != nullptr)
+      p.lse[row] = mx + ptx::lg2(wsum) * cfg::kLn2;
+  }
+}
+
+// The cluster form of merge_tile (packed tiles): the partial output rows of
+// key range c live in cluster CTA c's shared memory, row r at
+// part + r * D * 4 bytes, its LSE at part + kTM * D * 4 + r * 4.  Same
+// weights as merge_tile; ranges past a row's causal horizon or before its
+// window hold nothing for it and are not read.
+template <int D, bool kBF16, bool kWindow>
+__device__ __forceinline__ void merge_tile_cluster(const FwdParams& p,
+                                                   int plane0, uint32_t part,
+                                                   int tid) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  constexpr int kGroups = D / 4;
+  constexpr int kRowsPerPass = cfg::kTM / kGroups;
+  const uint32_t lse_off = cfg::kTM * D * 4;
+  const int split_keys = p.split_tiles * cfg::kTN;
+  const int nrows = p.group * p.Sq;
+  const int cg = tid % kGroups;
+  for (int r = tid / kGroups; r < nrows; r += kRowsPerPass) {
+    const int q_plane = plane0 + r / p.Sq;
+    const int q_row = r % p.Sq;
+    const long long row = static_cast<long long>(q_plane) * p.Sq + q_row;
+    const int row_pos = p.input_pos + q_row;
+    const int vis_end = p.causal ? min(p.Skv, row_pos + 1) : p.Skv;
+    const int ns = min(p.num_splits, (vis_end + split_keys - 1) / split_keys);
+    const int c0 =
+        kWindow ? max(0, row_pos - p.window + 1) / split_keys : 0;
+    const uint32_t lse_addr = part + lse_off + 4 * r;
+    const uint32_t o_addr = part + (r * D + 4 * cg) * 4;
+    float mx = -INFINITY;
+    for (int c = c0; c < ns; ++c)
+      mx = fmaxf(mx, ptx::ld_shared_cluster_f32(ptx::mapa_shared(lse_addr, c)));
+    float wsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = c0; c < ns; ++c) {
+      const float wc = ptx::ex2(
+          (ptx::ld_shared_cluster_f32(ptx::mapa_shared(lse_addr, c)) - mx) *
+          kLog2e);
+      const float4 x = ptx::ld_shared_cluster_v4(ptx::mapa_shared(o_addr, c));
       wsum += wc;
       acc.x += wc * x.x;
       acc.y += wc * x.y;
@@ -1170,28 +1229,55 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
         const bool empty = !(l_run > 0.f);
         const float inv_l =
             empty ? 0.f : (kFp8 ? ptx::rcp(l_run) * p.o_scale : ptx::rcp(l_run));
-        const long long prow =
-            (static_cast<long long>(w.split) * p.B * p.Hq + q_plane) * p.Sq +
-            q_row;
-        float4* orow = reinterpret_cast<float4*>(p.o_part + prow * D);
+        const float lse_row =
+            empty ? -INFINITY : (m_run + ptx::lg2(l_run)) * kLn2;
+        if (kPack && p.cluster_merge) {
+          // Into this CTA's shared memory (the K/V ring, idle now: every
+          // MMA of the unit is done), row r at r * D * 4 bytes; rank 0 of
+          // the cluster reads it after the cluster barrier below.
+          const uint32_t part = s_base + L::kRingOff;
 #pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
-          uint32_t o[32];
-          ptx::tmem_ld32(t_o + 32 * q, o);
-          ptx::tmem_wait_ld();
-          if (row_ok) {
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t o[32];
+            ptx::tmem_ld32(t_o + 32 * q, o);
+            ptx::tmem_wait_ld();
+            if (row_ok) {
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              orow[8 * q + v] = make_float4(__uint_as_float(o[4 * v]) * inv_l,
-                                            __uint_as_float(o[4 * v + 1]) * inv_l,
-                                            __uint_as_float(o[4 * v + 2]) * inv_l,
-                                            __uint_as_float(o[4 * v + 3]) * inv_l);
+              for (int v = 0; v < 8; ++v)
+                ptx::st_shared_v4(
+                    part + (r * D + 32 * q + 4 * v) * 4,
+                    __float_as_uint(__uint_as_float(o[4 * v]) * inv_l),
+                    __float_as_uint(__uint_as_float(o[4 * v + 1]) * inv_l),
+                    __float_as_uint(__uint_as_float(o[4 * v + 2]) * inv_l),
+                    __float_as_uint(__uint_as_float(o[4 * v + 3]) * inv_l));
+            }
           }
+          if (row_ok) ptx::st_shared_f32(part + kTM * D * 4 + 4 * r, lse_row);
+        } else {
+          const long long prow =
+              (static_cast<long long>(w.split) * p.B * p.Hq + q_plane) *
+                  p.Sq +
+              q_row;
+          float4* orow = reinterpret_cast<float4*>(p.o_part + prow * D);
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t o[32];
+            ptx::tmem_ld32(t_o + 32 * q, o);
+            ptx::tmem_wait_ld();
+            if (row_ok) {
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                orow[8 * q + v] =
+                    make_float4(__uint_as_float(o[4 * v]) * inv_l,
+                                __uint_as_float(o[4 * v + 1]) * inv_l,
+                                __uint_as_float(o[4 * v + 2]) * inv_l,
+                                __uint_as_float(o[4 * v + 3]) * inv_l);
+            }
+          }
+          if (row_ok) p.lse_part[prow] = lse_row;
         }
-        if (row_ok)
-          p.lse_part[prow] = empty ? -INFINITY : (m_run + ptx::lg2(l_run)) * kLn2;
       }
-      if constexpr (kSplit) {
+      if (kSplit && !(kPack && p.cluster_merge)) {
         // The unit that lands last among the key ranges of this tile's rows
         // merges them (no second launch).  The warpgroup barrier orders all
         // its partial writes before the counter update (a release at GPU
@@ -1222,6 +1308,33 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
+  if constexpr (kPack && kSplit) {
+    if (p.cluster_merge) {
+      // Every thread of every CTA of the cluster takes part in both
+      // barriers, on every path (an aborted CTA too), so neither can wait
+      // for a thread that will not come.  After the first, rank 0's softmax
+      // warps merge the key ranges (unless some CTA of the cluster gave up
+      // a wait: then the status word already reports it); the second keeps
+      // every CTA's shared memory alive until rank 0 has read it.
+      ptx::cluster_arrive_release();
+      ptx::cluster_wait_acquire();
+      if (ptx::cluster_ctarank() == 0 && warp >= kSoftmaxWarp0 &&
+          warp < kSoftmaxWarp0 + 4) {
+        const uint32_t abort_addr = s_base + L::kMiscOff + 4;
+        bool all_ok = true;
+        for (int c = 0; c < p.num_splits; ++c)
+          all_ok = all_ok &&
+                   ptx::ld_shared_cluster_s32(ptx::mapa_shared(abort_addr, c)) == 0;
+        if (all_ok) {
+          const Unit w = decode_unit<kPack, kWindow>(p, u_first);
+          merge_tile_cluster<D, kBF16, kWindow>(
+              p, w.plane[0], s_base + L::kRingOff, threadIdx.x % 128);
+        }
+      }
+      ptx::cluster_arrive_release();
+      ptx::cluster_wait_acquire();
+    }
+  }
   if (warp == kMmaWarp) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);

@@ -43,6 +43,17 @@ cudaError_t launch_variant(const CUtensorMap& q, const CUtensorMap& k,
   cfg.blockDim = dim3(cfg::kThreads, 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = stream;
+  // The key ranges of one (batch, K/V head) as one thread-block cluster
+  // (the grid holds every unit, num_splits consecutive CTAs per group).
+  cudaLaunchAttribute attr[1];
+  if (p.cluster_merge) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.num_splits);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
   return cudaLaunchKernelEx(&cfg, kernel, q, k, v, o, p);
 }
 

@@ -153,3 +153,29 @@ def test_workspace_contents_and_reuse(fill):
             TOL_O[w.dtype], (w.name, s)
         assert float(np.max(np.abs(lse.double().cpu().numpy() - lse_ref))) <= \
             TOL_LSE, (w.name, s)
+
+
+@pytest.mark.parametrize("w, splits", [
+    # 40 x 8 (batch, K/V head) groups x 2 ranges: more units than SMs, so
+    # the key ranges merge through the workspace and its counters.
+    (W("many_groups", 40, 32, 8, 1, 700, 128, "bf16", True, 699), 2),
+    # 2 groups x 8 ranges: every unit runs at once, each group's 8 ranges
+    # form one thread-block cluster and merge over its shared memory.
+    (W("cluster_of_8", 1, 8, 2, 1, 4000, 128, "f16", True, 3999), 8),
+    (W("cluster_window", 2, 8, 2, 3, 3000, 64, "bf16", True, 2997), 4),
+], ids=["counter_merge", "cluster_merge_8", "cluster_merge_window"])
+def test_merge_paths_against_oracle(w, splits):
+    """Both ways of merging the key ranges of packed split-KV tiles."""
+    q, k, v = make_qkv(w, seed=31)
+    window = 1500 if "window" in w.name else 0
+    o, lse = attn.fwd_splitkv(q.cuda(), k.cuda(), v.cuda(), scale=w.scale,
+                              causal=True, input_pos=w.input_pos,
+                              num_splits=splits, window=window)
+    torch.cuda.synchronize()
+    assert attn.attn_device_status() == (0, 0)
+    o_ref, lse_ref = oracle.attention(q, k, v, w.scale, True, w.input_pos,
+                                      window)
+    assert float(np.max(np.abs(o.double().cpu().numpy() - o_ref))) <= \
+        TOL_O[w.dtype]
+    assert float(np.max(np.abs(lse.double().cpu().numpy() - lse_ref))) <= \
+        TOL_LSE
