@@ -244,3 +244,38 @@ def test_bwd_workspace_bytes(lib):
     # Padding: every Sq in one 128-row tile needs the same workspace.
     assert len({attn.attn_bwd_workspace_bytes(1, 4, s)
                 for s in range(1, 129)}) == 1
+
+
+def test_dispatch_entries_host_only(lib):
+    """attn_dispatch names the table entry without a GPU: tile mode, unit
+    order and O store follow the group size, Sq, the mask and the split
+    count; bad arguments get the validation code attn_fwd would return."""
+    bf, f16, e4 = attn.ATTN_BF16, attn.ATTN_F16, attn.ATTN_E4M3
+    e = attn.attn_dispatch(1, 32, 4, 8192, 8192, 128, 1, 0, bf)
+    assert e["name"] == "d128.bf16.paired-heads.lpt.tma"
+    assert (e["q_tiles"], e["paired"], e["s_buffers"], e["order"],
+            e["o_store"], e["hold_scores"], e["num_splits"]) == \
+        (2, 1, 2, 0, 1, 1, 0)
+    assert e["units"] == 32 // 2 * 8192 // 128
+    e = attn.attn_dispatch(4, 16, 16, 1024, 1024, 64, 0, 0, f16)
+    assert e["name"] == "d64.f16.256-rows.head-major.tma"
+    assert e["s_buffers"] == 3 and e["units"] == 4 * 16 * 4
+    e = attn.attn_dispatch(8, 32, 8, 1, 4096, 128, 1, 4095, bf, num_splits=2)
+    assert e["name"] == "d128.bf16.gqa-packed.lpt.rows"
+    assert e["q_tiles"] == 1 and e["num_splits"] == 2
+    assert e["units"] == 8 * 8 * 2 and e["block_m"] == 4
+    e = attn.attn_dispatch(1, 32, 4, 8192, 8192, 128, 1, 0, e4)
+    assert e["name"] == "d128.e4m3.paired-heads.lpt.tma"
+    # window entry: causal, LPT order
+    e = attn.attn_dispatch(1, 32, 4, 32768, 32768, 128, 1, 0, bf,
+                           window=4096)
+    assert e["order"] == 0
+    for bad in [dict(Hq=3, Hkv=2), dict(D=96), dict(window=8, causal=0)]:
+        args = dict(B=1, Hq=2, Hkv=2, Sq=64, Skv=64, D=64, causal=1,
+                    input_pos=0, dtype=f16)
+        args.update(bad)
+        with pytest.raises(attn.AttnError):
+            attn.attn_dispatch(args["B"], args["Hq"], args["Hkv"], args["Sq"],
+                               args["Skv"], args["D"], args["causal"],
+                               args["input_pos"], args["dtype"],
+                               window=args.get("window", 0))
