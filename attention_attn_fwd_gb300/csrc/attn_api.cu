@@ -428,6 +428,12 @@ attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
   p.merge_ctr = merge_ctr;
   p.merge_seq = merge_ctr != nullptr ? next_merge_seq() : 0u;
   p.num_units = static_cast<int>(grid_size(s) * splits);
+  p.fd_splits = attn::make_fast_div(splits);
+  p.fd_m_blocks = attn::make_fast_div(p.num_m_blocks);
+  p.fd_heads = attn::make_fast_div(p.pair_heads ? s.Hq / 2 : s.Hq);
+  p.fd_per_m = attn::make_fast_div(s.B * p.fd_heads.d);
+  p.fd_group = attn::make_fast_div(group);
+  p.fd_hkv = attn::make_fast_div(s.Hkv);
   // Packed split-KV whose units all fit in one wave: the key ranges of a
   // (batch, K/V head) run as one cluster and merge over distributed shared
   // memory.  (The workspace still has to be valid: it is the fallback.)

@@ -42,6 +42,7 @@
 #include <cuda.h>
 
 #include "attn_sync.cuh"
+#include "fast_div.h"
 #include "sm103_ptx.cuh"
 
 namespace attn {
@@ -87,6 +88,10 @@ struct FwdParams {
   // own shared memory and rank 0 merges them over distributed shared
   // memory (no global partials, no counters).
   int cluster_merge;
+  // Divisors of the unit decode: num_splits, num_m_blocks, units per
+  // m-block (B*Hq/2 paired, else B*Hq), heads per batch entry (Hq/2 paired,
+  // else Hq), group, and Hkv (packed units).
+  FastDiv fd_splits, fd_m_blocks, fd_per_m, fd_heads, fd_group, fd_hkv;
   unsigned int* status;    // device status word (timeouts)
   unsigned long long timeout_ns;
   // Self-test of the bounded waits (0 in every normal launch): CTA 0's
@@ -211,15 +216,18 @@ struct Unit {
 template <bool kPack, bool kWindow>
 __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   Unit w;
-  w.split = u % p.num_splits;
-  u /= p.num_splits;
+  {
+    const int us = fast_div(u, p.fd_splits);
+    w.split = u - us * p.num_splits;
+    u = us;
+  }
   const int kt0 = w.split * p.split_tiles;  // key range of the unit
   const int kt1 = kt0 + p.split_tiles;
   TileKeys tk[2];
   if constexpr (kPack) {
     // Unit = one (batch, K/V head): tile 0 holds all its query rows.
-    const int b = u / p.Hkv;
-    const int kvh = u % p.Hkv;
+    const int b = fast_div(u, p.fd_hkv);
+    const int kvh = u - b * p.Hkv;
     w.kv_plane = b * p.Hkv + kvh;
     w.plane[0] = b * p.Hq + kvh * p.group;  // first head of the group
     w.plane[1] = w.plane[0];
@@ -231,13 +239,19 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
     // every unit carries the same work (no mask), the row blocks of a head
     // in turn, so that the units in flight share a few heads' K/V (which
     // stay in L2) instead of each streaming its own head's.
-    const int per_m = p.pair_heads ? p.B * (p.Hq / 2) : p.B * p.Hq;
-    const int mb = p.head_major ? u % p.num_m_blocks
-                                : p.num_m_blocks - 1 - u / per_m;
-    const int ub = p.head_major ? u / p.num_m_blocks : u % per_m;
-    const int b = p.pair_heads ? ub / (p.Hq / 2) : ub / p.Hq;
-    const int h0 = p.pair_heads ? 2 * (ub % (p.Hq / 2)) : ub % p.Hq;
-    w.kv_plane = b * p.Hkv + h0 / (p.Hq / p.Hkv);
+    int mb, ub;
+    if (p.head_major) {
+      ub = fast_div(u, p.fd_m_blocks);
+      mb = u - ub * p.num_m_blocks;
+    } else {
+      const int q = fast_div(u, p.fd_per_m);
+      mb = p.num_m_blocks - 1 - q;
+      ub = u - q * p.fd_per_m.d;
+    }
+    const int b = fast_div(ub, p.fd_heads);
+    const int hh = ub - b * p.fd_heads.d;
+    const int h0 = p.pair_heads ? 2 * hh : hh;
+    w.kv_plane = b * p.Hkv + fast_div(h0, p.fd_group);
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       w.plane[t] = b * p.Hq + h0 + (p.pair_heads ? t : 0);
@@ -1289,7 +1303,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
         ptx::named_barrier_sync(1 + t, kTM);
         if (r == 0)
           *merge_flag = merge_arrive(
-              p.merge_ctr + 2 * (u / p.num_splits) + t, p.merge_seq,
+              p.merge_ctr + 2 * fast_div(u, p.fd_splits) + t, p.merge_seq,
               ranges_visited(p, w, t), p);
         ptx::named_barrier_sync(1 + t, kTM);
         if (*merge_flag) {
