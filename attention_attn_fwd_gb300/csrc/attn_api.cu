@@ -278,7 +278,7 @@ namespace {
 constexpr int kMaxSplits = 128;
 // Largest key-range count merged inside a thread-block cluster (the
 // portable cluster size).
-constexpr int kMaxClusterSplits = 8;
+constexpr int kMaxClusterSplits = attn::cfg::kMaxClusterRanges;
 constexpr size_t kWorkspaceAlign = 256;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

@@ -112,6 +112,8 @@ constexpr int kMmaWarp = 0;
 constexpr int kLoadWarp = 1;
 constexpr int kSoftmaxWarp0 = 4;  // warps 4-7: Q tile 0, warps 8-11: Q tile 1
 constexpr int kTmemCols = 512;
+// Key ranges merged in one thread-block cluster (the portable cluster size).
+constexpr int kMaxClusterRanges = 8;
 constexpr float kRescaleTau = 8.0f;  // lazy rescale threshold (log2 units)
 // Register split of the variants that hold a whole S row (128 fp32) in
 // registers from the max pass to the exp pass (all two-tile variants: 1-5 %
@@ -401,21 +403,33 @@ __device__ __forceinline__ void merge_tile_cluster(const FwdParams& p,
         kWindow ? max(0, row_pos - p.window + 1) / split_keys : 0;
     const uint32_t lse_addr = part + lse_off + 4 * r;
     const uint32_t o_addr = part + (r * D + 4 * cg) * 4;
+    // Every range's LSE and columns are requested before any is used: one
+    // round trip over the cluster instead of one per range and pass.
+    float lse_c[cfg::kMaxClusterRanges];
+    float4 x_c[cfg::kMaxClusterRanges];
+#pragma unroll
+    for (int c = 0; c < cfg::kMaxClusterRanges; ++c) {
+      lse_c[c] = -INFINITY;
+      x_c[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c >= c0 && c < ns) {
+        lse_c[c] = ptx::ld_shared_cluster_f32(ptx::mapa_shared(lse_addr, c));
+        x_c[c] = ptx::ld_shared_cluster_v4(ptx::mapa_shared(o_addr, c));
+      }
+    }
     float mx = -INFINITY;
-    for (int c = c0; c < ns; ++c)
-      mx = fmaxf(mx, ptx::ld_shared_cluster_f32(ptx::mapa_shared(lse_addr, c)));
+#pragma unroll
+    for (int c = 0; c < cfg::kMaxClusterRanges; ++c) mx = fmaxf(mx, lse_c[c]);
     float wsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c = c0; c < ns; ++c) {
-      const float wc = ptx::ex2(
-          (ptx::ld_shared_cluster_f32(ptx::mapa_shared(lse_addr, c)) - mx) *
-          kLog2e);
-      const float4 x = ptx::ld_shared_cluster_v4(ptx::mapa_shared(o_addr, c));
+#pragma unroll
+    for (int c = 0; c < cfg::kMaxClusterRanges; ++c) {
+      // Ranges outside [c0, ns) hold LSE -inf: weight 0.
+      const float wc = ptx::ex2((lse_c[c] - mx) * kLog2e);
       wsum += wc;
-      acc.x += wc * x.x;
-      acc.y += wc * x.y;
-      acc.z += wc * x.z;
-      acc.w += wc * x.w;
+      acc.x += wc * x_c[c].x;
+      acc.y += wc * x_c[c].y;
+      acc.z += wc * x_c[c].z;
+      acc.w += wc * x_c[c].w;
     }
     const float inv = ptx::rcp(wsum);
     uint2 out;
@@ -1250,16 +1264,18 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
           // MMA of the unit is done), row r at r * D * 4 bytes; rank 0 of
           // the cluster reads it after the cluster barrier below.
           const uint32_t part = s_base + L::kRingOff;
+          // 64 columns per TMEM wait.
 #pragma unroll
-          for (int q = 0; q < D / 32; ++q) {
-            uint32_t o[32];
-            ptx::tmem_ld32(t_o + 32 * q, o);
+          for (int q = 0; q < D / 64; ++q) {
+            uint32_t o[64];
+            ptx::tmem_ld32(t_o + 64 * q, o);
+            ptx::tmem_ld32(t_o + 64 * q + 32, o + 32);
             ptx::tmem_wait_ld();
             if (row_ok) {
 #pragma unroll
-              for (int v = 0; v < 8; ++v)
+              for (int v = 0; v < 16; ++v)
                 ptx::st_shared_v4(
-                    part + (r * D + 32 * q + 4 * v) * 4,
+                    part + (r * D + 64 * q + 4 * v) * 4,
                     __float_as_uint(__uint_as_float(o[4 * v]) * inv_l),
                     __float_as_uint(__uint_as_float(o[4 * v + 1]) * inv_l),
                     __float_as_uint(__uint_as_float(o[4 * v + 2]) * inv_l),
@@ -1335,10 +1351,13 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
       if (ptx::cluster_ctarank() == 0 && warp >= kSoftmaxWarp0 &&
           warp < kSoftmaxWarp0 + 4) {
         const uint32_t abort_addr = s_base + L::kMiscOff + 4;
-        bool all_ok = true;
-        for (int c = 0; c < p.num_splits; ++c)
-          all_ok = all_ok &&
-                   ptx::ld_shared_cluster_s32(ptx::mapa_shared(abort_addr, c)) == 0;
+        // Every CTA's abort flag in one round trip.
+        int aborted = 0;
+#pragma unroll
+        for (int c = 0; c < cfg::kMaxClusterRanges; ++c)
+          if (c < p.num_splits)
+            aborted |= ptx::ld_shared_cluster_s32(ptx::mapa_shared(abort_addr, c));
+        const bool all_ok = aborted == 0;
         if (all_ok) {
           const Unit w = decode_unit<kPack, kWindow>(p, u_first);
           merge_tile_cluster<D, kBF16, kWindow>(

@@ -500,11 +500,23 @@ def run_decode(args, fp8=False):
             step(args.warmup + i)
             ends[i].record(stream)
         torch.cuda.synchronize()
+    # The same steps launched back to back, one event pair around them all:
+    # the rate a loop of decode steps sees, without the event and launch
+    # latency each isolated step above carries.
+    b2b_a = torch.cuda.Event(enable_timing=True)
+    b2b_b = torch.cuda.Event(enable_timing=True)
+    b2b_a.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i)
+    b2b_b.record(stream)
+    torch.cuda.synchronize()
     st, code = attn.attn_device_status()
     if st != attn.ATTN_OK:
         raise RuntimeError("device status %d code %#x" % (st, code))
     ms = sum(s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)) / args.steps
     gbs = w.io_bytes() / (ms * 1e-3) / 1e9
+    ms_b2b = b2b_a.elapsed_time(b2b_b) / args.steps
+    gbs_b2b = w.io_bytes() / (ms_b2b * 1e-3) / 1e9
     _, hbm, src = peaks()
     out = {
         "metric": "attention decode (split-KV) GB/s of algorithmic traffic"
@@ -520,6 +532,12 @@ def run_decode(args, fp8=False):
                   % (DECODE_SETS, DECODE_SETS * w.io_bytes() / 1e6),
             "algorithmic_bytes_per_step": w.io_bytes(),
             "tokens_per_s": round(w.B / (ms * 1e-3), 1),
+            "back_to_back": {
+                "note": "the same steps launched back to back between one "
+                        "event pair (value: each step between its own "
+                        "events)",
+                "ms_per_step": round(ms_b2b, 5), "GB/s": round(gbs_b2b, 1),
+                "frac": round(gbs_b2b / hbm, 4)},
             "tflops_formula": round(w.flops() / (ms * 1e-3) / 1e12, 2)}),
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
                      "unit": "GB/s", "frac": round(gbs / hbm, 4),
