@@ -33,7 +33,9 @@ FLUSH_BYTES = 256 << 20  # > 129 MB L2
 # probe kernel (one CTA per SM, dependent-free ex2 streams).
 EX2_PER_CLK_PER_SM = 32
 KERNEL_SOURCES = ["attention_attn_fwd_gb300/csrc/attn_fwd_kernel.cuh",
-                  "attention_attn_fwd_gb300/csrc/sm103_ptx.cuh"]
+                  "attention_attn_fwd_gb300/csrc/sm103_ptx.cuh",
+                  "attention_attn_fwd_gb300/csrc/attn_sync.cuh",
+                  "attention_attn_fwd_gb300/csrc/fast_div.h"]
 # DRAM bytes of one headline launch from an ncu capture (data file written
 # from the capture's summary; see the .md of the same name for the command).
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles",
