@@ -49,6 +49,11 @@ EDGE = [
     W("skv_tile_plus_one_causal", 1, 2, 2, 129, 257, 64, "f16", True, 128),
     W("long_keys_short_q", 1, 4, 4, 40, 2049, 128, "f16", False),
     W("sq_gt_skv_causal", 1, 2, 2, 600, 200, 64, "bf16", True),
+    # Head counts that are not powers of two: the unit decode divides by
+    # the group (3, 5, 6), by Hq or Hq / 2 and by the units per row block.
+    W("gqa3_causal_batch2", 2, 6, 2, 333, 333, 128, "bf16", True),
+    W("gqa6_paired_offset", 1, 12, 2, 300, 700, 64, "f16", True, 400),
+    W("gqa5_noncausal_batch3", 3, 10, 2, 200, 450, 64, "bf16", False),
     # Few query rows with grouped K/V heads: all heads of a group in one tile.
     W("packed_full_tile", 1, 32, 4, 16, 900, 128, "bf16", True, 884),
     W("packed_ragged", 2, 8, 2, 30, 333, 64, "f16", True, 303),
