@@ -21,7 +21,8 @@ __all__ = [
     "attn_splitkv_plan", "attn_fwd_splitkv_noalloc",
     "attn_noalloc_scratch_bytes", "attn_status_string", "attn_device_status",
     "attn_stream_status", "attn_selftest_wait_timeout", "attn_dispatch",
-    "attn_tile_config", "attn_version", "attn_bwd", "attn_bwd_workspace_bytes",
+    "attn_tile_config", "attn_unit_plan", "attn_version", "attn_bwd",
+    "attn_bwd_workspace_bytes",
     "fwd", "fwd_splitkv", "fwd_fp8", "bwd",
     "library_path", "load_library",
 ]
@@ -122,6 +123,9 @@ def load_library():
         lib.attn_dispatch.argtypes = [i, i, i, i, i, i, i, i, i, i, i,
                                       ctypes.POINTER(_Dispatch)]
         lib.attn_dispatch.restype = i
+        lp = ctypes.POINTER(ctypes.c_longlong)
+        lib.attn_unit_plan.argtypes = [i] * 10 + [ip, lp, lp, ip, ip]
+        lib.attn_unit_plan.restype = i
         lib.attn_stream_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
         lib.attn_stream_status.restype = i
         lib.attn_selftest_wait_timeout.argtypes = [
@@ -285,6 +289,34 @@ def attn_dispatch(B, Hq, Hkv, Sq, Skv, D, causal, input_pos, dtype,
         raise AttnError("attn_dispatch: " + attn_status_string(st), st)
     out = {n: getattr(d, n) for n, _ in _Dispatch._fields_}
     out["name"] = d.name.decode()
+    return out
+
+
+def attn_unit_plan(B, Hq, Hkv, Sq, Skv, D, causal, input_pos, grid,
+                   window=0):
+    """How a one-pass forward call assigns its units to `grid` CTAs (host
+    only): dict with planned, work_max, work_rounds (half K/V steps) and,
+    when planned, cta_units (one list of unit indices per CTA)."""
+    lib = load_library()
+    planned = ctypes.c_int(0)
+    wmax, wrounds = ctypes.c_longlong(0), ctypes.c_longlong(0)
+    d = attn_dispatch(B, Hq, Hkv, Sq, Skv, D, causal, input_pos, ATTN_BF16,
+                      window=window)
+    n = d["units"]
+    g = max(1, min(n, grid))
+    order = (ctypes.c_int * max(1, n))()
+    start = (ctypes.c_int * (g + 1))()
+    st = int(lib.attn_unit_plan(
+        B, Hq, Hkv, Sq, Skv, D, int(causal), int(input_pos), int(window),
+        int(grid), ctypes.byref(planned), ctypes.byref(wmax),
+        ctypes.byref(wrounds), order, start))
+    if st != ATTN_OK:
+        raise AttnError("attn_unit_plan: " + attn_status_string(st), st)
+    out = {"planned": planned.value, "work_max": wmax.value,
+           "work_rounds": wrounds.value, "units": n}
+    if planned.value:
+        out["cta_units"] = [list(order[start[c]:start[c + 1]])
+                            for c in range(g)]
     return out
 
 

@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdint>
 #include <algorithm>
+#include <vector>
 #include <atomic>
 #include <cstddef>
 #include <cstdlib>
@@ -366,6 +367,149 @@ attn_status_t check_call(const Shape& s, float scale, attn_dtype_t dtype,
   return ATTN_OK;
 }
 
+// ---------------------------------------------------------------- unit plan
+// Work (in K/V steps) of two-tile unit u of a one-pass launch: the key
+// tiles its later Q tile sees, from the first tile its earlier one sees.
+// The same arithmetic as the kernel's unit decode and tile_keys, for the
+// host's balancing only (a different count would only unbalance, never
+// drop or repeat a unit).
+int unit_steps(const Shape& s, long long u) {
+  const long long mbs = m_blocks(s);
+  const long long per_m = pair_heads(s) ? static_cast<long long>(s.B) * (s.Hq / 2)
+                                        : static_cast<long long>(s.B) * s.Hq;
+  const long long mb = head_major(s) ? u % mbs : mbs - 1 - u / per_m;
+  const int tm = attn::cfg::kTM, tn = attn::cfg::kTN;
+  int lo = 0, n_kv = 0;
+  for (int t = 0; t < 2; ++t) {
+    const long long m0 = pair_heads(s) ? mb * tm : mb * attn::cfg::kBlockM + t * tm;
+    if (m0 >= s.Sq) continue;
+    const long long pos_first = s.input_pos + m0;
+    const long long pos_last = s.input_pos + std::min<long long>(m0 + tm, s.Sq) - 1;
+    const long long kend = s.causal ? std::min<long long>(pos_last + 1, s.Skv) : s.Skv;
+    const int hi = static_cast<int>((kend + tn - 1) / tn);
+    if (t == 0 && s.window > 0)
+      lo = static_cast<int>(std::max<long long>(0, pos_first - s.window + 1) / tn);
+    n_kv = std::max(n_kv, hi - lo);
+  }
+  return n_kv;
+}
+
+// Unit assignment of a causal two-tile one-pass launch of `units` units on
+// `grid` CTAs.  The zigzag rounds leave the busiest CTA 2-4 % above the mean
+// (unit granularity: 7 units against 6); packing the units heaviest first
+// into the first CTA with room under a capacity, searched from the mean
+// upwards (first-fit decreasing, as in the MULTIFIT method of Coffman,
+// Garey and Johnson, 1978), leaves it within a fraction of a percent.  Each
+// unit costs its K/V steps plus 1.5 (a unit boundary, measured).  Returns
+// false (keep the zigzag rounds) when the plan would not be better.
+struct UnitPlan {
+  int units = 0;
+  long long work_max = 0;     // busiest CTA, half K/V steps
+  long long work_rounds = 0;  // the same under the zigzag rounds
+  unsigned short start[attn::kMaxPlanCtas + 1];
+  unsigned short unit[attn::kMaxPlanUnits];
+};
+
+// Plans the causal two-tile one-pass launches (other launches keep the
+// rounds: their units are equal, or they take another path).
+bool plannable(const Shape& s) {
+  return s.causal && !pack_gqa(s);
+}
+
+bool make_plan(const Shape& s, int units, int grid, UnitPlan* plan) {
+  plan->work_max = plan->work_rounds = 0;
+  if (!plannable(s) || units <= grid || units > attn::kMaxPlanUnits ||
+      grid > attn::kMaxPlanCtas)
+    return false;
+  std::vector<int> cost(units);  // in half steps
+  long long total = 0;
+  int cmax = 0;
+  for (int u = 0; u < units; ++u) {
+    const int n = unit_steps(s, u);
+    cost[u] = n > 0 ? 2 * n + 3 : 0;
+    total += cost[u];
+    cmax = std::max(cmax, cost[u]);
+  }
+  // Makespan of the zigzag rounds.
+  std::vector<long long> load(grid, 0);
+  for (int u = 0; u < units; ++u) {
+    const int k = u / grid, r = u % grid;
+    load[(k & 1) ? grid - 1 - r : r] += cost[u];
+  }
+  const long long zigzag = *std::max_element(load.begin(), load.end());
+  plan->work_max = plan->work_rounds = zigzag;
+  // Heaviest first; equal costs keep the unit order (heads in turn).
+  std::vector<int> order(units);
+  for (int u = 0; u < units; ++u) order[u] = u;
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int a, int b) { return cost[a] > cost[b]; });
+  std::vector<int> bin(units);
+  auto pack = [&](long long cap) {
+    std::fill(load.begin(), load.end(), 0);
+    for (int u : order) {
+      int c = 0;
+      while (c < grid && load[c] + cost[u] > cap) ++c;
+      if (c == grid) return false;
+      load[c] += cost[u];
+      bin[u] = c;
+    }
+    return true;
+  };
+  long long lo = std::max<long long>((total + grid - 1) / grid, cmax);
+  long long hi = zigzag - 1;  // a plan must beat the rounds
+  if (lo > hi || !pack(hi)) return false;
+  while (lo < hi) {  // smallest capacity that packs
+    const long long mid = (lo + hi) / 2;
+    if (pack(mid)) hi = mid; else lo = mid + 1;
+  }
+  pack(hi);
+  plan->work_max = *std::max_element(load.begin(), load.end());
+  // CTA c's units, heaviest first (the order they were packed in).
+  std::vector<int> count(grid, 0);
+  for (int u = 0; u < units; ++u) ++count[bin[u]];
+  plan->start[0] = 0;
+  for (int c = 0; c < grid; ++c)
+    plan->start[c + 1] = static_cast<unsigned short>(plan->start[c] + count[c]);
+  std::vector<int> fill(plan->start, plan->start + grid);
+  for (int u : order) plan->unit[fill[bin[u]]++] = static_cast<unsigned short>(u);
+  plan->units = units;
+  return true;
+}
+
+// Plans are computed once per launch shape and kept (a few dozen bytes of
+// key and 2.4 KB of plan each, the most recent kPlanCache shapes).
+constexpr int kPlanCache = 16;
+struct PlanEntry {
+  long long key[10];
+  bool used = false, valid = false;
+  UnitPlan plan;
+};
+std::mutex g_plan_mu;
+PlanEntry g_plans[kPlanCache];
+int g_plan_next = 0;
+
+// Copies the plan of this launch shape into `p` (computing it on first
+// use); leaves p.plan_units at 0 when the zigzag rounds stay.
+void apply_plan(const Shape& s, int units, int grid, attn::FwdParams* p) {
+  const long long key[10] = {s.B, s.Hq, s.Hkv, s.Sq, s.Skv, s.causal,
+                             s.input_pos, s.window, units, grid};
+  std::lock_guard<std::mutex> lock(g_plan_mu);
+  PlanEntry* e = nullptr;
+  for (PlanEntry& c : g_plans)
+    if (c.used && std::equal(key, key + 10, c.key)) e = &c;
+  if (e == nullptr) {
+    e = &g_plans[g_plan_next];
+    g_plan_next = (g_plan_next + 1) % kPlanCache;
+    std::copy(key, key + 10, e->key);
+    e->used = true;
+    e->valid = make_plan(s, units, grid, &e->plan);
+  }
+  if (!e->valid) return;
+  p->plan_units = e->plan.units;
+  std::copy(e->plan.start, e->plan.start + grid + 1, p->plan_start);
+  std::copy(e->plan.unit, e->plan.unit + units, p->plan_unit);
+}
+
 // Builds the tensor maps and parameters and launches the forward kernel.
 // `scale` is the score factor (FP8: times the Q and K descales), `o_scale`
 // multiplies O (FP8: the V descale; else 1).
@@ -445,6 +589,10 @@ attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
 
   // Persistent launch: at most one CTA per SM, each walking its units.
   const int grid = static_cast<int>(std::min<long long>(p.num_units, sms));
+  // Causal one-pass two-tile launches: units differ in work, so pack them
+  // onto the CTAs on the host.
+  if (plannable(s) && o_part == nullptr && withhold_first_load == 0)
+    apply_plan(s, p.num_units, grid, &p);
   const bool bf16 = dtype == ATTN_BF16;
   auto launch = [&]() {
     return dtype == ATTN_E4M3
@@ -906,6 +1054,38 @@ attn_status_t attn_dispatch(int B, int Hq, int Hkv, int Sq, int Skv, int D,
   d.name =
       kNames[s.D == 128][static_cast<int>(dtype)][mode][d.order][d.o_store];
   *out = d;
+  return ATTN_OK;
+}
+
+attn_status_t attn_unit_plan(int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                             int causal, int input_pos, int window, int grid,
+                             int* planned, long long* work_max,
+                             long long* work_rounds, int* unit_order,
+                             int* cta_start) {
+  if (planned == nullptr || work_max == nullptr || work_rounds == nullptr ||
+      grid < 1)
+    return ATTN_ERR_INVALID_ARG;
+  const Shape s{B, Hq, Hkv, Sq, Skv, D, causal != 0, input_pos, window};
+  const attn_status_t st = check_scalars(s, 1.0f, ATTN_BF16);
+  if (st != ATTN_OK) return st;
+  const long long units = grid_size(s);
+  const int g = static_cast<int>(std::min<long long>(units, grid));
+  UnitPlan* plan = new UnitPlan;
+  const bool ok = units > 0 && units <= 0x7fffffffLL &&
+                  make_plan(s, static_cast<int>(units), g, plan);
+  *planned = ok ? 1 : 0;
+  if (ok) {
+    *work_max = plan->work_max;
+    *work_rounds = plan->work_rounds;
+    if (unit_order != nullptr)
+      for (int i = 0; i < plan->units; ++i) unit_order[i] = plan->unit[i];
+    if (cta_start != nullptr)
+      for (int c = 0; c <= g; ++c) cta_start[c] = plan->start[c];
+  } else {
+    // The rounds: busiest CTA of the zigzag order (when the plan had a say).
+    *work_max = *work_rounds = plan->work_rounds;
+  }
+  delete plan;
   return ATTN_OK;
 }
 

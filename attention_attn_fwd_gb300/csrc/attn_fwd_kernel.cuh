@@ -47,6 +47,10 @@
 
 namespace attn {
 
+// Largest planned unit assignment (it travels in the kernel parameters).
+constexpr int kMaxPlanUnits = 1024;
+constexpr int kMaxPlanCtas = 160;
+
 struct FwdParams {
   int B, Hq, Hkv, Sq, Skv;
   int causal;
@@ -92,6 +96,13 @@ struct FwdParams {
   // m-block (B*Hq/2 paired, else B*Hq), heads per batch entry (Hq/2 paired,
   // else Hq), group, and Hkv (packed units).
   FastDiv fd_splits, fd_m_blocks, fd_per_m, fd_heads, fd_group, fd_hkv;
+  // Planned unit assignment (plan_units > 0; two-tile one-pass launches of
+  // at most kMaxPlanUnits units whose work differs): CTA c walks units
+  // plan_unit[plan_start[c] .. plan_start[c + 1]) in that order.  Otherwise
+  // the zigzag rounds of unit_index.
+  int plan_units;
+  unsigned short plan_start[kMaxPlanCtas + 1];
+  unsigned short plan_unit[kMaxPlanUnits];
   unsigned int* status;    // device status word (timeouts)
   unsigned long long timeout_ns;
   // Self-test of the bounded waits (0 in every normal launch): CTA 0's
@@ -441,12 +452,24 @@ __device__ __forceinline__ void merge_tile_cluster(const FwdParams& p,
   }
 }
 
-// k-th unit of CTA `cta` among `ctas`: rounds of `ctas` units, the CTA order
-// reversed every other round.  With units sorted heaviest first this keeps
-// the per-CTA totals within a few percent of the mean for causal masks
-// (plain round-robin gives every CTA's first pick of each round to CTA 0).
-__device__ __forceinline__ int unit_index(int k, int cta, int ctas) {
+// k-th unit of CTA `cta` among `ctas`: from the launch's plan, or rounds of
+// `ctas` units with the CTA order reversed every other round.  With units
+// sorted heaviest first the rounds keep the per-CTA totals within a few
+// percent of the mean for causal masks (plain round-robin gives every
+// CTA's first pick of each round to CTA 0); the plan, packed on the host,
+// within a fraction of a percent.
+__device__ __forceinline__ int unit_index(const FwdParams& p, int k, int cta,
+                                          int ctas) {
+  if (p.plan_units > 0) return p.plan_unit[p.plan_start[cta] + k];
   return k * ctas + ((k & 1) ? (ctas - 1 - cta) : cta);
+}
+
+// Units CTA `cta` walks (the loop bound of every role; under the zigzag
+// rounds the last round's index may lie past num_units and is skipped).
+__device__ __forceinline__ int units_of_cta(const FwdParams& p, int cta,
+                                            int ctas) {
+  if (p.plan_units > 0) return p.plan_start[cta + 1] - p.plan_start[cta];
+  return (p.num_units + ctas - 1) / ctas;
 }
 
 // Persistent kernel: one CTA per SM walks its units (unit_index) in
@@ -508,6 +531,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
   constexpr int nslots = L::kSlots;
   const int u_first = static_cast<int>(blockIdx.x);
   const int u_step = static_cast<int>(gridDim.x);
+  const int k_end = units_of_cta(p, u_first, u_step);  // units of this CTA
 
   if constexpr (kPack) {
     // A packed Q load fills only group*Sq rows of the tile: keep the other
@@ -549,8 +573,8 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
     int it = 0;               // ring items (K_0, V_0, K_1, ...) issued so far
     int q_loads[2] = {0, 0};  // Q tile loads issued so far, per tile
     const bool withhold = p.withhold_first_load != 0 && blockIdx.x == 0;
-    for (int k = 0; k * u_step < p.num_units && ok; ++k) {
-      const int u = unit_index(k, u_first, u_step);
+    for (int k = 0; k < k_end && ok; ++k) {
+      const int u = unit_index(p, k, u_first, u_step);
       if (u >= p.num_units) continue;
       const Unit w = decode_unit<kPack, kWindow>(p, u);
 #pragma unroll
@@ -659,8 +683,8 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
     int q_uses[2] = {0, 0};   // Q tile loads consumed, per tile
     int p_waits[2] = {0, 0};  // P-ready phases consumed, per tile
     int s_issued = 0;         // kTriple: S MMAs issued (buffer = count % 3)
-    for (int k = 0; k * u_step < p.num_units && ok; ++k) {
-      const int u = unit_index(k, u_first, u_step);
+    for (int k = 0; k < k_end && ok; ++k) {
+      const int u = unit_index(p, k, u_first, u_step);
       if (u >= p.num_units) continue;
       const Unit w = decode_unit<kPack, kWindow>(p, u);
       // A key range wholly past the causal horizon of both tiles has no
@@ -909,8 +933,8 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
     int s_before = 0;           // kTriple: S MMAs of this CTA's earlier units
     int s_uses[3] = {0, 0, 0};  // kTriple: this tile's uses of each buffer
 
-    for (int k = 0; k * u_step < p.num_units && ok; ++k) {
-      const int u = unit_index(k, u_first, u_step);
+    for (int k = 0; k < k_end && ok; ++k) {
+      const int u = unit_index(p, k, u_first, u_step);
       if (u >= p.num_units) continue;
       const Unit w = decode_unit<kPack, kWindow>(p, u);
       const int n = t ? w.n[1] : w.n[0];

@@ -386,6 +386,37 @@ attn_status_t attn_dispatch(int B, int Hq, int Hkv, int Sq, int Skv, int D,
                             attn_dtype_t dtype, int num_splits,
                             attn_dispatch_t* out);
 
+/*
+ * attn_unit_plan — how a one-pass forward call of this shape assigns its
+ * work units to `grid` persistent CTAs (host only, no GPU needed; the call
+ * itself uses grid = min(units, SM count)).  Has no counterpart in the
+ * method's description: it exposes the launch's load balancing.
+ * Causal two-tile launches (not the packed few-row mode) of more units
+ * than CTAs and at most 1024 units are packed on the host: units heaviest
+ * first into the first CTA with room under a capacity searched from the
+ * mean upwards (first-fit decreasing, the MULTIFIT method), kept only when
+ * its busiest CTA beats the zigzag rounds the kernel otherwise walks.
+ *   planned      out: 1 when such a plan assigns the units, else 0 (the
+ *                rounds: non-causal or packed launches, units <= grid,
+ *                more than 1024 units, or no better plan);
+ *   work_max     out: the busiest CTA's work under the assignment the
+ *                call uses, in half K/V steps (each unit counts 2 per K/V
+ *                step its later Q tile visits, plus 3 for its boundary);
+ *                0 when not computed (a launch the plan never considers);
+ *   work_rounds  out: the same under the zigzag rounds (0 likewise);
+ *   unit_order   optional (NULL: not written), room for the unit count:
+ *                CTA c walks units unit_order[cta_start[c] ..
+ *                cta_start[c + 1]) in order (written only when planned);
+ *   cta_start    optional, room for min(units, grid) + 1 entries.
+ * Returns the validation code of attn_fwd for the shape (bf16), or
+ * ATTN_ERR_INVALID_ARG for grid < 1 or a NULL output.
+ */
+attn_status_t attn_unit_plan(int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                             int causal, int input_pos, int window, int grid,
+                             int* planned, long long* work_max,
+                             long long* work_rounds, int* unit_order,
+                             int* cta_start);
+
 /* Library version as major*10000 + minor*100 + patch. */
 int attn_version(void);
 

@@ -97,6 +97,42 @@ def test_full_size_sweep(w):
     check_sampled(w, seed=1, n_rows=96)
 
 
+# Causal launches whose units the host packs onto the CTAs (attn_unit_plan):
+# every element against the oracle on two that are small enough, and on the
+# full-size ones every row written (the plan must give each unit to one CTA).
+PLANNED = [
+    W("planned_group5_batch2", 2, 20, 4, 1800, 1800, 128, "bf16", True),
+    W("planned_offset_d64", 1, 32, 8, 2560, 3000, 64, "f16", True, 400),
+]
+
+
+def planned(w):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return attn.attn_unit_plan(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.causal,
+                               w.input_pos, grid=sms)["planned"] == 1
+
+
+@pytest.mark.parametrize("w", PLANNED, ids=lambda w: w.name)
+def test_planned_launches(w):
+    assert planned(w)
+    check_full(w, seed=9)
+
+
+@pytest.mark.parametrize("w", [MHA_4K, GQA_8K, PREFILL_CHUNK],
+                         ids=lambda w: w.name)
+def test_planned_full_size_writes_every_row(w):
+    assert planned(w)
+    q, k, v = (t.cuda() for t in make_qkv(w, seed=10))
+    o = torch.full(q.shape, float("nan"), dtype=w.out_dtype, device="cuda")
+    lse = torch.full((w.B, w.Hq, w.Sq), float("nan"), dtype=torch.float32,
+                     device="cuda")
+    attn.fwd(q, k, v, scale=w.scale, causal=w.causal, input_pos=w.input_pos,
+             out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert attn.attn_device_status() == (0, 0)
+    assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(lse).all())
+
+
 def test_bitwise_reproducible():
     w = W("repro", 1, 8, 2, 1000, 1000, 128, "bf16", True, 0)
     q, k, v = make_qkv(w, 6)
