@@ -21,6 +21,7 @@ SOURCES = ["attn_api.cu", "attn_fwd_d64.cu", "attn_fwd_d128.cu",
            "attn_fwd_d128_fp8.cu", "attn_fwd_d128_fp8_packed.cu",
            "attn_noalloc.cu", "attn_bwd.cu"]
 HEADERS = ["attn_fwd_kernel.cuh", "attn_fwd_launch.cuh", "attn_sync.cuh",
+           "fast_div.h",
            "attn_bwd_kernel.cuh",
            "sm103_ptx.cuh", "attn_launch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
