@@ -88,6 +88,16 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar,
 }
 
 // ------------------------------------------------------------------ TMA
+// 3-D tiled prefetch global -> L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* m, int c0,
+                                                int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::
+          "l"(reinterpret_cast<uint64_t>(m)),
+      "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m))
                : "memory");
