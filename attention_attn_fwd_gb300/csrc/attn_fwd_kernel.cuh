@@ -168,11 +168,12 @@ struct Layout {
   static constexpr int kBarOff = kStageOff + 2 * kStageTileBytes;
   // barriers: q_full[2], full[S], empty[S], s_full[6] (two S regions, or
   // three shared S buffers with one barrier per tile and buffer),
-  // p_full[2], o_full[2], drain[1], q_free[2], pv_done[2]
-  static constexpr int kNumBars = 2 + 2 * kSlots + 6 + 2 + 2 + 1 + 2 + 2;
-  // misc: TMEM base, abort flag, per-tile "merge here" flags
+  // p_full[2], o_full[2], drain[1], q_free[2], pv_done[2], epi[2]
+  static constexpr int kNumBars = 2 + 2 * kSlots + 6 + 2 + 2 + 1 + 2 + 2 + 2;
+  // misc: TMEM base, abort flag, per-tile "merge here" flags, per-tile
+  // epilogue "saw O complete" flags (4 bytes per warp)
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
-  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kBytes = kMiscOff + 16 + 32;
   static constexpr int kSmemBytes = kBytes + 1024;  // slack for 1 KB alignment
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 };
@@ -523,6 +524,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
   const uint32_t bar_drain = bar_o + 8 * 2;            // [1]
   const uint32_t bar_qfree = bar_drain + 8;            // [2]
   const uint32_t bar_pvdone = bar_qfree + 8 * 2;       // [2] every PV but a unit's last
+  const uint32_t bar_epi = bar_pvdone + 8 * 2;         // [2] epilogue entry, all warps
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<int*>(smem + L::kMiscOff + 4);
 
@@ -567,11 +569,14 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
     }
   }
   if (threadIdx.x == 0) {
-    // P-ready barriers collect one arrival per softmax thread; the others
-    // one arrival (an expect-tx, a tcgen05.commit).
+    // P-ready and epilogue-entry barriers collect one arrival per softmax
+    // thread of the tile; the others one arrival (an expect-tx, a
+    // tcgen05.commit).
     for (int i = 0; i < L::kNumBars; ++i) {
       const uint32_t bar = bar0 + 8 * i;
-      ptx::mbar_init(bar, (bar == bar_p || bar == bar_p + 8) ? kTM : 1);
+      const bool per_thread = bar == bar_p || bar == bar_p + 8 ||
+                              bar == bar_epi || bar == bar_epi + 8;
+      ptx::mbar_init(bar, per_thread ? kTM : 1);
     }
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -1221,6 +1226,24 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
       // this warpgroup's next P, so the reads below come first.
       ok = __all_sync(0xffffffffu, wait_bounded(bar_o + 8 * t, o_waits & 1,
                                                 abort_flag, p, 4));
+      if (kStageO || (kSplit && !(kPack && p.cluster_merge))) {
+        // The epilogue below meets at named barriers, which do not time out.
+        // After an abort the tile's warps may have left the step loop at
+        // different waits (a phase that completed for one had already been
+        // given up by another), so they first meet on a bounded barrier and
+        // go on only if all four came and all saw O complete; a warp that
+        // never comes lets the others' wait run out.  With the staged store
+        // this barrier is also the first box's "buffer free" signal: the
+        // storing thread arrives once TMA has read the previous box out.
+        volatile int* in_ok = reinterpret_cast<volatile int*>(
+            smem + L::kMiscOff + 16 + 16 * t);
+        if (lane == 0) in_ok[warp % 4] = ok ? 1 : 0;
+        if (kStageO && r == 0) ptx::bulk_wait_group_read_all();
+        ptx::mbar_arrive(bar_epi + 8 * t);
+        ok = __all_sync(0xffffffffu, wait_bounded(bar_epi + 8 * t, o_waits & 1,
+                                                  abort_flag, p, 4));
+        ok = ok && in_ok[0] && in_ok[1] && in_ok[2] && in_ok[3];
+      }
       if (!ok) break;
       ++o_waits;
       ptx::tc_fence_after();
@@ -1247,9 +1270,12 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
           ptx::tmem_ld32(t_o + 64 * h, o);
           ptx::tmem_ld32(t_o + 64 * h + 32, o + 32);
           ptx::tmem_wait_ld();
-          // The buffer is free once TMA has read the previous box out of it.
-          if (r == 0) ptx::bulk_wait_group_read_all();
-          ptx::named_barrier_sync(1 + t, kTM);
+          // The buffer is free once TMA has read the previous box out of it
+          // (for the first box: the entry barrier above).
+          if (h > 0) {
+            if (r == 0) ptx::bulk_wait_group_read_all();
+            ptx::named_barrier_sync(1 + t, kTM);
+          }
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             uint32_t wv[4];
