@@ -1030,18 +1030,32 @@ attn_status_t attn_dispatch(int B, int Hq, int Hkv, int Sq, int Skv, int D,
   d.s_buffers = (!pack && s.D == 64) ? 3 : 2;
   d.stages = t.stages;
   d.order = (!pack && head_major(s)) ? 1 : 0;
+  if (!split && plannable(s)) {
+    // The launch assigns causal units by a host-packed plan when one beats
+    // the zigzag rounds; the grid is the current device's SM count (the
+    // GB300's 152 without a device).
+    int dev = -1, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) sms = num_sms(dev);
+    cudaGetLastError();  // no device: not an error of the caller's
+    if (sms <= 0) sms = 152;
+    const int units = static_cast<int>(grid_size(s));
+    UnitPlan* plan = new UnitPlan;
+    if (make_plan(s, units, std::min(units, sms), plan)) d.order = 2;
+    delete plan;
+  }
   d.o_store = (!pack && !split) ? 1 : 0;
   d.hold_scores = pack ? 0 : 1;
   d.num_splits = split ? splits : 0;
   d.units = static_cast<int>(grid_size(s) * splits);
   d.smem_bytes = t.smem_bytes;
   // Static names: D x element type x tile mode x order x O store.
-  static const char* const kNames[2][3][3][2][2] = {
+  static const char* const kNames[2][3][3][3][2] = {
 #define ATTN_N(d, e, m, o, st) "d" d "." e "." m "." o "." st
 #define ATTN_O(d, e, m)                                          \
   {{ATTN_N(d, e, m, "lpt", "rows"), ATTN_N(d, e, m, "lpt", "tma")}, \
    {ATTN_N(d, e, m, "head-major", "rows"),                       \
-    ATTN_N(d, e, m, "head-major", "tma")}}
+    ATTN_N(d, e, m, "head-major", "tma")},                       \
+   {ATTN_N(d, e, m, "plan", "rows"), ATTN_N(d, e, m, "plan", "tma")}}
 #define ATTN_M(d, e)                                                \
   {ATTN_O(d, e, "paired-heads"), ATTN_O(d, e, "256-rows"),           \
    ATTN_O(d, e, "gqa-packed")}

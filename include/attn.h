@@ -362,7 +362,12 @@ attn_status_t attn_tile_config(int B, int Hq, int Hkv, int Sq, int Skv, int D,
  *                         row block in turn (longest-processing-time order
  *                         over the persistent CTAs); order 1: the row blocks
  *                         of one head in turn (non-causal: equal units, K/V
- *                         of the few heads in flight stays in L2);
+ *                         of the few heads in flight stays in L2); order 2:
+ *                         causal units assigned to the CTAs by a plan packed
+ *                         on the host (one-pass launches of more units than
+ *                         SMs and at most 1024, when the plan beats the
+ *                         order-0 rounds; see attn_unit_plan), so the entry
+ *                         depends on Sq through the unit count;
  *   o_store 1             O leaves through a 128-byte-swizzled shared-memory
  *                         box stored by TMA; 0: each softmax thread stores
  *                         its row (packed tiles, split-KV fp32 partials);

@@ -252,11 +252,19 @@ def test_dispatch_entries_host_only(lib):
     count; bad arguments get the validation code attn_fwd would return."""
     bf, f16, e4 = attn.ATTN_BF16, attn.ATTN_F16, attn.ATTN_E4M3
     e = attn.attn_dispatch(1, 32, 4, 8192, 8192, 128, 1, 0, bf)
-    assert e["name"] == "d128.bf16.paired-heads.lpt.tma"
+    assert e["name"] == "d128.bf16.paired-heads.plan.tma"
     assert (e["q_tiles"], e["paired"], e["s_buffers"], e["order"],
             e["o_store"], e["hold_scores"], e["num_splits"]) == \
-        (2, 1, 2, 0, 1, 1, 0)
+        (2, 1, 2, 2, 1, 1, 0)
     assert e["units"] == 32 // 2 * 8192 // 128
+    # The plan's unit bound makes the causal entry depend on Sq: 2048
+    # units at 16k keep the LPT rounds, as do fewer units than SMs.
+    e = attn.attn_dispatch(1, 32, 4, 16384, 16384, 128, 1, 0, bf)
+    assert e["name"] == "d128.bf16.paired-heads.lpt.tma" and e["order"] == 0
+    e = attn.attn_dispatch(1, 32, 4, 1024, 1024, 128, 1, 0, bf)
+    assert e["order"] == 0 and e["units"] == 128
+    e = attn.attn_dispatch(1, 32, 32, 4096, 4096, 128, 1, 0, f16)
+    assert e["name"] == "d128.f16.256-rows.plan.tma"
     e = attn.attn_dispatch(4, 16, 16, 1024, 1024, 64, 0, 0, f16)
     assert e["name"] == "d64.f16.256-rows.head-major.tma"
     assert e["s_buffers"] == 3 and e["units"] == 4 * 16 * 4
@@ -265,7 +273,7 @@ def test_dispatch_entries_host_only(lib):
     assert e["q_tiles"] == 1 and e["num_splits"] == 2
     assert e["units"] == 8 * 8 * 2 and e["block_m"] == 4
     e = attn.attn_dispatch(1, 32, 4, 8192, 8192, 128, 1, 0, e4)
-    assert e["name"] == "d128.e4m3.paired-heads.lpt.tma"
+    assert e["name"] == "d128.e4m3.paired-heads.plan.tma"
     # window entry: causal, LPT order
     e = attn.attn_dispatch(1, 32, 4, 32768, 32768, 128, 1, 0, bf,
                            window=4096)

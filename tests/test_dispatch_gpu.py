@@ -53,7 +53,8 @@ def entry(w):
 
 
 def test_cases_cover_the_table():
-    """Host only: the shapes above reach every 16-bit one-pass entry."""
+    """Host only: the shapes above reach every 16-bit one-pass entry but
+    the plan entries (test_plan_entries_named)."""
     names = {entry(w)["name"] for w in CASES}
     want = set()
     for D, dt in itertools.product(("64", "128"), ("f16", "bf16")):
@@ -62,6 +63,18 @@ def test_cases_cover_the_table():
                 want.add("d%s.%s.%s.%s.tma" % (D, dt, mode, order))
         want.add("d%s.%s.gqa-packed.lpt.rows" % (D, dt))
     assert names == want, sorted(want - names)
+
+
+def test_plan_entries_named():
+    """Host only: causal one-pass launches of more units than SMs (and at
+    most 1024) run the plan entries, one per tile mode and D among the
+    planned launches whose every element test_parity_gpu.py compares with
+    the oracle (the plan decision uses 152 SMs without a device)."""
+    from tests.test_parity_gpu import PLANNED
+    names = {entry(w)["name"] for w in PLANNED}
+    want = {"d128.bf16.256-rows.plan.tma", "d64.f16.paired-heads.plan.tma",
+            "d64.bf16.256-rows.plan.tma", "d128.f16.paired-heads.plan.tma"}
+    assert names == want
 
 
 @pytest.mark.gpu

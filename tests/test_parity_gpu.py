@@ -103,6 +103,9 @@ def test_full_size_sweep(w):
 PLANNED = [
     W("planned_group5_batch2", 2, 20, 4, 1800, 1800, 128, "bf16", True),
     W("planned_offset_d64", 1, 32, 8, 2560, 3000, 64, "f16", True, 400),
+    # the other two (tile mode, D) pairs of the plan entries
+    W("planned_group5_d64", 4, 20, 4, 1024, 1024, 64, "bf16", True),
+    W("planned_paired_d128", 4, 16, 4, 1280, 1280, 128, "f16", True),
 ]
 
 
