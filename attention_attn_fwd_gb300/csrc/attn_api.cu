@@ -795,11 +795,12 @@ attn_status_t bwd_impl(const Shape& s, const void* Q, const void* K,
 
   const long long q_planes = static_cast<long long>(s.B) * s.Hq;
   const long long kv_planes = static_cast<long long>(s.B) * s.Hkv;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   if (!make_map(&tq, Q, dtype, s.D, s.Sq, q_planes) ||
       !make_map(&tk, K, dtype, s.D, s.Skv, kv_planes) ||
       !make_map(&tv, V, dtype, s.D, s.Skv, kv_planes) ||
-      !make_map(&tdo, dO, dtype, s.D, s.Sq, q_planes))
+      !make_map(&tdo, dO, dtype, s.D, s.Sq, q_planes) ||
+      !make_map(&tdq, dQ, dtype, s.D, s.Sq, q_planes))
     return ATTN_ERR_CUDA;
   const size_t rows = static_cast<size_t>(s.B) * s.Hq * bwd_sq_pad(s);
   float* lse2 = static_cast<float*>(workspace);
@@ -829,7 +830,7 @@ attn_status_t bwd_impl(const Shape& s, const void* Q, const void* K,
   p.status = status;
   p.timeout_ns = timeout_ns();
   const cudaError_t err = attn::launch_bwd(s.D, dtype == ATTN_BF16, tq, tk,
-                                           tv, tdo, O, dO, LSE, p, cs);
+                                           tv, tdo, tdq, O, dO, LSE, p, cs);
   return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -71,24 +71,22 @@ cudaError_t set_smem(Kernel kernel, int smem, int* configured,
   return cudaSuccess;
 }
 
-template <class Kernel>
+template <class Kernel, class... Args>
 cudaError_t launch(Kernel kernel, int smem, int grid, cudaStream_t stream,
-                   const CUtensorMap& q, const CUtensorMap& k,
-                   const CUtensorMap& v, const CUtensorMap& d,
-                   const BwdParams& p) {
+                   const Args&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(bwd::kThreads, 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, kernel, q, k, v, d, p);
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 template <int D, bool kBF16>
 cudaError_t run(const CUtensorMap& q, const CUtensorMap& k,
-                const CUtensorMap& v, const CUtensorMap& d, const void* O,
-                const void* dO, const float* LSE, const BwdParams& p,
-                cudaStream_t stream) {
+                const CUtensorMap& v, const CUtensorMap& d,
+                const CUtensorMap& dqm, const void* O, const void* dO,
+                const float* LSE, const BwdParams& p, cudaStream_t stream) {
   static thread_local int cfg_dkdv = -1, cfg_dq = -1;
   const long long planes = static_cast<long long>(p.B) * p.Hq;
   const long long rows = planes * p.Sq;
@@ -124,7 +122,7 @@ cudaError_t run(const CUtensorMap& q, const CUtensorMap& k,
   err = launch(dkdv, smem_kv, p.B * p.Hkv * p.k_tiles, stream, q, k, v, d, p);
   if (err != cudaSuccess) return err;
   err = launch(dq, smem_q, p.B * p.Hq * p.q_tiles, side->stream, q, k, v, d,
-               p);
+               dqm, p);
   if (err != cudaSuccess) return err;
   err = cudaEventRecord(side->join, side->stream);
   if (err != cudaSuccess) return err;
@@ -135,14 +133,14 @@ cudaError_t run(const CUtensorMap& q, const CUtensorMap& k,
 
 cudaError_t launch_bwd(int D, bool bf16, const CUtensorMap& q,
                        const CUtensorMap& k, const CUtensorMap& v,
-                       const CUtensorMap& d, const void* O, const void* dO,
-                       const float* LSE, const BwdParams& p,
-                       cudaStream_t stream) {
+                       const CUtensorMap& d, const CUtensorMap& dq,
+                       const void* O, const void* dO, const float* LSE,
+                       const BwdParams& p, cudaStream_t stream) {
   if (D == 64)
-    return bf16 ? run<64, true>(q, k, v, d, O, dO, LSE, p, stream)
-                : run<64, false>(q, k, v, d, O, dO, LSE, p, stream);
-  return bf16 ? run<128, true>(q, k, v, d, O, dO, LSE, p, stream)
-              : run<128, false>(q, k, v, d, O, dO, LSE, p, stream);
+    return bf16 ? run<64, true>(q, k, v, d, dq, O, dO, LSE, p, stream)
+                : run<64, false>(q, k, v, d, dq, O, dO, LSE, p, stream);
+  return bf16 ? run<128, true>(q, k, v, d, dq, O, dO, LSE, p, stream)
+              : run<128, false>(q, k, v, d, dq, O, dO, LSE, p, stream);
 }
 
 }  // namespace attn

@@ -295,8 +295,8 @@ struct DqLayout : BwdTiles<D> {
   static constexpr int kVOff = kKOff + kKSlots * T::kTileBytes;
   static constexpr int kBarOff = kVOff + kVSlots * T::kTileBytes;
   // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_ready[2],
-  // dp_ready, ds_ready, acc_done, drain
-  static constexpr int kNumBars = 1 + 2 * kKSlots + 2 * kVSlots + 6;
+  // dp_ready, ds_ready, acc_done, drain, box_full[2] (dQ output boxes)
+  static constexpr int kNumBars = 1 + 2 * kKSlots + 2 * kVSlots + 6 + 2;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -816,6 +816,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_do,
+                       const __grid_constant__ CUtensorMap tm_dq,
                        const BwdParams p) {
   using L = DqLayout<D>;
   using namespace bwd;
@@ -838,6 +839,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
   const uint32_t bar_ds = bar_dp + 8;
   const uint32_t bar_acc = bar_ds + 8;
   const uint32_t bar_drain = bar_acc + 8;
+  const uint32_t bar_box = bar_drain + 8;  // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<int*>(smem + L::kMiscOff + 4);
 
@@ -849,9 +851,15 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
   const int kvplane = (qplane / p.Hq) * p.Hkv + (qplane % p.Hq) / p.group;
 
   if (threadIdx.x == 0) {
+    // dQ box b collects one arrival per thread that writes into it: both
+    // halves at D = 64 (one 64-column box), one half each at D = 128.
     for (int i = 0; i < L::kNumBars; ++i) {
       const uint32_t bar = bar0 + 8 * i;
-      ptx::mbar_init(bar, bar == bar_ds ? kWork : 1);
+      const uint32_t count = bar == bar_ds                ? kWork
+                             : bar == bar_box && D == 64 ? kWork
+                             : (bar == bar_box || bar == bar_box + 8) ? kT
+                                                                      : 1;
+      ptx::mbar_init(bar, count);
     }
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -874,6 +882,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       ptx::prefetch_tensormap(&tm_k);
       ptx::prefetch_tensormap(&tm_v);
       ptx::prefetch_tensormap(&tm_do);
+      ptx::prefetch_tensormap(&tm_dq);
     }
     ptx::mbar_arrive_expect_tx_elect(bar_q, 2 * L::kTileBytes);
     for (int c = 0; c < L::kChunks; ++c) {
@@ -1045,8 +1054,6 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const uint32_t t_dp = tmem + lane_off + 2 * kT;
     const int q_row = m * kT + r;
-    const bool row_ok = q_row < p.Sq;
-    const long long grow = static_cast<long long>(qplane) * p.Sq + q_row;
     const long long vrow = static_cast<long long>(qplane) * p.sq_pad + q_row;
     const float lse2 = p.lse2[vrow];  // +inf past Sq: P = 0
     const float dlt = p.delta[vrow];
@@ -1132,11 +1139,49 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     if (ok && s > 0) {
       ok = __all_sync(0xffffffffu, wait_bounded(bar_acc, 0, abort_flag, p, 4));
       if (ok) {
-        // Half h writes columns [h*D/2, (h+1)*D/2) of the scale * dQ row.
+        // scale * dQ in 16 bits through 128-row x 128-byte boxes in shared
+        // memory (the K ring, idle now: every MMA has completed), stored by
+        // TMA (rows >= Sq fall outside the tensor).  Half h writes columns
+        // [h*D/2, (h+1)*D/2) of its row: at D = 128 one box per half, at
+        // D = 64 half of one box each; chunk c of row r sits at c ^ (r % 8).
+        // The storing thread waits (bounded) for every writer of its box;
+        // nobody else waits, so an abort cannot strand a warp here.
         ptx::tc_fence_after();
-        store_cols<D / 2, kBF16>(
-            tmem + lane_off + 3 * kT + h * (D / 2), p.scale,
-            static_cast<uint16_t*>(p.dq) + grow * D + h * (D / 2), row_ok);
+        constexpr int kCols = D / 2;
+        const int box = D == 64 ? 0 : h;
+        const int chunk0 = D == 64 ? 4 * h : 0;
+        const uint32_t row_base = s_kr + box * kT * 128 + r * 128;
+        const uint32_t swz = r % 8;
+#pragma unroll
+        for (int q = 0; q < kCols / 32; ++q) {
+          uint32_t a[32];
+          ptx::tmem_ld32(tmem + lane_off + 3 * kT + h * kCols + 32 * q, a);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8) {
+            uint32_t wv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              wv[e] = ptx::pack2<kBF16>(
+                  __uint_as_float(a[8 * c8 + 2 * e]) * p.scale,
+                  __uint_as_float(a[8 * c8 + 2 * e + 1]) * p.scale);
+            ptx::st_shared_v4(row_base + (((chunk0 + 4 * q + c8) ^ swz) << 4),
+                              wv[0], wv[1], wv[2], wv[3]);
+          }
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(bar_box + 8 * box);
+        if (warp == kWorkWarp0 + 4 * box && (D == 128 || h == 0)) {
+          const bool all_in = __all_sync(
+              0xffffffffu,
+              wait_bounded(bar_box + 8 * box, 0, abort_flag, p, 4));
+          if (all_in && lane == 0) {
+            ptx::tma_store_3d(&tm_dq, s_kr + box * kT * 128, 64 * box,
+                              m * kT, qplane);
+            ptx::bulk_commit_group();
+            ptx::bulk_wait_group_all();
+          }
+        }
       }
     }
   }

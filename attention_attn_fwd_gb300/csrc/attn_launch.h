@@ -49,13 +49,13 @@ cudaError_t launch_fwd_d128_fp8_packed(const CUtensorMap& q,
                                        cudaStream_t stream);
 
 // Backward pass: row pass (D, lse2 into p.lse2 / p.delta), dK/dV kernel,
-// dQ kernel, in that order on `stream` (attn_bwd.cu).  `d` maps dO like `q`
-// maps Q.
+// dQ kernel, in that order on `stream` (attn_bwd.cu).  `d` maps dO and `dq`
+// maps dQ like `q` maps Q (dQ is stored through it by TMA).
 struct BwdParams;
 cudaError_t launch_bwd(int D, bool bf16, const CUtensorMap& q,
                        const CUtensorMap& k, const CUtensorMap& v,
-                       const CUtensorMap& d, const void* O, const void* dO,
-                       const float* LSE, const BwdParams& p,
-                       cudaStream_t stream);
+                       const CUtensorMap& d, const CUtensorMap& dq,
+                       const void* O, const void* dO, const float* LSE,
+                       const BwdParams& p, cudaStream_t stream);
 
 }  // namespace attn
