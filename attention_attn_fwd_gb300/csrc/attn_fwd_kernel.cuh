@@ -334,57 +334,98 @@ __device__ __forceinline__ bool merge_arrive(unsigned long long* ctr,
 // output O_c and log-sum-exp lse_c; with M = max_c lse_c and
 // w_c = e^(lse_c - M),  O = sum_c w_c O_c / sum_c w_c  and
 // LSE = M + ln(sum_c w_c) -- the online-softmax rescale applied once more,
-// across ranges.  Ranges past a row's causal horizon or before its window
-// hold nothing for it and are not read.  Thread tid takes 4 columns of one row, so the 32 (or
-// 16) threads of a row read its partials as contiguous 512 (256) bytes.
+// across ranges, here in its online form (a running maximum, the sums
+// rescaled when it grows).  Ranges past a row's causal horizon or before
+// its window hold nothing for it and are not read.  Thread tid takes 4
+// columns of a row (the 32 or 16 threads of a row read its partials as
+// contiguous 512 or 256 bytes) and kRowBatch rows at once, whose loads of
+// one range are all in flight together: the merge is bound by L2 latency,
+// and one row at a time kept too few loads in flight.
 template <int D, bool kBF16, bool kPack, bool kWindow>
 __device__ __forceinline__ void merge_tile(const FwdParams& p, int plane0,
                                            int m0, int tid) {
   constexpr float kLog2e = 1.4426950408889634f;
   constexpr int kGroups = D / 4;               // 4-column groups per row
   constexpr int kRowsPerPass = cfg::kTM / kGroups;
+  constexpr int kRowBatch = 4;                 // rows per thread in flight
   const long long rows = static_cast<long long>(p.B) * p.Hq * p.Sq;
   const int split_keys = p.split_tiles * cfg::kTN;
   const int nrows =
       kPack ? p.group * p.Sq : min(cfg::kTM, p.Sq - m0);
   const int cg = tid % kGroups;
-  for (int r = tid / kGroups; r < nrows; r += kRowsPerPass) {
-    int q_plane = plane0, q_row = m0 + r;
-    if constexpr (kPack) {
-      q_plane += r / p.Sq;
-      q_row = r % p.Sq;
+  for (int r0 = tid / kGroups; r0 < nrows; r0 += kRowsPerPass * kRowBatch) {
+    long long row[kRowBatch];
+    int c0[kRowBatch], ns[kRowBatch];
+    int cmin = p.num_splits, cmax = 0;
+#pragma unroll
+    for (int b = 0; b < kRowBatch; ++b) {
+      const int r = r0 + b * kRowsPerPass;
+      row[b] = 0;
+      c0[b] = 0;
+      ns[b] = 0;  // no range: the row is past the tile
+      if (r < nrows) {
+        int q_plane = plane0, q_row = m0 + r;
+        if constexpr (kPack) {
+          q_plane += r / p.Sq;
+          q_row = r % p.Sq;
+        }
+        row[b] = static_cast<long long>(q_plane) * p.Sq + q_row;
+        const int row_pos = p.input_pos + q_row;
+        const int vis_end = p.causal ? min(p.Skv, row_pos + 1) : p.Skv;
+        ns[b] = min(p.num_splits, (vis_end + split_keys - 1) / split_keys);
+        c0[b] = kWindow ? max(0, row_pos - p.window + 1) / split_keys : 0;
+        cmin = min(cmin, c0[b]);
+        cmax = max(cmax, ns[b]);
+      }
     }
-    const long long row = static_cast<long long>(q_plane) * p.Sq + q_row;
-    const int row_pos = p.input_pos + q_row;
-    const int vis_end = p.causal ? min(p.Skv, row_pos + 1) : p.Skv;
-    const int ns = min(p.num_splits, (vis_end + split_keys - 1) / split_keys);
-    const int c0 =
-        kWindow ? max(0, row_pos - p.window + 1) / split_keys : 0;
-    float mx = -INFINITY;
-    for (int c = c0; c < ns; ++c)
-      mx = fmaxf(mx, __ldcg(p.lse_part + c * rows + row));
-    float wsum = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int c = c0; c < ns; ++c) {
-      const float wc =
-          ptx::ex2((__ldcg(p.lse_part + c * rows + row) - mx) * kLog2e);
-      const float4 x = __ldcg(
-          reinterpret_cast<const float4*>(p.o_part + (c * rows + row) * D) +
-          cg);
-      wsum += wc;
-      acc.x += wc * x.x;
-      acc.y += wc * x.y;
-      acc.z += wc * x.z;
-      acc.w += wc * x.w;
+    float mx[kRowBatch], wsum[kRowBatch];
+    float4 acc[kRowBatch];
+#pragma unroll
+    for (int b = 0; b < kRowBatch; ++b) {
+      mx[b] = -INFINITY;
+      wsum[b] = 0.f;
+      acc[b] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    const float inv = ptx::rcp(wsum);
-    uint2 out;
-    out.x = ptx::pack2<kBF16>(acc.x * inv, acc.y * inv);
-    out.y = ptx::pack2<kBF16>(acc.z * inv, acc.w * inv);
-    reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.o) + row * D)[cg] = out;
-    if (cg == 0 && p.lse != nullptr)
-      p.lse[row] = mx + ptx::lg2(wsum) * cfg::kLn2;
+    for (int c = cmin; c < cmax; ++c) {
+      float lc[kRowBatch];
+      float4 xc[kRowBatch];
+#pragma unroll
+      for (int b = 0; b < kRowBatch; ++b) {
+        lc[b] = -INFINITY;
+        xc[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c >= c0[b] && c < ns[b]) {
+          lc[b] = __ldcg(p.lse_part + c * rows + row[b]);
+          xc[b] = __ldcg(reinterpret_cast<const float4*>(
+                             p.o_part + (c * rows + row[b]) * D) +
+                         cg);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kRowBatch; ++b) {
+        const float mn = fmaxf(mx[b], lc[b]);
+        if (mn == -INFINITY) continue;  // nothing seen yet
+        const float a = ptx::ex2((mx[b] - mn) * kLog2e);  // 0 while mx = -inf
+        const float wc = ptx::ex2((lc[b] - mn) * kLog2e);
+        wsum[b] = wsum[b] * a + wc;
+        acc[b].x = acc[b].x * a + wc * xc[b].x;
+        acc[b].y = acc[b].y * a + wc * xc[b].y;
+        acc[b].z = acc[b].z * a + wc * xc[b].z;
+        acc[b].w = acc[b].w * a + wc * xc[b].w;
+        mx[b] = mn;
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kRowBatch; ++b) {
+      if (ns[b] == 0) continue;
+      const float inv = ptx::rcp(wsum[b]);
+      uint2 out;
+      out.x = ptx::pack2<kBF16>(acc[b].x * inv, acc[b].y * inv);
+      out.y = ptx::pack2<kBF16>(acc[b].z * inv, acc[b].w * inv);
+      reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.o) + row[b] * D)[cg] =
+          out;
+      if (cg == 0 && p.lse != nullptr)
+        p.lse[row[b]] = mx[b] + ptx::lg2(wsum[b]) * cfg::kLn2;
+    }
   }
 }
 
