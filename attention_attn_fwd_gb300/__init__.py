@@ -57,7 +57,7 @@ class _Dispatch(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "block_m", "block_n", "q_tiles", "paired", "s_buffers", "stages",
         "order", "o_store", "hold_scores", "num_splits", "units",
-        "smem_bytes")] + [("name", ctypes.c_char_p)]
+        "smem_bytes", "merge")] + [("name", ctypes.c_char_p)]
 
 
 def library_path() -> str:

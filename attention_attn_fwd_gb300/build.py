@@ -19,7 +19,7 @@ LIB = os.path.join(OUT_DIR, "libattn_fwd_gb300.so")
 SOURCES = ["attn_api.cu", "attn_fwd_d64.cu", "attn_fwd_d128.cu",
            "attn_fwd_d64_packed.cu", "attn_fwd_d128_packed.cu",
            "attn_fwd_d128_fp8.cu", "attn_fwd_d128_fp8_packed.cu",
-           "attn_noalloc.cu", "attn_bwd.cu"]
+           "attn_noalloc.cu", "attn_bwd.cu", "attn_merge.cu"]
 HEADERS = ["attn_fwd_kernel.cuh", "attn_fwd_launch.cuh", "attn_sync.cuh",
            "fast_div.h",
            "attn_bwd_kernel.cuh",

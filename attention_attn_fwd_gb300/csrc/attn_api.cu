@@ -284,43 +284,46 @@ constexpr size_t kWorkspaceAlign = 256;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Bytes of the split-KV workspace: fp32 partial outputs, partial LSEs,
-// then one 64-bit merge counter per (row block, Q tile).
+// Bytes of the split-KV workspace: fp32 partial outputs, then partial
+// LSEs.
 size_t splitkv_bytes(const Shape& s, int splits) {
   const size_t rows = static_cast<size_t>(s.B) * s.Hq * s.Sq;
   return round_up(static_cast<size_t>(splits) * rows * s.D * 4, kWorkspaceAlign) +
-         round_up(static_cast<size_t>(splits) * rows * 4, kWorkspaceAlign) +
-         round_up(static_cast<size_t>(grid_size(s)) * 2 * 8, kWorkspaceAlign);
+         round_up(static_cast<size_t>(splits) * rows * 4, kWorkspaceAlign);
 }
 
-// Tag of one split-KV call: marks its merge-counter arrivals, so counters
-// left by earlier calls in a reused workspace are recognised as stale.
-unsigned int next_merge_seq() {
-  static std::atomic<unsigned int> seq{0};
-  unsigned int v = ++seq;
-  if (v == 0) v = ++seq;  // skip 0 on wrap-around
-  return v;
-}
-
-// Split count and K/V tiles per split.  `splits` <= 0 picks enough splits
-// to give every SM a unit (at most kMaxSplits, at least one tile each).
-void splitkv_shape(const Shape& s, int splits, int sms, int* out_splits,
-                   int* out_tiles) {
+// Split count and K/V tiles per split.  `splits` <= 0 picks the count
+// with the shortest estimated time, in half steps of one CTA (a step: one
+// 128-key K/V tile for the unit's Q tiles, about 1.4 us with D = 128):
+// waves of units over the SMs times (tiles per range + a fixed cost per
+// unit), plus the merge launch, and never less than streaming every K/V
+// byte once from HBM (about 7 MB per step of time).  Fixed costs, fitted to
+// GB300 timings of one pass and of 2-32 ranges over seven shapes (B1-8,
+// 8-32 query heads, 1-1024 query rows, 4k-128k keys): one pass 4 steps
+// (Q load, pipeline fill, epilogue), a unit of a cluster-merged launch 4,
+// any other split unit 9 (its fp32 partial rows written out) and its merge
+// launch 3.5.  Ties go to fewer ranges (less partial traffic).
+void splitkv_shape(const Shape& s, int splits, int sms, int elem,
+                   int* out_splits, int* out_tiles) {
   const int tiles = (s.Skv + attn::cfg::kTN - 1) / attn::cfg::kTN;
   if (splits <= 0) {
-    // Pick the count with the shortest estimated critical path: waves of
-    // units over the SMs times (key tiles per range + a fixed per-unit cost
-    // of Q load, pipeline fill and epilogue, about kUnitTiles tiles), plus
-    // one tile's worth for the merge launch.  Ties go to fewer ranges (less
-    // partial traffic).
-    constexpr int kUnitTiles = 3;
     const long long units = grid_size(s);
+    const double kv_bytes = 2.0 * s.B * s.Hkv * static_cast<double>(s.Skv) *
+                            s.D * elem;
+    const long long floor2 =
+        static_cast<long long>(2.0 * kv_bytes / 7.0e6);
     long long best = -1;
     const int cap = std::max(1, std::min(tiles, kMaxSplits));
     for (int c = 1; c <= cap; ++c) {
+      const int per = (tiles + c - 1) / c;
+      if (c > 1 && (tiles + per - 1) / per != c) continue;  // not a count
       const long long waves = (units * c + sms - 1) / sms;
+      const bool cluster = c > 1 && pack_gqa(s) && c <= kMaxClusterSplits &&
+                           units * c <= sms;
+      const int unit2 = (c == 1 || cluster) ? 8 : 18;
+      const int merge2 = (c == 1 || cluster) ? 0 : 7;
       const long long cost =
-          waves * ((tiles + c - 1) / c + kUnitTiles) + (c > 1 ? 1 : 0);
+          std::max(waves * (2LL * per + unit2) + merge2, floor2);
       if (best < 0 || cost < best) {
         best = cost;
         splits = c;
@@ -517,7 +520,7 @@ attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
                              const void* V, void* O, float* LSE, float scale,
                              attn_dtype_t dtype, unsigned int* status, int sms,
                              int splits, int split_tiles, float* o_part,
-                             float* lse_part, unsigned long long* merge_ctr,
+                             float* lse_part,
                              cudaStream_t stream, float o_scale = 1.f,
                              unsigned long long timeout = 0,
                              int withhold_first_load = 0) {
@@ -569,8 +572,6 @@ attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
   p.split_tiles = split_tiles;
   p.o_part = o_part;
   p.lse_part = lse_part;
-  p.merge_ctr = merge_ctr;
-  p.merge_seq = merge_ctr != nullptr ? next_merge_seq() : 0u;
   p.num_units = static_cast<int>(grid_size(s) * splits);
   p.fd_splits = attn::make_fast_div(splits);
   p.fd_m_blocks = attn::make_fast_div(p.num_m_blocks);
@@ -581,6 +582,7 @@ attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
   // Packed split-KV whose units all fit in one wave: the key ranges of a
   // (batch, K/V head) run as one cluster and merge over distributed shared
   // memory.  (The workspace still has to be valid: it is the fallback.)
+  // Otherwise the merge is a second launch over the whole GPU.
   p.cluster_merge = pack && splits > 1 && splits <= kMaxClusterSplits &&
                     p.num_units <= sms && o_part != nullptr;
   p.status = status;
@@ -610,11 +612,13 @@ attn_status_t launch_forward(const Shape& s, const void* Q, const void* K,
   cudaError_t err = launch();
   if (err != cudaSuccess && p.cluster_merge) {
     // No cluster of that size could be placed: merge through the
-    // workspace and its counters instead.
+    // workspace instead.
     cudaGetLastError();
     p.cluster_merge = 0;
     err = launch();
   }
+  if (err == cudaSuccess && o_part != nullptr && !p.cluster_merge)
+    err = attn::launch_merge(s.D, dtype != ATTN_F16, p, sms, stream);
   return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -635,7 +639,7 @@ attn_status_t fwd_impl(const Shape& s, const void* Q, const void* K,
   if (st != ATTN_OK) return st;
   const int tiles = (s.Skv + attn::cfg::kTN - 1) / attn::cfg::kTN;
   return launch_forward(s, Q, K, V, O, LSE, scale, dtype, status, sms, 1,
-                        tiles, nullptr, nullptr, nullptr,
+                        tiles, nullptr, nullptr,
                         reinterpret_cast<cudaStream_t>(stream), 1.f, timeout,
                         withhold_first_load);
 }
@@ -661,7 +665,7 @@ attn_status_t splitkv_impl(const Shape& s, const void* Q, const void* K,
   st = check_call(s, scale, dtype, Q, K, V, O, LSE, &dev, &status, &sms);
   if (st != ATTN_OK) return st;
   int splits = 0, tiles = 0;
-  splitkv_shape(s, num_splits, sms, &splits, &tiles);
+  splitkv_shape(s, num_splits, sms, elem_bytes(dtype), &splits, &tiles);
   if (splits != num_splits) return ATTN_ERR_INVALID_ARG;  // not a planned count
   if (workspace == nullptr ||
       reinterpret_cast<uintptr_t>(workspace) % kWorkspaceAlign != 0)
@@ -671,14 +675,12 @@ attn_status_t splitkv_impl(const Shape& s, const void* Q, const void* K,
   const size_t rows = static_cast<size_t>(s.B) * s.Hq * s.Sq;
   const size_t o_bytes =
       round_up(static_cast<size_t>(splits) * rows * s.D * 4, kWorkspaceAlign);
-  const size_t lse_bytes =
-      round_up(static_cast<size_t>(splits) * rows * 4, kWorkspaceAlign);
   char* ws = static_cast<char*>(workspace);
-  // One launch: the forward kernel also merges the key ranges.
+  // The forward launch, then (unless its key ranges merge in clusters) the
+  // merge launch.
   return launch_forward(
       s, Q, K, V, O, LSE, scale, dtype, status, sms, splits, tiles,
       reinterpret_cast<float*>(ws), reinterpret_cast<float*>(ws + o_bytes),
-      reinterpret_cast<unsigned long long*>(ws + o_bytes + lse_bytes),
       reinterpret_cast<cudaStream_t>(stream), o_scale);
 }
 
@@ -708,7 +710,7 @@ attn_status_t fp8_impl(const Shape& s, const void* Q, const void* K,
   if (st != ATTN_OK) return st;
   const int tiles = (s.Skv + attn::cfg::kTN - 1) / attn::cfg::kTN;
   return launch_forward(s, Q, K, V, O, LSE, s_eff, ATTN_E4M3, status, sms, 1,
-                        tiles, nullptr, nullptr, nullptr,
+                        tiles, nullptr, nullptr,
                         reinterpret_cast<cudaStream_t>(stream), v_descale);
 }
 
@@ -870,7 +872,7 @@ attn_status_t attn_splitkv_plan(int B, int Hq, int Hkv, int Sq, int Skv, int D,
     if (sms <= 0) return ATTN_ERR_CUDA;
   }
   int splits = 0, tiles = 0;
-  splitkv_shape(s, *num_splits, sms, &splits, &tiles);
+  splitkv_shape(s, *num_splits, sms, elem_bytes(dtype), &splits, &tiles);
   *num_splits = splits;
   if (workspace_bytes != nullptr) *workspace_bytes = splitkv_bytes(s, splits);
   return ATTN_OK;
@@ -1021,7 +1023,8 @@ attn_status_t attn_dispatch(int B, int Hq, int Hkv, int Sq, int Skv, int D,
   const TileChoice t = choose_tiles(s, dtype);
   const bool pack = pack_gqa(s);
   int splits = 1, tiles = 0;
-  if (num_splits > 0) splitkv_shape(s, num_splits, 1, &splits, &tiles);
+  if (num_splits > 0)
+    splitkv_shape(s, num_splits, 1, elem_bytes(dtype), &splits, &tiles);
   const bool split = num_splits > 0;
   attn_dispatch_t d{};
   d.block_m = t.block_m;
@@ -1031,14 +1034,14 @@ attn_status_t attn_dispatch(int B, int Hq, int Hkv, int Sq, int Skv, int D,
   d.s_buffers = (!pack && s.D == 64) ? 3 : 2;
   d.stages = t.stages;
   d.order = (!pack && head_major(s)) ? 1 : 0;
+  // The current device's SM count (the GB300's 152 without a device).
+  int dev = -1, sms = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) sms = num_sms(dev);
+  cudaGetLastError();  // no device: not an error of the caller's
+  if (sms <= 0) sms = 152;
   if (!split && plannable(s)) {
     // The launch assigns causal units by a host-packed plan when one beats
-    // the zigzag rounds; the grid is the current device's SM count (the
-    // GB300's 152 without a device).
-    int dev = -1, sms = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess) sms = num_sms(dev);
-    cudaGetLastError();  // no device: not an error of the caller's
-    if (sms <= 0) sms = 152;
+    // the zigzag rounds; the grid is the SM count.
     const int units = static_cast<int>(grid_size(s));
     UnitPlan* plan = new UnitPlan;
     if (make_plan(s, units, std::min(units, sms), plan)) d.order = 2;
@@ -1049,6 +1052,11 @@ attn_status_t attn_dispatch(int B, int Hq, int Hkv, int Sq, int Skv, int D,
   d.num_splits = split ? splits : 0;
   d.units = static_cast<int>(grid_size(s) * splits);
   d.smem_bytes = t.smem_bytes;
+  d.merge = !split ? 0
+            : (pack && splits > 1 && splits <= kMaxClusterSplits &&
+               d.units <= sms)
+                ? 1
+                : 2;
   // Static names: D x element type x tile mode x order x O store.
   static const char* const kNames[2][3][3][3][2] = {
 #define ATTN_N(d, e, m, o, st) "d" d "." e "." m "." o "." st

@@ -81,16 +81,13 @@ struct FwdParams {
   int split_tiles;
   float* o_part;           // [num_splits, B*Hq, Sq, D]
   float* lse_part;         // [num_splits, B*Hq, Sq]
-  // Split-KV merge: one arrival counter per (row block, Q tile), tagged with
-  // this call's sequence number in the high 32 bits; the unit whose arrival
-  // completes the set merges the key ranges of that tile's rows into O/LSE.
-  unsigned long long* merge_ctr;  // [num_units / num_splits, 2]
-  unsigned int merge_seq;         // nonzero, distinct per call
   // Packed split-KV launch whose units all run at once, one per CTA, the
   // num_splits key ranges of a (batch, K/V head) forming one thread-block
   // cluster (rank = key range): each CTA keeps its partial results in its
   // own shared memory and rank 0 merges them over distributed shared
   // memory (no global partials, no counters).
+  // (Otherwise the key ranges are merged by a second launch on the same
+  // stream, attn_merge_kernel: this kernel only writes the partials.)
   int cluster_merge;
   // Divisors of the unit decode: num_splits, num_m_blocks, units per
   // m-block (B*Hq/2 paired, else B*Hq), heads per batch entry (Hq/2 paired,
@@ -289,143 +286,136 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   return w;
 }
 
-// Number of key ranges (split-KV) that reach Q tile t of unit w: ranges
-// before the unit's window or past the tile's causal horizon are never
-// visited.
-__device__ __forceinline__ int ranges_visited(const FwdParams& p,
-                                              const Unit& w, int t) {
-  const int hi = t ? w.hi[1] : w.hi[0];
-  return min(p.num_splits, (hi + p.split_tiles - 1) / p.split_tiles) -
-         w.lo / p.split_tiles;
-}
-
-// Counts this unit's arrival on a tile's merge counter; true for the
-// arrival that completes the expected set of this call.  A counter left by
-// an earlier call (another sequence number) restarts at one, so the
-// workspace needs no clearing.  The first CAS guesses that every other
-// range has arrived, so the arrival that completes the set usually needs
-// one round trip.  Lock-free: a CAS fails only when the guess was stale or
-// another arrival succeeded, so the loop ends within `expect` + 1 rounds;
-// the cap only guards against a corrupted counter.  Acquire-release: the
-// caller's CTA barrier orders its warpgroup's partial writes before this
-// operation, which publishes them; the completing arrival acquires all.
-__device__ __forceinline__ bool merge_arrive(unsigned long long* ctr,
-                                             unsigned int seq, int expect,
-                                             const FwdParams& p) {
-  unsigned long long cur = (static_cast<unsigned long long>(seq) << 32) |
-                           static_cast<unsigned int>(expect - 1);
-  for (int i = 0; i < (1 << 16); ++i) {
-    const unsigned int cnt =
-        static_cast<unsigned int>(cur >> 32) == seq
-            ? static_cast<unsigned int>(cur) + 1u
-            : 1u;
-    const unsigned long long nv =
-        (static_cast<unsigned long long>(seq) << 32) | cnt;
-    const unsigned long long prev = ptx::atom_cas_acq_rel_gpu(ctr, cur, nv);
-    if (prev == cur) return cnt == static_cast<unsigned int>(expect);
-    cur = prev;
-  }
-  atomicOr(p.status, 1u | (5u << 8));
-  return false;
-}
-
-// Split-KV merge of the rows of one Q tile by its 128 softmax threads
-// (index tid).  Key range c of a row contributes its normalised partial
-// output O_c and log-sum-exp lse_c; with M = max_c lse_c and
-// w_c = e^(lse_c - M),  O = sum_c w_c O_c / sum_c w_c  and
-// LSE = M + ln(sum_c w_c) -- the online-softmax rescale applied once more,
-// across ranges, here in its online form (a running maximum, the sums
+// Split-KV merge of query rows.  Key range c of a row contributes its
+// normalised partial output O_c and log-sum-exp lse_c; with
+// M = max_c lse_c and w_c = e^(lse_c - M),  O = sum_c w_c O_c / sum_c w_c
+// and LSE = M + ln(sum_c w_c) -- the online-softmax rescale applied once
+// more, across ranges, here in its online form (a running maximum, the sums
 // rescaled when it grows).  Ranges past a row's causal horizon or before
-// its window hold nothing for it and are not read.  Thread tid takes 4
-// columns of a row (the 32 or 16 threads of a row read its partials as
-// contiguous 512 or 256 bytes) and kRowBatch rows at once, whose loads of
-// one range are all in flight together: the merge is bound by L2 latency,
-// and one row at a time kept too few loads in flight.
-template <int D, bool kBF16, bool kPack, bool kWindow>
-__device__ __forceinline__ void merge_tile(const FwdParams& p, int plane0,
-                                           int m0, int tid) {
+// its window hold nothing for it and are not read.  A thread takes 4
+// columns (group cg) of kRowBatch rows (flat row index row[b] into
+// [B*Hq, Sq], position q_row[b] in the chunk; q_row < 0: no row) and reads
+// kRangeBatch ranges of them per round: the merge is bound by L2 latency,
+// so every load of a round is issued before the first is used.
+template <int D, bool kBF16, bool kWindow, int kRowBatch, int kRangeBatch>
+__device__ __forceinline__ void merge_rows(const FwdParams& p,
+                                           const long long (&row)[kRowBatch],
+                                           const int (&q_row)[kRowBatch],
+                                           int cg) {
   constexpr float kLog2e = 1.4426950408889634f;
-  constexpr int kGroups = D / 4;               // 4-column groups per row
-  constexpr int kRowsPerPass = cfg::kTM / kGroups;
-  constexpr int kRowBatch = 4;                 // rows per thread in flight
   const long long rows = static_cast<long long>(p.B) * p.Hq * p.Sq;
   const int split_keys = p.split_tiles * cfg::kTN;
-  const int nrows =
-      kPack ? p.group * p.Sq : min(cfg::kTM, p.Sq - m0);
-  const int cg = tid % kGroups;
-  for (int r0 = tid / kGroups; r0 < nrows; r0 += kRowsPerPass * kRowBatch) {
-    long long row[kRowBatch];
-    int c0[kRowBatch], ns[kRowBatch];
-    int cmin = p.num_splits, cmax = 0;
+  int c0[kRowBatch], ns[kRowBatch];
+  int cmin = p.num_splits, cmax = 0;
 #pragma unroll
-    for (int b = 0; b < kRowBatch; ++b) {
-      const int r = r0 + b * kRowsPerPass;
-      row[b] = 0;
-      c0[b] = 0;
-      ns[b] = 0;  // no range: the row is past the tile
-      if (r < nrows) {
-        int q_plane = plane0, q_row = m0 + r;
-        if constexpr (kPack) {
-          q_plane += r / p.Sq;
-          q_row = r % p.Sq;
-        }
-        row[b] = static_cast<long long>(q_plane) * p.Sq + q_row;
-        const int row_pos = p.input_pos + q_row;
-        const int vis_end = p.causal ? min(p.Skv, row_pos + 1) : p.Skv;
-        ns[b] = min(p.num_splits, (vis_end + split_keys - 1) / split_keys);
-        c0[b] = kWindow ? max(0, row_pos - p.window + 1) / split_keys : 0;
-        cmin = min(cmin, c0[b]);
-        cmax = max(cmax, ns[b]);
-      }
+  for (int b = 0; b < kRowBatch; ++b) {
+    c0[b] = 0;
+    ns[b] = 0;  // no range: not a row
+    if (q_row[b] >= 0) {
+      const int row_pos = p.input_pos + q_row[b];
+      const int vis_end = p.causal ? min(p.Skv, row_pos + 1) : p.Skv;
+      ns[b] = min(p.num_splits, (vis_end + split_keys - 1) / split_keys);
+      c0[b] = kWindow ? max(0, row_pos - p.window + 1) / split_keys : 0;
+      cmin = min(cmin, c0[b]);
+      cmax = max(cmax, ns[b]);
     }
-    float mx[kRowBatch], wsum[kRowBatch];
-    float4 acc[kRowBatch];
+  }
+  float mx[kRowBatch], wsum[kRowBatch];
+  float4 acc[kRowBatch];
 #pragma unroll
-    for (int b = 0; b < kRowBatch; ++b) {
-      mx[b] = -INFINITY;
-      wsum[b] = 0.f;
-      acc[b] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    for (int c = cmin; c < cmax; ++c) {
-      float lc[kRowBatch];
-      float4 xc[kRowBatch];
+  for (int b = 0; b < kRowBatch; ++b) {
+    mx[b] = -INFINITY;
+    wsum[b] = 0.f;
+    acc[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int cb = cmin; cb < cmax; cb += kRangeBatch) {
+    float lc[kRangeBatch][kRowBatch];
+    float4 xc[kRangeBatch][kRowBatch];
+#pragma unroll
+    for (int k = 0; k < kRangeBatch; ++k) {
+      const int c = cb + k;
 #pragma unroll
       for (int b = 0; b < kRowBatch; ++b) {
-        lc[b] = -INFINITY;
-        xc[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+        lc[k][b] = -INFINITY;
+        xc[k][b] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (c >= c0[b] && c < ns[b]) {
-          lc[b] = __ldcg(p.lse_part + c * rows + row[b]);
-          xc[b] = __ldcg(reinterpret_cast<const float4*>(
-                             p.o_part + (c * rows + row[b]) * D) +
-                         cg);
+          lc[k][b] = __ldcg(p.lse_part + c * rows + row[b]);
+          xc[k][b] = __ldcg(reinterpret_cast<const float4*>(
+                                p.o_part + (c * rows + row[b]) * D) +
+                            cg);
         }
       }
+    }
+#pragma unroll
+    for (int k = 0; k < kRangeBatch; ++k) {
 #pragma unroll
       for (int b = 0; b < kRowBatch; ++b) {
-        const float mn = fmaxf(mx[b], lc[b]);
+        const float mn = fmaxf(mx[b], lc[k][b]);
         if (mn == -INFINITY) continue;  // nothing seen yet
         const float a = ptx::ex2((mx[b] - mn) * kLog2e);  // 0 while mx = -inf
-        const float wc = ptx::ex2((lc[b] - mn) * kLog2e);
+        const float wc = ptx::ex2((lc[k][b] - mn) * kLog2e);
         wsum[b] = wsum[b] * a + wc;
-        acc[b].x = acc[b].x * a + wc * xc[b].x;
-        acc[b].y = acc[b].y * a + wc * xc[b].y;
-        acc[b].z = acc[b].z * a + wc * xc[b].z;
-        acc[b].w = acc[b].w * a + wc * xc[b].w;
+        acc[b].x = acc[b].x * a + wc * xc[k][b].x;
+        acc[b].y = acc[b].y * a + wc * xc[k][b].y;
+        acc[b].z = acc[b].z * a + wc * xc[k][b].z;
+        acc[b].w = acc[b].w * a + wc * xc[k][b].w;
         mx[b] = mn;
       }
     }
+  }
 #pragma unroll
-    for (int b = 0; b < kRowBatch; ++b) {
-      if (ns[b] == 0) continue;
-      const float inv = ptx::rcp(wsum[b]);
-      uint2 out;
-      out.x = ptx::pack2<kBF16>(acc[b].x * inv, acc[b].y * inv);
-      out.y = ptx::pack2<kBF16>(acc[b].z * inv, acc[b].w * inv);
-      reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.o) + row[b] * D)[cg] =
-          out;
-      if (cg == 0 && p.lse != nullptr)
-        p.lse[row[b]] = mx[b] + ptx::lg2(wsum[b]) * cfg::kLn2;
+  for (int b = 0; b < kRowBatch; ++b) {
+    if (ns[b] == 0) continue;
+    const float inv = ptx::rcp(wsum[b]);
+    uint2 out;
+    out.x = ptx::pack2<kBF16>(acc[b].x * inv, acc[b].y * inv);
+    out.y = ptx::pack2<kBF16>(acc[b].z * inv, acc[b].w * inv);
+    reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.o) + row[b] * D)[cg] =
+        out;
+    if (cg == 0 && p.lse != nullptr)
+      p.lse[row[b]] = mx[b] + ptx::lg2(wsum[b]) * cfg::kLn2;
+  }
+}
+
+// Split-KV merge as a launch of its own, after the forward kernel on the
+// same stream (programmatic dependent launch: its CTAs wait in
+// griddepcontrol.wait until the forward grid has completed).  The rows of
+// all (batch, head) planes in one flat range, spread over the whole GPU:
+// kMergeThreads threads take kMergeRowBatch rows of kMergeThreads / (D/4)
+// at a time per CTA, grid-stride.  (Merging inside the forward kernel, by
+// the unit whose arrival on a per-tile counter completed the set, put that
+// CTA's latency-bound reads of every range -- about 4.6 us per range of a
+// two-tile unit -- on each wave's critical path.)
+constexpr int kMergeThreads = 256;
+constexpr int kMergeRowBatch = 2;
+constexpr int kMergeRangeBatch = 4;
+template <int D>
+__host__ __device__ constexpr int merge_rows_per_cta() {
+  return kMergeThreads / (D / 4) * kMergeRowBatch;
+}
+
+template <int D, bool kBF16, bool kWindow>
+__global__ void __launch_bounds__(kMergeThreads)
+    attn_merge_kernel(const __grid_constant__ FwdParams p) {
+  ptx::griddep_wait();
+  constexpr int kGroups = D / 4;
+  constexpr int kRowsPerPass = kMergeThreads / kGroups;
+  const long long rows = static_cast<long long>(p.B) * p.Hq * p.Sq;
+  const int tid = threadIdx.x;
+  for (long long r0 = static_cast<long long>(blockIdx.x) *
+                          merge_rows_per_cta<D>() + tid / kGroups;
+       r0 < rows;
+       r0 += static_cast<long long>(gridDim.x) * merge_rows_per_cta<D>()) {
+    long long row[kMergeRowBatch];
+    int q_row[kMergeRowBatch];
+#pragma unroll
+    for (int b = 0; b < kMergeRowBatch; ++b) {
+      row[b] = r0 + b * kRowsPerPass;
+      q_row[b] = row[b] < rows ? static_cast<int>(row[b] % p.Sq) : -1;
+      if (q_row[b] < 0) row[b] = 0;
     }
+    merge_rows<D, kBF16, kWindow, kMergeRowBatch, kMergeRangeBatch>(
+        p, row, q_row, tid % kGroups);
   }
 }
 
@@ -519,9 +509,9 @@ __device__ __forceinline__ int units_of_cta(const FwdParams& p, int cta,
 // TMEM carry over from unit to unit, so the next unit's Q load and first
 // MMAs overlap the current unit's last MMAs and epilogue.
 // kPack: the query heads of a GQA group share tile 0 (few query rows).
-// kSplit: split-KV launch (o_part set) -- compiles the in-kernel merge of
-// the per-range partial results; the partial writes themselves follow
-// o_part at run time.
+// kSplit: split-KV launch (o_part set) -- each unit writes its key range's
+// partial results: into its shared memory for the cluster merge (packed
+// launches of one wave), else to o_part / lse_part for the merge launch.
 // kWindow: causal sliding window (window > 0) -- compiles the lower mask.
 // The variants keep each launch's softmax loop free of the others' code:
 // in one kernel with run-time switches the two-tile loop ran out of
@@ -576,6 +566,12 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
   const int u_step = static_cast<int>(gridDim.x);
   const int k_end = units_of_cta(p, u_first, u_step);  // units of this CTA
 
+  // The merge launch queued behind a split-KV launch may be scheduled as
+  // soon as every CTA has started (its CTAs only wait, for this grid's
+  // completion).
+  if constexpr (kSplit) {
+    if (!p.cluster_merge) ptx::griddep_launch_dependents();
+  }
   if constexpr (kPack) {
     // A packed Q load fills only group*Sq rows of the tile: keep the other
     // rows zero so their (discarded) scores stay finite.
@@ -1276,6 +1272,11 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
         // never comes lets the others' wait run out.  With the staged store
         // this barrier is also the first box's "buffer free" signal: the
         // storing thread arrives once TMA has read the previous box out.
+        // Split-KV tiles written to the workspace meet here too (the tile's
+        // partial rows then go out together); no named barrier follows
+        // them, but without the meeting the packed split variants compiled
+        // with register spills and the decode step took 3 % longer
+        // (same-box A/B).
         volatile int* in_ok = reinterpret_cast<volatile int*>(
             smem + L::kMiscOff + 16 + 16 * t);
         if (lane == 0) in_ok[warp % 4] = ok ? 1 : 0;
@@ -1418,26 +1419,6 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
             }
           }
           if (row_ok) p.lse_part[prow] = lse_row;
-        }
-      }
-      if (kSplit && !(kPack && p.cluster_merge)) {
-        // The unit that lands last among the key ranges of this tile's rows
-        // merges them (no second launch).  The warpgroup barrier orders all
-        // its partial writes before the counter update (a release at GPU
-        // scope); the completing update acquires the other units' partials,
-        // and the second barrier hands that on to the merging threads, which
-        // read through L2.
-        volatile int* merge_flag =
-            reinterpret_cast<volatile int*>(smem + L::kMiscOff + 8 + 4 * t);
-        ptx::named_barrier_sync(1 + t, kTM);
-        if (r == 0)
-          *merge_flag = merge_arrive(
-              p.merge_ctr + 2 * fast_div(u, p.fd_splits) + t, p.merge_seq,
-              ranges_visited(p, w, t), p);
-        ptx::named_barrier_sync(1 + t, kTM);
-        if (*merge_flag) {
-          merge_tile<D, kBF16, kPack, kWindow>(p, t ? w.plane[1] : w.plane[0],
-                                               m0, r);
         }
       }
       ptx::tc_fence_before();

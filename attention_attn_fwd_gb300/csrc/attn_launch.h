@@ -48,6 +48,13 @@ cudaError_t launch_fwd_d128_fp8_packed(const CUtensorMap& q,
                                        const CUtensorMap& o, const FwdParams& p, int grid,
                                        cudaStream_t stream);
 
+// Split-KV merge launch (attn_merge.cu): merges p's key-range partials
+// into p.o / p.lse for every query row; queued behind the forward kernel on
+// `stream` as a programmatic dependent launch.  `bf16`: O's element type
+// (bf16, else fp16).
+cudaError_t launch_merge(int D, bool bf16, const FwdParams& p, int sms,
+                         cudaStream_t stream);
+
 // Backward pass: row pass (D, lse2 into p.lse2 / p.delta), dK/dV kernel,
 // dQ kernel, in that order on `stream` (attn_bwd.cu).  `d` maps dO and `dq`
 // maps dQ like `q` maps Q (dQ is stored through it by TMA).

@@ -1,0 +1,53 @@
+// Launch of the split-KV merge kernel (attn_merge_kernel): the key ranges'
+// partial results of a split-KV forward launch merged into O and LSE by a
+// grid over all query rows, queued behind the forward kernel on the same
+// stream with programmatic serialization.
+#include <algorithm>
+
+#include "attn_launch.h"
+
+namespace attn {
+namespace {
+
+template <int D, bool kBF16, bool kWindow>
+cudaError_t launch_merge_variant(const FwdParams& p, int sms,
+                                 cudaStream_t stream) {
+  const long long rows = static_cast<long long>(p.B) * p.Hq * p.Sq;
+  const long long ctas =
+      (rows + merge_rows_per_cta<D>() - 1) / merge_rows_per_cta<D>();
+  // Grid-stride beyond 8 CTAs per SM (the merge kernel's residency).
+  const int grid = static_cast<int>(std::max<long long>(
+      1, std::min<long long>(ctas, 8LL * std::max(sms, 1))));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kMergeThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_merge_kernel<D, kBF16, kWindow>, p);
+}
+
+template <int D>
+cudaError_t launch_merge_d(bool bf16, const FwdParams& p, int sms,
+                           cudaStream_t stream) {
+  const bool window = p.window > 0;
+  if (bf16)
+    return window ? launch_merge_variant<D, true, true>(p, sms, stream)
+                  : launch_merge_variant<D, true, false>(p, sms, stream);
+  return window ? launch_merge_variant<D, false, true>(p, sms, stream)
+                : launch_merge_variant<D, false, false>(p, sms, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_merge(int D, bool bf16, const FwdParams& p, int sms,
+                         cudaStream_t stream) {
+  return D == 64 ? launch_merge_d<64>(bf16, p, sms, stream)
+                 : launch_merge_d<128>(bf16, p, sms, stream);
+}
+
+}  // namespace attn

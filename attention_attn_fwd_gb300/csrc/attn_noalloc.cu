@@ -77,8 +77,7 @@ attn_status_t attn_fwd_splitkv_noalloc(const void* Q, const void* K,
   st = scratch_address(&scratch);
   if (st != ATTN_OK) return st;
   // Every partial result the merge reads is written first by the forward
-  // kernel, and the merge counters carry a per-call tag (a counter left by
-  // an earlier call restarts), so the scratch needs no clearing between
+  // kernel of the same call, so the scratch needs no clearing between
   // calls.
   return attn_fwd_splitkv(Q, K, V, O, LSE, B, Hq, Hkv, Sq, Skv, D, scale,
                           causal, input_pos, dtype, splits, scratch,

@@ -139,6 +139,18 @@ __device__ __forceinline__ void bulk_wait_group_read_all() {
 }
 
 // Generic-proxy shared-memory writes -> visible to the async (TMA) proxy.
+// Programmatic dependent launch: launch_dependents lets a grid launched
+// after this one on the stream (with programmatic serialization) be
+// scheduled once every CTA of this grid has issued it or exited; wait, in
+// that dependent grid, returns once this grid has completed and its memory
+// operations are visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

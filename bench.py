@@ -441,7 +441,9 @@ DECODE_SETS = 4
 def run_decode(args, fp8=False):
     """Split-KV decode step: HBM-bound, reported in GB/s of algorithmic
     traffic (Q, K, V read once; O and LSE written once) against the measured
-    copy bandwidth.  One kernel per step (partials and their merge).
+    copy bandwidth.  One kernel per step when the key ranges merge inside
+    thread-block clusters (the automatic count here), else two (the forward
+    kernel and the merge kernel).
     ``fp8``: the same step with E4M3 Q/K/V (half the K/V bytes) through
     attn_fwd_fp8, bf16 O.
 
@@ -473,6 +475,11 @@ def run_decode(args, fp8=False):
                                               w.D, 1, w.input_pos, dt,
                                               args.splits)
     work = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    # Kernels per step: the forward kernel, plus the merge kernel unless
+    # the key ranges merge inside clusters.
+    kernels = 2 if attn.attn_dispatch(
+        w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, 1, w.input_pos, dt,
+        num_splits=splits)["merge"] == 2 else 1
 
     def step(i):
         q, k, v, o, lse = sets[i % DECODE_SETS]
@@ -545,7 +552,7 @@ def run_decode(args, fp8=False):
                      "unit": "GB/s", "frac": round(gbs / hbm, 4),
                      "peak_source": "%s copy bandwidth" % src,
                      "traffic": None},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * kernels,
         "clocks": clocks.summary(),
     }
     if rank == 0:

@@ -125,13 +125,15 @@ attn_status_t attn_fwd_window(const void* Q, const void* K, const void* V,
  * workspace        device memory owned by the caller, 256-byte aligned,
  *                  of at least the size attn_splitkv_plan reports: fp32
  *                  partial outputs [num_splits, B, Hq, Sq, D], fp32
- *                  partial LSEs [num_splits, B, Hq, Sq], then 64-bit
- *                  merge counters; its contents need no initialisation
- *                  (each call tags its counter updates with a number of
- *                  its own);
+ *                  partial LSEs [num_splits, B, Hq, Sq]; its contents
+ *                  need no initialisation (every value read is written
+ *                  first by the same call);
  * workspace_bytes  its size.
- * One kernel is enqueued on `stream`: the unit that finishes a row block's
- * last key range merges that row block.  The workspace must not be used by
+ * Enqueued on `stream`: the forward kernel, and unless its key ranges merge
+ * inside thread-block clusters (GQA-packed launches whose units all run at
+ * once, at most 8 ranges), a merge kernel after it (a programmatic
+ * dependent launch: its blocks start once every forward block has and wait
+ * for the forward grid to complete).  The workspace must not be used by
  * another call until this one has run.
  */
 attn_status_t attn_fwd_splitkv(const void* Q, const void* K, const void* V,
@@ -302,8 +304,7 @@ attn_status_t attn_device_status(unsigned int* code);
  * per device, shared by every stream and call, so a wait that ran out in a
  * kernel of another stream, finished before the read, is reported here too;
  * bits 8-15 name the role that gave up (in the forward kernel 1 producer,
- * 2 MMA issuer, 3 softmax, 4 epilogue, 5 split-KV merge; OR-ed when
- * several gave up).  Not for use while `stream` is being captured.  code
+ * 2 MMA issuer, 3 softmax, 4 epilogue; OR-ed when several gave up).  Not for use while `stream` is being captured.  code
  * may be NULL.
  */
 attn_status_t attn_stream_status(attn_stream_t stream, unsigned int* code);
@@ -377,12 +378,17 @@ attn_status_t attn_tile_config(int B, int Hq, int Hkv, int Sq, int Skv, int D,
  * persistent CTAs), stages the K/V tiles in flight, smem_bytes the dynamic
  * shared memory per CTA.  name is a static string naming the entry.
  * num_splits: 0 for the one-pass forward, else as attn_fwd_splitkv
- * (planned count; units then count (rows, key range) pairs).  Returns the
+ * (planned count; units then count (rows, key range) pairs).  merge: how
+ * the key ranges are merged -- 0 no split; 1 inside the forward kernel,
+ * the ranges of a K/V group forming one thread-block cluster (packed tiles,
+ * units <= SM count, at most 8 ranges; one kernel per call); 2 by a merge
+ * kernel enqueued after the forward kernel (two kernels per call).  The
+ * SM count is the current device's (152 without one).  Returns the
  * validation code the call would; out must be non-NULL.
  */
 typedef struct {
   int block_m, block_n, q_tiles, paired, s_buffers, stages;
-  int order, o_store, hold_scores, num_splits, units, smem_bytes;
+  int order, o_store, hold_scores, num_splits, units, smem_bytes, merge;
   const char* name;
 } attn_dispatch_t;
 

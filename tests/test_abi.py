@@ -120,11 +120,9 @@ def test_splitkv_plan_host_only(lib):
                                     attn.ATTN_BF16, 5)
     assert ns == 4           # 8 tiles in 5 requested ranges: 2 tiles each
     rows = 2 * 8 * 1
-    # Packed GQA: one row block per (batch, K/V head), two counters each.
-    counters = 2 * 2 * 2
+    # fp32 partial outputs, then fp32 partial LSEs, each 256-byte aligned.
     assert ws == (-(-(ns * rows * 128 * 4) // 256) * 256 +
-                  -(-(ns * rows * 4) // 256) * 256 +
-                  -(-(counters * 8) // 256) * 256)
+                  -(-(ns * rows * 4) // 256) * 256)
     ns1, _ = attn.attn_splitkv_plan(1, 2, 2, 4, 100, 64, 0, 0,
                                     attn.ATTN_F16, 8)
     assert ns1 == 1          # 100 keys: a single tile
@@ -272,6 +270,17 @@ def test_dispatch_entries_host_only(lib):
     assert e["name"] == "d128.bf16.gqa-packed.lpt.rows"
     assert e["q_tiles"] == 1 and e["num_splits"] == 2
     assert e["units"] == 8 * 8 * 2 and e["block_m"] == 4
+    # Merge modes: the decode's 128 units fit the SMs, 2 ranges per
+    # cluster; 4 ranges are 256 units (more than the 152 SMs),
+    # and unpacked tiles always merge in the second kernel.
+    assert e["merge"] == 1
+    e = attn.attn_dispatch(8, 32, 8, 1, 4096, 128, 1, 4095, bf, num_splits=4)
+    assert e["merge"] == 2 and e["units"] == 8 * 8 * 4
+    e = attn.attn_dispatch(1, 8, 8, 256, 32768, 128, 1, 32512, bf,
+                           num_splits=8)
+    assert e["merge"] == 2 and e["q_tiles"] == 2
+    assert attn.attn_dispatch(1, 8, 8, 256, 32768, 128, 1, 32512,
+                              bf)["merge"] == 0
     e = attn.attn_dispatch(1, 32, 4, 8192, 8192, 128, 1, 0, e4)
     assert e["name"] == "d128.e4m3.paired-heads.plan.tma"
     # window entry: causal, LPT order

@@ -157,13 +157,13 @@ def test_workspace_contents_and_reuse(fill):
 
 @pytest.mark.parametrize("w, splits", [
     # 40 x 8 (batch, K/V head) groups x 2 ranges: more units than SMs, so
-    # the key ranges merge through the workspace and its counters.
+    # the key ranges merge through the workspace in the merge launch.
     (W("many_groups", 40, 32, 8, 1, 700, 128, "bf16", True, 699), 2),
     # 2 groups x 8 ranges: every unit runs at once, each group's 8 ranges
     # form one thread-block cluster and merge over its shared memory.
     (W("cluster_of_8", 1, 8, 2, 1, 4000, 128, "f16", True, 3999), 8),
     (W("cluster_window", 2, 8, 2, 3, 3000, 64, "bf16", True, 2997), 4),
-], ids=["counter_merge", "cluster_merge_8", "cluster_merge_window"])
+], ids=["merge_launch", "cluster_merge_8", "cluster_merge_window"])
 def test_merge_paths_against_oracle(w, splits):
     """Both ways of merging the key ranges of packed split-KV tiles."""
     q, k, v = make_qkv(w, seed=31)
@@ -179,3 +179,50 @@ def test_merge_paths_against_oracle(w, splits):
         TOL_O[w.dtype]
     assert float(np.max(np.abs(lse.double().cpu().numpy() - lse_ref))) <= \
         TOL_LSE
+
+
+@pytest.mark.parametrize("w, splits, window", [
+    # 2 x 8 heads x 2 row blocks of 256 x 16 ranges = 512 units: four waves
+    # of units on 152 SMs, each row merged from 16 ranges.
+    (W("merge_waves", 2, 8, 8, 300, 4096, 128, "bf16", True, 3796), 16, 0),
+    # paired heads, D = 64, f16, a window: rows skip the ranges before it.
+    (W("merge_window_d64", 1, 4, 2, 200, 3000, 64, "f16", True, 2800), 6,
+     1000),
+    # one head, 32 ranges of one tile each, rows of a ragged last block.
+    (W("merge_32_ranges", 1, 1, 1, 70, 4000, 128, "f16", True, 3930), 32, 0),
+], ids=lambda x: x.name if isinstance(x, Workload) else str(x))
+def test_merge_launch_against_oracle(w, splits, window):
+    """The merge launch (split-KV launches not merged in a cluster): many
+    waves, many ranges, windows; sampled rows against the oracle."""
+    q, k, v = make_qkv(w, seed=33)
+    o, lse = attn.fwd_splitkv(q.cuda(), k.cuda(), v.cuda(), scale=w.scale,
+                              causal=True, input_pos=w.input_pos,
+                              num_splits=splits, window=window)
+    torch.cuda.synchronize()
+    assert attn.attn_device_status() == (0, 0)
+    rows = sample_rows(w, min(96, w.B * w.Hq * w.Sq), seed=4)
+    o_ref, lse_ref = oracle.attention_rows(q, k, v, w.scale, True,
+                                           w.input_pos, rows, window)
+    idx = torch.from_numpy(rows).cuda()
+    o_rows = o[idx[:, 0], idx[:, 1], idx[:, 2]].double().cpu().numpy()
+    l_rows = lse[idx[:, 0], idx[:, 1], idx[:, 2]].double().cpu().numpy()
+    assert float(np.max(np.abs(o_rows - o_ref))) <= TOL_O[w.dtype]
+    assert float(np.max(np.abs(l_rows - lse_ref))) <= TOL_LSE
+
+
+@pytest.mark.parametrize("shape, expect", [
+    ((8, 32, 8, 1, 4096, 128, 1, 4095), 2),          # decode: clusters of 2
+    ((4, 32, 8, 16, 16384, 128, 1, 16368), 4),       # packed chunk: clusters
+    ((1, 32, 8, 512, 32768, 128, 1, 32256), 2),      # one wave of 128 units
+    ((2, 16, 16, 1024, 16384, 128, 1, 15360), 1),    # one pass fills the GPU
+    ((1, 8, 8, 128, 131072, 128, 1, 130944), 16),    # bound by K/V streaming
+    ((1, 8, 8, 256, 32768, 128, 1, 32512), 19),      # one wave of 152 units
+])
+def test_plan_picks_on_gb300(shape, expect):
+    """The automatic split count on a 152-SM GB300 for shapes whose timings
+    over 1-32 ranges fitted the planner's costs (best or within 5 % of the
+    best measured count)."""
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("planner picks are stated for 152 SMs")
+    ns, _ = attn.attn_splitkv_plan(*shape, attn.ATTN_BF16, 0)
+    assert ns == expect

@@ -61,8 +61,8 @@ CHUNK = Workload("noalloc_chunk", 1, 8, 2, 96, 1500, 64, "f16", True, 1404)
 def test_consecutive_calls_match_workspace_call_and_oracle():
     assert attn.attn_noalloc_scratch_bytes() >= 1 << 20
     # The same shape twice with new inputs (the second call finds the
-    # first call's partials and tagged merge counters in the scratch), then
-    # another shape and split count.
+    # first call's partials in the scratch), then another shape and split
+    # count.
     calls = [(DECODE, 0, 40), (DECODE, 0, 41), (CHUNK, planned(CHUNK, 5), 42)]
     for w, splits, seed in calls:
         ns = planned(w, splits)
