@@ -1397,6 +1397,46 @@ __global__ void __launch_bounds__(cfg::kThreads, 1)
             }
           }
           if (row_ok) ptx::st_shared_f32(part + kTM * D * 4 + 4 * r, lse_row);
+        } else if constexpr (!kPack) {
+          // Through this warp's quarter of the tile's staging box: each
+          // thread writes a 32-column slice of its row (128 bytes, chunk c
+          // of row i at c ^ (i % 8), so 8 threads of a phase cover every
+          // bank), then the warp stores 4 rows x 128 bytes per instruction
+          // -- whole lines, where per-thread row stores touch 32 lines per
+          // instruction.  Only this warp uses its quarter.
+          const uint32_t wbuf = s_base + L::kStageOff +
+                                t * L::kStageTileBytes + (warp % 4) * 4096;
+          const long long plane_row0 =
+              (static_cast<long long>(w.split) * p.B * p.Hq + q_plane) *
+              p.Sq;
+          const int wrow0 = m0 + 32 * (warp % 4);  // the warp's first row
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t o[32];
+            ptx::tmem_ld32(t_o + 32 * q, o);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              ptx::st_shared_v4(
+                  wbuf + lane * 128 + ((c ^ (lane % 8)) << 4),
+                  __float_as_uint(__uint_as_float(o[4 * c]) * inv_l),
+                  __float_as_uint(__uint_as_float(o[4 * c + 1]) * inv_l),
+                  __float_as_uint(__uint_as_float(o[4 * c + 2]) * inv_l),
+                  __float_as_uint(__uint_as_float(o[4 * c + 3]) * inv_l));
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int rr = 4 * i + lane / 8, c = lane % 8;
+              const uint4 v =
+                  ptx::ld_shared_v4(wbuf + rr * 128 + ((c ^ (rr % 8)) << 4));
+              if (wrow0 + rr < p.Sq)
+                *reinterpret_cast<uint4*>(
+                    p.o_part + (plane_row0 + wrow0 + rr) * D + 32 * q +
+                    4 * c) = v;
+            }
+            __syncwarp();
+          }
+          if (row_ok) p.lse_part[plane_row0 + q_row] = lse_row;
         } else {
           const long long prow =
               (static_cast<long long>(w.split) * p.B * p.Hq + q_plane) *

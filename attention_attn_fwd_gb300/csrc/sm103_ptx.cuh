@@ -168,6 +168,15 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a,
                : "memory");
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 // ---------------------------------------------------- thread-block cluster
 // Cluster-wide barrier (every thread of every CTA of the cluster): arrive
 // with release semantics, wait with acquire semantics, so shared-memory
