@@ -22,7 +22,7 @@ SOURCES = ["attn_api.cu", "attn_fwd_d64.cu", "attn_fwd_d128.cu",
            "attn_noalloc.cu", "attn_bwd.cu", "attn_merge.cu"]
 HEADERS = ["attn_fwd_kernel.cuh", "attn_fwd_launch.cuh", "attn_sync.cuh",
            "fast_div.h",
-           "attn_bwd_kernel.cuh",
+           "attn_bwd_kernel.cuh", "attn_merge_kernel.cuh",
            "sm103_ptx.cuh", "attn_launch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

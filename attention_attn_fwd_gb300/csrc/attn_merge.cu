@@ -5,17 +5,15 @@
 #include <algorithm>
 
 #include "attn_launch.h"
+#include "attn_merge_kernel.cuh"
 
 namespace attn {
 namespace {
 
-template <int D, bool kBF16, bool kWindow>
-cudaError_t launch_merge_variant(const FwdParams& p, int sms,
-                                 cudaStream_t stream) {
-  const long long rows = static_cast<long long>(p.B) * p.Hq * p.Sq;
-  const long long ctas =
-      (rows + merge_rows_per_cta<D>() - 1) / merge_rows_per_cta<D>();
-  // Grid-stride beyond 8 CTAs per SM (the merge kernel's residency).
+template <int D, bool kBF16, bool kWindow, int kRowBatch>
+cudaError_t launch_merge_rows(const FwdParams& p, int sms, long long ctas,
+                              cudaStream_t stream) {
+  // Grid-stride beyond 8 CTAs per SM.
   const int grid = static_cast<int>(std::max<long long>(
       1, std::min<long long>(ctas, 8LL * std::max(sms, 1))));
   cudaLaunchConfig_t cfg = {};
@@ -28,7 +26,23 @@ cudaError_t launch_merge_variant(const FwdParams& p, int sms,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_merge_kernel<D, kBF16, kWindow>, p);
+  return cudaLaunchKernelEx(&cfg,
+                            attn_merge_kernel<D, kBF16, kWindow, kRowBatch>,
+                            p);
+}
+
+// Two rows per thread when that still gives every SM two CTAs, else one.
+template <int D, bool kBF16, bool kWindow>
+cudaError_t launch_merge_variant(const FwdParams& p, int sms,
+                                 cudaStream_t stream) {
+  const long long rows = static_cast<long long>(p.B) * p.Hq * p.Sq;
+  constexpr int kRows2 = merge_rows_per_cta<D, 2>();
+  constexpr int kRows1 = merge_rows_per_cta<D, 1>();
+  const long long ctas2 = (rows + kRows2 - 1) / kRows2;
+  if (ctas2 >= 2LL * std::max(sms, 1))
+    return launch_merge_rows<D, kBF16, kWindow, 2>(p, sms, ctas2, stream);
+  return launch_merge_rows<D, kBF16, kWindow, 1>(
+      p, sms, (rows + kRows1 - 1) / kRows1, stream);
 }
 
 template <int D>

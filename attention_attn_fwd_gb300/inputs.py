@@ -102,6 +102,19 @@ DECODE = Workload("decode_B8_Hq32_Hkv8_Sq1_pos4095_Skv4096_D128_bf16",
                   8, 32, 8, 1, 4096, 128, "bf16", True, 4095)
 
 
+# Chunks of a few hundred query rows per head against long KV caches (the
+# last rows of the cache): few units per head, so the split-KV path spreads
+# the keys over the SMs.
+LONG_KEY_CHUNKS = [
+    Workload("chunk_B1_H8_Sq256_pos32512_Skv32768_D128_bf16",
+             1, 8, 8, 256, 32768, 128, "bf16", True, 32512),
+    Workload("chunk_B1_H8_Sq128_pos130944_Skv131072_D128_bf16",
+             1, 8, 8, 128, 131072, 128, "bf16", True, 130944),
+    Workload("chunk_B1_Hq32_Hkv8_Sq512_pos32256_Skv32768_D128_bf16",
+             1, 32, 8, 512, 32768, 128, "bf16", True, 32256),
+]
+
+
 def sweep():
     """B=4, H=16 non-causal sweep over S, D and dtype."""
     out = []

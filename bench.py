@@ -721,6 +721,128 @@ def run_table(args):
         print(json.dumps(out), flush=True)
 
 
+# ------------------------------------------------- split-KV, long key ranges
+def run_splitkv_long(args):
+    """Chunks of a few hundred query rows against long KV caches, through
+    attn_fwd_splitkv at the count attn_splitkv_plan picks and through the
+    one-pass attn_fwd, L2 flushed before each call, CUDA events around
+    each (the split call's events enclose its forward and merge kernels).
+    Each row's roofline bound is the larger of streaming Q, K, V and O once
+    at the measured copy bandwidth and its exact visible FLOPs at the
+    measured bf16 peak; `value` is the summed split time (lower is better),
+    `roofline` the summed bounds over it."""
+    import torch
+
+    import attention_attn_fwd_gb300 as attn
+    from attention_attn_fwd_gb300.inputs import LONG_KEY_CHUNKS, make_qkv
+
+    ws, rank, local = dist_info()
+    if ws > 1:
+        torch.cuda.set_device(local)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    peak, hbm, src = peaks()
+    rows, launches, t_total, b_total = [], 0, 0.0, 0.0
+    with ClockSampler(dev.index) as clocks:
+        for w in LONG_KEY_CHUNKS:
+            q, k, v = (t.to(dev) for t in make_qkv(w, seed=0))
+            o = torch.empty_like(q)
+            lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32,
+                              device=dev)
+            dt = attn.ATTN_BF16
+            splits, ws_bytes = attn.attn_splitkv_plan(
+                w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, 1, w.input_pos, dt, 0)
+            work = torch.empty(max(ws_bytes, 1), dtype=torch.uint8,
+                               device=dev)
+            kernels = 2 if attn.attn_dispatch(
+                w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, 1, w.input_pos, dt,
+                num_splits=splits)["merge"] == 2 else 1
+            args_ = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                     lse.data_ptr(), w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D,
+                     w.scale, 1, w.input_pos, dt)
+
+            def split_step():
+                st = attn.attn_fwd_splitkv(*args_, splits, work.data_ptr(),
+                                           ws_bytes, stream.cuda_stream)
+                if st != attn.ATTN_OK:
+                    raise RuntimeError("attn_fwd_splitkv: " +
+                                       attn.attn_status_string(st))
+
+            def one_pass():
+                st = attn.attn_fwd(*args_, stream.cuda_stream)
+                if st != attn.ATTN_OK:
+                    raise RuntimeError("attn_fwd: " +
+                                       attn.attn_status_string(st))
+
+            med = {}
+            for name, fn in (("split", split_step), ("one_pass", one_pass)):
+                for _ in range(args.warmup):
+                    flush.fill_(1.0)
+                    fn()
+                torch.cuda.synchronize()
+                ev = [(torch.cuda.Event(enable_timing=True),
+                       torch.cuda.Event(enable_timing=True))
+                      for _ in range(args.steps)]
+                for i, (a_, b_) in enumerate(ev):
+                    flush.fill_(float(i))
+                    a_.record(stream)
+                    fn()
+                    b_.record(stream)
+                torch.cuda.synchronize()
+                t = sorted(a_.elapsed_time(b_) for a_, b_ in ev)
+                med[name] = t[len(t) // 2]
+            io_bytes = w.io_bytes()
+            hbm_us = io_bytes / (hbm * 1e9) * 1e6
+            tensor_us = w.exact_flops() / (peak * 1e12) * 1e6
+            bound_us = max(hbm_us, tensor_us)
+            us = 1000 * med["split"]
+            t_total += us
+            b_total += bound_us
+            launches += args.steps * (kernels + 1)
+            rows.append({
+                "workload": w.name, "num_splits": splits,
+                "kernels_per_call": kernels,
+                "us_split": round(us, 2),
+                "us_one_pass": round(1000 * med["one_pass"], 2),
+                "speedup": round(med["one_pass"] / med["split"], 2),
+                "bound": "hbm" if hbm_us >= tensor_us else "tensor",
+                "bound_us": round(bound_us, 2),
+                "frac": round(bound_us / us, 4),
+                "GB/s": round(io_bytes / (us * 1e-6) / 1e9, 1),
+                "tflops_exact": round(w.exact_flops() / (us * 1e-6) / 1e12,
+                                      1)})
+            del q, k, v, o, lse, work
+    st, code = attn.attn_device_status()
+    if st != attn.ATTN_OK:
+        raise RuntimeError("device status %d code %#x" % (st, code))
+    out = {
+        "metric": "split-KV time summed over long-key chunks (median call "
+                  "at the planned range count)",
+        "value": round(t_total, 2), "unit": "us", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: Q/K/V ~ N(0,1) from a seeded CPU generator",
+        "config": {"workload": "long-key chunks (%s)" % ", ".join(
+                       w.name for w in LONG_KEY_CHUNKS),
+                   "l2": "flushed before each call (256 MiB write, "
+                         "untimed)"},
+        "roofline": {"bound": "per row (hbm or tensor)",
+                     "achieved_us": round(t_total, 2),
+                     "bound_us": round(b_total, 2),
+                     "frac": round(b_total / t_total, 4),
+                     "peak_source": "%s copy bandwidth and bf16 dense burst"
+                                    % src,
+                     "traffic": None},
+        "table": rows,
+        "gpu_launches": launches,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
 # ------------------------------------------------------------ FP8 forward
 def run_fp8(args):
     """The headline GQA 8k causal forward with E4M3 Q/K/V (descale 1) and a
@@ -889,14 +1011,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload",
                     choices=["gqa8k", "decode", "window", "bwd", "fp8",
-                             "decode_fp8", "table"],
+                             "decode_fp8", "table", "splitkv_long"],
                     default="gqa8k",
                     help="gqa8k: the headline causal GQA forward (default); "
                          "decode: the split-KV decode step; window: causal "
                          "GQA 32k with a 4096-key sliding window; bwd: the "
                          "backward pass of gqa8k; fp8: gqa8k with E4M3 "
                          "inputs; decode_fp8: decode with E4M3 inputs; "
-                         "table: every named forward workload, one row each")
+                         "table: every named forward workload, one row each; "
+                         "splitkv_long: split-KV against one pass on chunks "
+                         "of few query rows over long key ranges")
     ap.add_argument("--splits", type=int, default=0,
                     help="split count for --workload decode (0: automatic)")
     args = ap.parse_args()
@@ -914,6 +1038,8 @@ def main():
         run_window(args)
     elif args.workload == "bwd":
         run_bwd(args)
+    elif args.workload == "splitkv_long":
+        run_splitkv_long(args)
     elif args.workload == "table":
         run_table(args)
     else:
