@@ -866,10 +866,11 @@ attn_status_t attn_splitkv_plan(int B, int Hq, int Hkv, int Sq, int Skv, int D,
   if (num_splits == nullptr) return ATTN_ERR_INVALID_ARG;
   int sms = 0;
   if (*num_splits <= 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
-    sms = num_sms(dev);
-    if (sms <= 0) return ATTN_ERR_CUDA;
+    // The current device's SM count (the GB300's 152 without a device).
+    int dev = -1;
+    if (cudaGetDevice(&dev) == cudaSuccess) sms = num_sms(dev);
+    cudaGetLastError();  // no device: not an error of the caller's
+    if (sms <= 0) sms = 152;
   }
   int splits = 0, tiles = 0;
   splitkv_shape(s, *num_splits, sms, elem_bytes(dtype), &splits, &tiles);

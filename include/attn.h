@@ -196,10 +196,13 @@ attn_status_t attn_fwd_fp8(const void* Q, const void* K, const void* V,
 
 /*
  * attn_splitkv_plan — split count and workspace size for attn_fwd_splitkv.
- * *num_splits in: the requested count, or <= 0 to choose one that gives
- * every SM of the current device work (this form needs a CUDA device); out:
- * the count attn_fwd_splitkv accepts (requests are clamped to the number of
- * 128-key tiles, and trailing empty ranges are dropped).
+ * *num_splits in: the requested count, or <= 0 to choose the count with
+ * the shortest estimated time on the current device's SMs (152, a GB300's,
+ * when the calling thread has no CUDA device): waves of units times key
+ * tiles per range plus fixed per-unit and merge costs, bounded below by
+ * streaming K and V once from HBM; out: the count attn_fwd_splitkv accepts
+ * (requests are clamped to the number of 128-key tiles, and trailing empty
+ * ranges are dropped).  Host only: launches nothing.
  * *workspace_bytes (may be NULL) receives the workspace size.
  */
 attn_status_t attn_splitkv_plan(int B, int Hq, int Hkv, int Sq, int Skv, int D,

@@ -130,6 +130,32 @@ def test_splitkv_plan_host_only(lib):
         attn.attn_splitkv_plan(1, 3, 2, 4, 100, 64, 0, 0, attn.ATTN_F16, 2)
 
 
+# (B, Hq, Hkv, Sq, Skv, D, causal, input_pos) and the automatic split count
+# on 152 SMs; each was the best or within 5 % of the best measured count on
+# a GB300 over 1-32 ranges (bf16).
+PLAN_PICKS = [
+    ((8, 32, 8, 1, 4096, 128, 1, 4095), 2),          # decode: clusters of 2
+    ((4, 32, 8, 16, 16384, 128, 1, 16368), 4),       # packed chunk: clusters
+    ((1, 32, 8, 512, 32768, 128, 1, 32256), 2),      # one wave of 128 units
+    ((2, 16, 16, 1024, 16384, 128, 1, 15360), 1),    # one pass fills the GPU
+    ((1, 8, 8, 128, 131072, 128, 1, 130944), 16),    # bound by K/V streaming
+    ((1, 8, 8, 256, 32768, 128, 1, 32512), 19),      # one wave of 152 units
+    ((1, 16, 16, 256, 32768, 64, 1, 32512), 9),      # D = 64, one wave
+]
+
+
+@pytest.mark.parametrize("shape, expect", PLAN_PICKS)
+def test_splitkv_plan_auto_host(lib, shape, expect):
+    """The automatic count is planned on the host (152 SMs without a
+    device), and only counts attn_fwd_splitkv accepts come out."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: the device's SM count applies")
+    ns, ws = attn.attn_splitkv_plan(*shape, attn.ATTN_BF16, 0)
+    assert ns == expect
+    assert attn.attn_splitkv_plan(*shape, attn.ATTN_BF16, ns) == (ns, ws)
+
+
 def test_splitkv_argument_checks(lib):
     a = dict(Q=BAD, K=BAD + 0x100000, V=BAD + 0x200000, O=BAD + 0x300000,
              LSE=0, B=1, Hq=2, Hkv=2, Sq=1, Skv=1000, D=128, scale=0.1,

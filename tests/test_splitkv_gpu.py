@@ -8,6 +8,7 @@ import attention_attn_fwd_gb300 as attn
 import oracle
 from attention_attn_fwd_gb300.inputs import PREFILL_CHUNK, Workload, make_qkv
 from tests.gpu_parity import TOL_LSE, TOL_O, sample_rows
+from tests.test_abi import PLAN_PICKS
 
 pytestmark = pytest.mark.gpu
 
@@ -210,14 +211,7 @@ def test_merge_launch_against_oracle(w, splits, window):
     assert float(np.max(np.abs(l_rows - lse_ref))) <= TOL_LSE
 
 
-@pytest.mark.parametrize("shape, expect", [
-    ((8, 32, 8, 1, 4096, 128, 1, 4095), 2),          # decode: clusters of 2
-    ((4, 32, 8, 16, 16384, 128, 1, 16368), 4),       # packed chunk: clusters
-    ((1, 32, 8, 512, 32768, 128, 1, 32256), 2),      # one wave of 128 units
-    ((2, 16, 16, 1024, 16384, 128, 1, 15360), 1),    # one pass fills the GPU
-    ((1, 8, 8, 128, 131072, 128, 1, 130944), 16),    # bound by K/V streaming
-    ((1, 8, 8, 256, 32768, 128, 1, 32512), 19),      # one wave of 152 units
-])
+@pytest.mark.parametrize("shape, expect", PLAN_PICKS)
 def test_plan_picks_on_gb300(shape, expect):
     """The automatic split count on a 152-SM GB300 for shapes whose timings
     over 1-32 ranges fitted the planner's costs (best or within 5 % of the
