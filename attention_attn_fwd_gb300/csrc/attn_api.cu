@@ -5,7 +5,6 @@
 #include <cstdint>
 #include <algorithm>
 #include <vector>
-#include <atomic>
 #include <cstddef>
 #include <cstdlib>
 #include <mutex>
